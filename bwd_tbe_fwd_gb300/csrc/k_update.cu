@@ -1,0 +1,596 @@
+// k_update.cu -- run classification and the per-row optimizer update.
+//
+// "Modernizing Table Batched Embeddings with FBTriton":
+//   section 3: runs are routed by segment length (SL): a short run (SL < 256) is owned start to
+//     finish by one program (gather, accumulate in registers, optimizer, plain store, no
+//     atomics); a long run (SL >= 256) is split into 256-lookup chunks whose partial sums meet
+//     in a workspace, after which either a second kernel applies the optimizer or, in one
+//     launch, the chunk that sees a countdown reach one applies it after a device-scope fence;
+//     weighted tables scale each gradient row by its per-sample weight before accumulating.
+//   section 4, Problems 3 and 4: short runs are bucketed by next_pow2(D) so each bucket launches
+//     with its own width; the classification runs on the device with one atomic per block per
+//     list (block counts, one atomicAdd, intra-block offsets), and the consumers read the counts
+//     from device memory, so the host never synchronizes.
+//   The row-wise Adagrad rule follows "Table-Batched Embeddings in Triton", section 5.
+//
+// GB300 design:
+//   classify   grid-stride over runs; per block, shared-memory counters per list, then one
+//              global atomicAdd per non-empty list (and one for chunk descriptors); long runs
+//              also get their countdown and a zeroed fp32 workspace row.
+//   short run  one group of min(32, D/4) lanes per run (so a warp holds 32/group runs of a
+//              narrow bucket); each lane owns float4 slices of the row; the group walks the run's
+//              sorted bags, broadcasting them by shuffle, with 4 gradient rows in flight; the
+//              optimizer runs in registers and the row is written with plain stores.
+//   long run   one warp per chunk (rows of the chunk spread over the warp like the forward);
+//              the chunk sum is merged with float4 atomicAdd (red.global.add.v4.f32) into the
+//              run's workspace row; fused mode then fences, counts down, and the last warp reads
+//              the complete sum from L2 and applies the optimizer.
+#include "tbe_internal.cuh"
+
+namespace tbe {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int kThreads = 256;
+constexpr int kWorkShort0 = 16;   // counters[16 + k]: work-claim counter of short bucket k
+constexpr int kWorkLong = 28;     // counters[28]: work-claim counter of long chunks
+constexpr int kClaim = 8;         // runs (per group) claimed per atomic in persistent mode
+
+__device__ __forceinline__ int bucket_of_width(int D) { return D <= 1 ? 0 : 32 - __clz(D - 1); }
+
+// ------------------------------------------------------------------------------------------
+// classify
+// ------------------------------------------------------------------------------------------
+template <typename Acc>
+__global__ void __launch_bounds__(kThreads) classify_kernel(BwdCtx c) {
+  __shared__ uint32_t s_cnt[kNumBuckets + 1];
+  __shared__ uint32_t s_base[kNumBuckets + 1];
+  __shared__ uint32_t s_chunks, s_chunk_base;
+  const uint32_t U = min(c.counters[TBE_CNT_RUNS], c.u_cap);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; r0 < U; r0 += stride) {
+    const int64_t r = r0 + threadIdx.x;
+    if (threadIdx.x <= kNumBuckets) s_cnt[threadIdx.x] = 0;
+    if (threadIdx.x == 0) s_chunks = 0;
+    __syncthreads();
+    int list = -1;
+    uint32_t nch = 0, my_off = 0, my_choff = 0, len = 0;
+    int D = 0;
+    if (r < U) {
+      const uint32_t key = c.unique[r];
+      len = c.run_off[r + 1] - c.run_off[r];
+      c.run_len[r] = len;
+      if (key < c.total_rows) {
+        const int t = table_of_row(c.roff, c.T, key);
+        D = __ldg(c.doff + t + 1) - __ldg(c.doff + t);
+        if (len >= static_cast<uint32_t>(c.threshold)) {
+          list = kNumBuckets;
+          nch = (len + c.chunk - 1) / c.chunk;
+          my_choff = atomicAdd(&s_chunks, nch);
+        } else {
+          list = bucket_of_width(D);
+        }
+        my_off = atomicAdd(&s_cnt[list], 1u);
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x <= kNumBuckets && s_cnt[threadIdx.x] > 0) {
+      const int ctr = threadIdx.x == kNumBuckets ? TBE_CNT_LONG : TBE_CNT_SHORT0 + threadIdx.x;
+      s_base[threadIdx.x] = atomicAdd(c.counters + ctr, s_cnt[threadIdx.x]);
+    }
+    if (threadIdx.x == kNumBuckets + 1 && s_chunks > 0)
+      s_chunk_base = atomicAdd(c.counters + TBE_CNT_CHUNKS, s_chunks);
+    __syncthreads();
+    if (list >= 0) {
+      const uint32_t slot = s_base[list] + my_off;
+      if (list < kNumBuckets) {
+        if (slot < c.short_cap[list]) c.short_list[list][slot] = static_cast<uint32_t>(r);
+      } else if (slot < c.long_cap) {
+        c.long_list[slot] = static_cast<uint32_t>(r);
+        c.countdown[slot] = nch;
+        float4* row = reinterpret_cast<float4*>(static_cast<Acc*>(c.ws_rows) + static_cast<int64_t>(slot) * c.max_D);
+        const int n16 = D * static_cast<int>(sizeof(Acc)) / 16;
+        for (int i = 0; i < n16; ++i) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t cb = s_chunk_base + my_choff;
+        for (uint32_t k = 0; k < nch; ++k)
+          if (cb + k < c.chunk_cap) c.chunks[cb + k] = make_uint2(slot, k);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// optimizer on one row held by `nl` lanes, each lane owning float4 slices j*LPRV + li
+// ------------------------------------------------------------------------------------------
+template <typename WT, int OPT, typename Acc, int VPL>
+__device__ __forceinline__ void apply_row_group(WT* wrow, float* state_ptr, Acc (&g)[VPL][4], int li,
+                                                int lanes, int nv, int D, float lr, float eps,
+                                                unsigned mask) {
+  using IO = VecIO<WT, 4 * sizeof(WT)>;
+  using Raw = typename IO::Raw;
+  Acc scale = static_cast<Acc>(lr);
+  if (OPT == TBE_OPT_ROWWISE_ADAGRAD) {
+    Acc ss = 0;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      if (li + j * lanes < nv)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ss += g[j][i] * g[j][i];
+    for (int m = lanes >> 1; m > 0; m >>= 1) ss += __shfl_xor_sync(mask, ss, m);
+    const Acc s_new = static_cast<Acc>(*state_ptr) + ss / static_cast<Acc>(D);
+    __syncwarp(mask);
+    if (li == 0) *state_ptr = static_cast<float>(s_new);
+    if constexpr (sizeof(Acc) == 8)
+      scale = static_cast<Acc>(lr) / (sqrt(s_new) + static_cast<Acc>(eps));
+    else
+      scale = lr / (sqrtf(s_new) + eps);
+  }
+  Raw* wv = reinterpret_cast<Raw*>(wrow);
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int vec = li + j * lanes;
+    if (vec < nv) {
+      float f[4];
+      IO::unpack(wv[vec], f);
+      float o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = static_cast<float>(static_cast<Acc>(f[i]) - scale * g[j][i]);
+      wv[vec] = IO::pack(o);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// short runs
+// ------------------------------------------------------------------------------------------
+template <typename WT, bool PSW, int OPT, int LPR, int VPL, bool PERSIST>
+__global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucket,
+                                                            const uint32_t* __restrict__ sorted_vals,
+                                                            const float* __restrict__ sorted_psw) {
+  using Acc = typename WTraits<WT>::Acc;
+  constexpr int GPW = kWarp / LPR;  // runs per warp
+  constexpr int UNROLL = 4;
+  const int lane = lane_id();
+  const int g = lane / LPR, li = lane % LPR;
+  const unsigned gmask = LPR == kWarp ? FULL : (((1u << LPR) - 1u) << (g * LPR));
+  const uint32_t count = min(c.counters[TBE_CNT_SHORT0 + bucket], c.short_cap[bucket]);
+  const uint32_t* list = c.short_list[bucket];
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / kWarp;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) / kWarp;
+
+  int64_t claim_base = 0, claim_left = 0;
+  int64_t it = 0;
+  while (true) {
+    int64_t base;
+    if (PERSIST) {
+      if (claim_left == 0) {
+        uint32_t b0 = 0;
+        if (lane == 0) b0 = atomicAdd(c.counters + kWorkShort0 + bucket, static_cast<uint32_t>(GPW * kClaim));
+        claim_base = __shfl_sync(FULL, b0, 0);
+        claim_left = kClaim;
+      }
+      base = claim_base;
+      claim_base += GPW;
+      --claim_left;
+    } else {
+      base = (gw + it * nw) * GPW;
+      ++it;
+    }
+    if (base >= count) break;  // warp-uniform
+    const int64_t i = base + g;
+    uint32_t key = 0, off = 0, len = 0;
+    if (i < count) {
+      const uint32_t r = list[i];
+      key = c.unique[r];
+      off = c.run_off[r];
+      len = c.run_off[r + 1] - off;
+    }
+    const int t = table_of_row(c.roff, c.T, key);
+    const int col0 = __ldg(c.doff + t);
+    const int D = __ldg(c.doff + t + 1) - col0;
+    const int nv = D / 4;
+    const uint32_t maxlen = __reduce_max_sync(FULL, len);
+
+    Acc acc[VPL][4];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[j][q] = Acc(0);
+
+    for (uint32_t j0 = 0; j0 < maxlen; j0 += LPR) {
+      uint32_t my_b = 0;
+      float my_w = 1.f;
+      bool my_ok = false;
+      if (j0 + li < len) {
+        my_b = __ldg(sorted_vals + off + j0 + li);
+        if (PSW) my_w = __ldg(sorted_psw + off + j0 + li);
+        my_ok = my_b < c.B;
+      }
+      const int steps = static_cast<int>(min(static_cast<uint32_t>(LPR), maxlen - j0));
+      for (int q0 = 0; q0 < steps; q0 += UNROLL) {
+        float4 v[UNROLL][VPL];
+        float w[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+          const int src = g * LPR + ((q0 + u) & (LPR - 1));
+          const uint32_t b = __shfl_sync(FULL, my_b, src);
+          const bool ok = __shfl_sync(FULL, static_cast<int>(my_ok), src) && (q0 + u < steps) &&
+                          (j0 + q0 + u < len);
+          w[u] = PSW ? __shfl_sync(FULL, my_w, src) : 1.f;
+          const float4* grow = reinterpret_cast<const float4*>(c.grad_out + static_cast<int64_t>(b) * c.total_D + col0);
+#pragma unroll
+          for (int jj = 0; jj < VPL; ++jj) {
+            const int vec = li + jj * LPR;
+            v[u][jj] = (ok && vec < nv) ? __ldg(grow + vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+#pragma unroll
+          for (int jj = 0; jj < VPL; ++jj) {
+            const Acc wu = static_cast<Acc>(w[u]);
+            acc[jj][0] += PSW ? static_cast<Acc>(v[u][jj].x) * wu : static_cast<Acc>(v[u][jj].x);
+            acc[jj][1] += PSW ? static_cast<Acc>(v[u][jj].y) * wu : static_cast<Acc>(v[u][jj].y);
+            acc[jj][2] += PSW ? static_cast<Acc>(v[u][jj].z) * wu : static_cast<Acc>(v[u][jj].z);
+            acc[jj][3] += PSW ? static_cast<Acc>(v[u][jj].w) * wu : static_cast<Acc>(v[u][jj].w);
+          }
+      }
+    }
+    if (len > 0) {
+      const int64_t row = static_cast<int64_t>(key) - __ldg(c.roff + t);
+      WT* wrow = static_cast<WT*>(c.weights) + __ldg(c.woff + t) + row * D;
+      apply_row_group<WT, OPT, Acc, VPL>(wrow, c.state + key, acc, li, LPR, nv, D, c.lr, c.eps, gmask);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// long runs: chunk partial sums, fused or separate apply
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ int next_pow2_int(int v) { return v <= 1 ? 1 : 1 << (32 - __clz(v - 1)); }
+
+template <typename Acc>
+__device__ __forceinline__ void merge_partial(void* ws_row, int vec, const Acc (&a)[4]);
+template <>
+__device__ __forceinline__ void merge_partial<float>(void* ws_row, int vec, const float (&a)[4]) {
+  atomicAdd(reinterpret_cast<float4*>(ws_row) + vec, make_float4(a[0], a[1], a[2], a[3]));
+}
+template <>
+__device__ __forceinline__ void merge_partial<double>(void* ws_row, int vec, const double (&a)[4]) {
+  double* p = reinterpret_cast<double*>(ws_row) + 4 * vec;
+  atomicAdd(p + 0, a[0]);
+  atomicAdd(p + 1, a[1]);
+  atomicAdd(p + 2, a[2]);
+  atomicAdd(p + 3, a[3]);
+}
+
+// Reads a complete workspace row from L2 (bypassing L1) and applies the optimizer with the
+// whole warp: lane l owns float4 slices l, l + 32, ...
+template <typename WT, int OPT, typename Acc, int MAXV>
+__device__ __forceinline__ void apply_from_workspace(const BwdCtx& c, uint32_t key, const void* ws_row) {
+  const int t = table_of_row(c.roff, c.T, key);
+  const int D = __ldg(c.doff + t + 1) - __ldg(c.doff + t);
+  const int nv = D / 4;
+  const int lane = lane_id();
+  Acc g[MAXV][4];
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    const int vec = lane + j * kWarp;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) g[j][i] = Acc(0);
+    if (vec < nv) {
+      if constexpr (sizeof(Acc) == 8) {
+        const double* p = reinterpret_cast<const double*>(ws_row) + 4 * vec;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) g[j][i] = __ldcg(p + i);
+      } else {
+        const float4 f = __ldcg(reinterpret_cast<const float4*>(ws_row) + vec);
+        g[j][0] = f.x;
+        g[j][1] = f.y;
+        g[j][2] = f.z;
+        g[j][3] = f.w;
+      }
+    }
+  }
+  const int64_t row = static_cast<int64_t>(key) - __ldg(c.roff + t);
+  WT* wrow = static_cast<WT*>(c.weights) + __ldg(c.woff + t) + row * D;
+  apply_row_group<WT, OPT, Acc, MAXV>(wrow, c.state + key, g, lane, kWarp, nv, D, c.lr, c.eps, FULL);
+}
+
+template <typename WT, bool PSW, int OPT, int MAXV, bool FUSED, bool PERSIST>
+__global__ void __launch_bounds__(kThreads) long_chunk_kernel(BwdCtx c,
+                                                             const uint32_t* __restrict__ sorted_vals,
+                                                             const float* __restrict__ sorted_psw) {
+  using Acc = typename WTraits<WT>::Acc;
+  constexpr int UNROLL = 4;
+  const int lane = lane_id();
+  const uint32_t nchunks = min(c.counters[TBE_CNT_CHUNKS], c.chunk_cap);
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / kWarp;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) / kWarp;
+  const size_t row_bytes = static_cast<size_t>(c.max_D) * sizeof(Acc);
+  int64_t it = 0;
+  while (true) {
+    int64_t ci;
+    if (PERSIST) {
+      uint32_t x = 0;
+      if (lane == 0) x = atomicAdd(c.counters + kWorkLong, 1u);
+      ci = __shfl_sync(FULL, x, 0);
+    } else {
+      ci = gw + it * nw;
+      ++it;
+    }
+    if (ci >= nchunks) break;
+    const uint2 desc = c.chunks[ci];
+    const uint32_t slot = desc.x;
+    if (slot >= c.long_cap) continue;
+    const uint32_t r = c.long_list[slot];
+    const uint32_t key = c.unique[r];
+    const uint32_t run_beg = c.run_off[r], run_end = c.run_off[r + 1];
+    const uint32_t s = run_beg + desc.y * static_cast<uint32_t>(c.chunk);
+    const uint32_t e = min(s + static_cast<uint32_t>(c.chunk), run_end);
+    const int t = table_of_row(c.roff, c.T, key);
+    const int col0 = __ldg(c.doff + t);
+    const int D = __ldg(c.doff + t + 1) - col0;
+    const int nv = D / 4;
+    const int lpr = nv >= kWarp ? kWarp : next_pow2_int(nv);
+    const int rps = kWarp / lpr;
+    const int rs = lane / lpr, vi = lane & (lpr - 1);
+
+    Acc acc[MAXV][4];
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[j][i] = Acc(0);
+    for (uint32_t base = s; base < e; base += kWarp) {
+      const int n = static_cast<int>(min(static_cast<uint32_t>(kWarp), e - base));
+      uint32_t my_b = 0;
+      float my_w = 1.f;
+      bool my_ok = false;
+      if (lane < n) {
+        my_b = __ldg(sorted_vals + base + lane);
+        if (PSW) my_w = __ldg(sorted_psw + base + lane);
+        my_ok = my_b < c.B;
+      }
+      for (int j = 0; j < n; j += rps * UNROLL) {
+        float4 v[UNROLL][MAXV];
+        float w[UNROLL];
+#pragma unroll
+        for (int q = 0; q < UNROLL; ++q) {
+          const int rr = j + q * rps + rs;
+          const int src = rr & (kWarp - 1);
+          const uint32_t b = __shfl_sync(FULL, my_b, src);
+          const bool ok = __shfl_sync(FULL, static_cast<int>(my_ok), src) && rr < n;
+          w[q] = PSW ? __shfl_sync(FULL, my_w, src) : 1.f;
+          const float4* grow = reinterpret_cast<const float4*>(c.grad_out + static_cast<int64_t>(b) * c.total_D + col0);
+#pragma unroll
+          for (int k = 0; k < MAXV; ++k) {
+            const int vec = vi + k * kWarp;
+            v[q][k] = (ok && vec < nv) ? __ldg(grow + vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < UNROLL; ++q)
+#pragma unroll
+          for (int k = 0; k < MAXV; ++k) {
+            const Acc wq = static_cast<Acc>(w[q]);
+            acc[k][0] += PSW ? static_cast<Acc>(v[q][k].x) * wq : static_cast<Acc>(v[q][k].x);
+            acc[k][1] += PSW ? static_cast<Acc>(v[q][k].y) * wq : static_cast<Acc>(v[q][k].y);
+            acc[k][2] += PSW ? static_cast<Acc>(v[q][k].z) * wq : static_cast<Acc>(v[q][k].z);
+            acc[k][3] += PSW ? static_cast<Acc>(v[q][k].w) * wq : static_cast<Acc>(v[q][k].w);
+          }
+      }
+    }
+    for (int m = lpr; m < kWarp; m <<= 1)
+#pragma unroll
+      for (int k = 0; k < MAXV; ++k)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[k][i] += __shfl_xor_sync(FULL, acc[k][i], m);
+    void* ws_row = static_cast<char*>(c.ws_rows) + static_cast<size_t>(slot) * row_bytes;
+    if (rs == 0) {
+#pragma unroll
+      for (int k = 0; k < MAXV; ++k) {
+        const int vec = vi + k * kWarp;
+        if (vec < nv) merge_partial<Acc>(ws_row, vec, acc[k]);
+      }
+    }
+    if (FUSED) {
+      // every lane's partial is visible device-wide before the countdown moves
+      __threadfence();
+      __syncwarp();
+      uint32_t old = 0;
+      if (lane == 0) old = atomicSub(c.countdown + slot, 1u);
+      old = __shfl_sync(FULL, old, 0);
+      if (old == 1) {
+        __threadfence();  // acquire: the other chunks' partials, published before their decrements
+        apply_from_workspace<WT, OPT, Acc, MAXV>(c, key, ws_row);
+      }
+    }
+  }
+}
+
+template <typename WT, int OPT, int MAXV>
+__global__ void __launch_bounds__(kThreads) long_apply_kernel(BwdCtx c) {
+  using Acc = typename WTraits<WT>::Acc;
+  const uint32_t nlong = min(c.counters[TBE_CNT_LONG], c.long_cap);
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / kWarp;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) / kWarp;
+  const size_t row_bytes = static_cast<size_t>(c.max_D) * sizeof(Acc);
+  for (int64_t slot = gw; slot < nlong; slot += nw) {
+    const uint32_t r = c.long_list[slot];
+    const uint32_t key = c.unique[r];
+    const void* ws_row = static_cast<const char*>(c.ws_rows) + static_cast<size_t>(slot) * row_bytes;
+    apply_from_workspace<WT, OPT, Acc, MAXV>(c, key, ws_row);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// dispatch
+// ------------------------------------------------------------------------------------------
+template <typename WT, bool PSW, int OPT, int LPR, int VPL>
+cudaError_t launch_short_t(const BwdCtx& c, int bucket, const uint32_t* vals, const float* psw,
+                           bool persist, const DeviceInfo& dev, cudaStream_t s) {
+  constexpr int GPW = kWarp / LPR;
+  const int64_t groups_per_cta = (kThreads / kWarp) * GPW;
+  const int64_t want = (static_cast<int64_t>(c.short_cap[bucket]) + groups_per_cta - 1) / groups_per_cta;
+  if (persist) {
+    auto k = short_run_kernel<WT, PSW, OPT, LPR, VPL, true>;
+    const int grid = persistent_grid(k, kThreads, 0, dev, want);
+    k<<<grid, kThreads, 0, s>>>(c, bucket, vals, psw);
+  } else {
+    auto k = short_run_kernel<WT, PSW, OPT, LPR, VPL, false>;
+    const int grid = persistent_grid(k, kThreads, 0, dev, want);
+    k<<<grid, kThreads, 0, s>>>(c, bucket, vals, psw);
+  }
+  return cudaGetLastError();
+}
+
+template <typename WT, bool PSW, int OPT>
+cudaError_t launch_short_bucket(const BwdCtx& c, int bucket, const uint32_t* vals, const float* psw,
+                                bool persist, const DeviceInfo& dev, cudaStream_t s) {
+  switch (bucket) {  // next_pow2(D) = 2^bucket; float4 slices per row = 2^(bucket-2)
+    case 2: return launch_short_t<WT, PSW, OPT, 1, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 3: return launch_short_t<WT, PSW, OPT, 2, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 4: return launch_short_t<WT, PSW, OPT, 4, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 5: return launch_short_t<WT, PSW, OPT, 8, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 6: return launch_short_t<WT, PSW, OPT, 16, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 7: return launch_short_t<WT, PSW, OPT, 32, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 8: return launch_short_t<WT, PSW, OPT, 32, 2>(c, bucket, vals, psw, persist, dev, s);
+    case 9: return launch_short_t<WT, PSW, OPT, 32, 4>(c, bucket, vals, psw, persist, dev, s);
+    case 10: return launch_short_t<WT, PSW, OPT, 32, 8>(c, bucket, vals, psw, persist, dev, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename WT, bool PSW, int OPT, int MAXV>
+cudaError_t launch_long_t(const BwdCtx& c, const uint32_t* vals, const float* psw, bool fused,
+                          bool persist, const DeviceInfo& dev, cudaStream_t s) {
+  const int64_t want = (static_cast<int64_t>(c.chunk_cap) + (kThreads / kWarp) - 1) / (kThreads / kWarp);
+#define TBE_LONG_LAUNCH(F, P)                                            \
+  {                                                                      \
+    auto k = long_chunk_kernel<WT, PSW, OPT, MAXV, F, P>;                \
+    const int grid = persistent_grid(k, kThreads, 0, dev, want);         \
+    k<<<grid, kThreads, 0, s>>>(c, vals, psw);                           \
+  }
+  if (fused) {
+    if (persist) TBE_LONG_LAUNCH(true, true) else TBE_LONG_LAUNCH(true, false)
+  } else {
+    if (persist) TBE_LONG_LAUNCH(false, true) else TBE_LONG_LAUNCH(false, false)
+  }
+#undef TBE_LONG_LAUNCH
+  return cudaGetLastError();
+}
+
+template <typename WT, bool PSW, int OPT>
+cudaError_t launch_long_maxv(const BwdCtx& c, const uint32_t* vals, const float* psw, bool fused,
+                             bool persist, int maxv, const DeviceInfo& dev, cudaStream_t s) {
+  switch (maxv) {
+    case 1: return launch_long_t<WT, PSW, OPT, 1>(c, vals, psw, fused, persist, dev, s);
+    case 2: return launch_long_t<WT, PSW, OPT, 2>(c, vals, psw, fused, persist, dev, s);
+    case 4: return launch_long_t<WT, PSW, OPT, 4>(c, vals, psw, fused, persist, dev, s);
+    default: return launch_long_t<WT, PSW, OPT, 8>(c, vals, psw, fused, persist, dev, s);
+  }
+}
+
+template <typename WT, int OPT>
+cudaError_t launch_apply_maxv(const BwdCtx& c, int maxv, const DeviceInfo& dev, cudaStream_t s) {
+  const int64_t want = (static_cast<int64_t>(c.long_cap) + (kThreads / kWarp) - 1) / (kThreads / kWarp);
+#define TBE_APPLY_LAUNCH(M)                                          \
+  {                                                                  \
+    auto k = long_apply_kernel<WT, OPT, M>;                          \
+    const int grid = persistent_grid(k, kThreads, 0, dev, want);     \
+    k<<<grid, kThreads, 0, s>>>(c);                                  \
+    return cudaGetLastError();                                       \
+  }
+  switch (maxv) {
+    case 1: TBE_APPLY_LAUNCH(1)
+    case 2: TBE_APPLY_LAUNCH(2)
+    case 4: TBE_APPLY_LAUNCH(4)
+    default: TBE_APPLY_LAUNCH(8)
+  }
+#undef TBE_APPLY_LAUNCH
+}
+
+int maxv_for(int max_D) {
+  const int nv = max_D / 4;
+  const int m = (nv + kWarp - 1) / kWarp;
+  return m <= 1 ? 1 : (m <= 2 ? 2 : (m <= 4 ? 4 : 8));
+}
+
+template <typename F>
+cudaError_t by_weight_type(int wdtype, F&& f) {
+  switch (wdtype) {
+    case TBE_F32: return f(float{});
+    case TBE_F16: return f(__half{});
+    default: return f(__nv_bfloat16{});
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_classify(const Problem& P, const BwdCtx& c, const DeviceInfo& dev, cudaStream_t s) {
+  const int64_t want = (static_cast<int64_t>(c.u_cap) + kThreads - 1) / kThreads;
+  if (P.wdtype == TBE_F32) {  // fp64 workspace rows for fp32 tables
+    const int grid = persistent_grid(classify_kernel<double>, kThreads, 0, dev, want);
+    classify_kernel<double><<<grid, kThreads, 0, s>>>(c);
+  } else {
+    const int grid = persistent_grid(classify_kernel<float>, kThreads, 0, dev, want);
+    classify_kernel<float><<<grid, kThreads, 0, s>>>(c);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_short_updates(const Problem& P, const BwdCtx& c, const BwdLayout& L,
+                                 tbe_optimizer opt, int scheduler, const DeviceInfo& dev,
+                                 cudaStream_t s) {
+  const uint32_t* vals = c.vals[L.final_buf];
+  const float* psw = P.weighted ? c.pswbuf[L.final_buf] : nullptr;
+  const bool persist = scheduler == TBE_SCHED_PERSISTENT;
+  for (int k = 2; k < kNumBuckets; ++k) {
+    if (c.short_cap[k] == 0) continue;
+    cudaError_t e = by_weight_type(P.wdtype, [&](auto w) -> cudaError_t {
+      using WT = decltype(w);
+      if (P.weighted) {
+        return opt == TBE_OPT_SGD ? launch_short_bucket<WT, true, TBE_OPT_SGD>(c, k, vals, psw, persist, dev, s)
+                                  : launch_short_bucket<WT, true, TBE_OPT_ROWWISE_ADAGRAD>(c, k, vals, psw, persist, dev, s);
+      }
+      return opt == TBE_OPT_SGD ? launch_short_bucket<WT, false, TBE_OPT_SGD>(c, k, vals, psw, persist, dev, s)
+                                : launch_short_bucket<WT, false, TBE_OPT_ROWWISE_ADAGRAD>(c, k, vals, psw, persist, dev, s);
+    });
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_long_updates(const Problem& P, const BwdCtx& c, const BwdLayout& L,
+                                tbe_optimizer opt, bool fused, int scheduler, const DeviceInfo& dev,
+                                cudaStream_t s) {
+  if (c.long_cap == 0) return cudaSuccess;
+  const uint32_t* vals = c.vals[L.final_buf];
+  const float* psw = P.weighted ? c.pswbuf[L.final_buf] : nullptr;
+  const bool persist = scheduler == TBE_SCHED_PERSISTENT;
+  const int maxv = maxv_for(P.max_D);
+  return by_weight_type(P.wdtype, [&](auto w) -> cudaError_t {
+    using WT = decltype(w);
+    if (P.weighted) {
+      return opt == TBE_OPT_SGD ? launch_long_maxv<WT, true, TBE_OPT_SGD>(c, vals, psw, fused, persist, maxv, dev, s)
+                                : launch_long_maxv<WT, true, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, persist, maxv, dev, s);
+    }
+    return opt == TBE_OPT_SGD ? launch_long_maxv<WT, false, TBE_OPT_SGD>(c, vals, psw, fused, persist, maxv, dev, s)
+                              : launch_long_maxv<WT, false, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, persist, maxv, dev, s);
+  });
+}
+
+cudaError_t launch_long_apply(const Problem& P, const BwdCtx& c, const BwdLayout& L,
+                              tbe_optimizer opt, const DeviceInfo& dev, cudaStream_t s) {
+  (void)L;
+  if (c.long_cap == 0) return cudaSuccess;
+  const int maxv = maxv_for(P.max_D);
+  return by_weight_type(P.wdtype, [&](auto w) -> cudaError_t {
+    using WT = decltype(w);
+    return opt == TBE_OPT_SGD ? launch_apply_maxv<WT, TBE_OPT_SGD>(c, maxv, dev, s)
+                              : launch_apply_maxv<WT, TBE_OPT_ROWWISE_ADAGRAD>(c, maxv, dev, s);
+  });
+}
+
+}  // namespace tbe

@@ -1,0 +1,459 @@
+// tbe_api.cu -- the C interface (tbe.h): argument validation, the host-side plan of each call
+// (sizes only from the host description, never from device data), workspace carving and the
+// launch sequence of each operation.  Nothing here synchronizes with the device, copies device
+// data to the host, or allocates memory.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "tbe_internal.cuh"
+
+namespace tbe {
+
+namespace {
+thread_local int g_last_cuda_error = 0;
+
+tbe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return TBE_OK;
+  g_last_cuda_error = static_cast<int>(e);
+  return TBE_ERR_CUDA;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int bucket_of(int D) {
+  int k = 0;
+  while ((1 << k) < D) ++k;
+  return k;
+}
+
+void record(const tbe_options& opt, int i, cudaStream_t s) {
+  if (opt.events != nullptr && i < opt.num_events && opt.events[i] != nullptr)
+    cudaEventRecord(static_cast<cudaEvent_t>(opt.events[i]), s);
+}
+
+tbe_options resolve(const tbe_options* opt) {
+  tbe_options o;
+  tbe_default_options(&o);
+  if (opt != nullptr) o = *opt;
+  return o;
+}
+
+tbe_status check_options(const tbe_options& o) {
+  if (o.long_threshold < 1 || o.chunk < 1) return TBE_ERR_INVALID_ARG;
+  if (o.long_mode < TBE_LONG_AUTO || o.long_mode > TBE_LONG_FUSED) return TBE_ERR_INVALID_ARG;
+  if (o.scheduler != TBE_SCHED_GRID && o.scheduler != TBE_SCHED_PERSISTENT) return TBE_ERR_INVALID_ARG;
+  if (o.num_events < 0 || (o.num_events > 0 && o.events == nullptr)) return TBE_ERR_INVALID_ARG;
+  return TBE_OK;
+}
+}  // namespace
+
+tbe_status make_problem(const tbe_problem* p, Problem* out) {
+  if (p == nullptr || out == nullptr) return TBE_ERR_INVALID_ARG;
+  if (p->T < 1 || p->B < 0 || p->num_indices < 0 || p->D == nullptr || p->E == nullptr)
+    return TBE_ERR_INVALID_ARG;
+  if (p->T > kMaxTables) return TBE_ERR_UNSUPPORTED;
+  if (p->wdtype != TBE_F32 && p->wdtype != TBE_F16 && p->wdtype != TBE_BF16) return TBE_ERR_UNSUPPORTED;
+  if (p->itype != TBE_I32 && p->itype != TBE_I64) return TBE_ERR_UNSUPPORTED;
+  Problem& P = *out;
+  P = Problem();
+  P.T = p->T;
+  P.B = p->B;
+  P.TB = static_cast<int64_t>(p->T) * p->B;
+  P.num_indices = p->num_indices;
+  P.wdtype = p->wdtype;
+  P.itype = p->itype;
+  P.weighted = p->weighted != 0;
+  P.wbytes = p->wdtype == TBE_F32 ? 4 : 2;
+  P.D.assign(p->D, p->D + p->T);
+  P.E.assign(p->E, p->E + p->T);
+  P.long_bags.assign(p->T, 0);
+  if (p->long_bags != nullptr) P.long_bags.assign(p->long_bags, p->long_bags + p->T);
+  bool all_vec16 = true;
+  for (int t = 0; t < P.T; ++t) {
+    const int D = P.D[t];
+    if (D < 4 || D > kMaxD || D % 4 != 0) return TBE_ERR_UNSUPPORTED;
+    if (P.E[t] < 1) return TBE_ERR_INVALID_ARG;
+    P.total_rows += P.E[t];
+    P.total_D += D;
+    if (D > P.max_D) P.max_D = D;
+    if ((static_cast<int64_t>(D) * P.wbytes) % 16 != 0) all_vec16 = false;
+  }
+  P.vec_bytes = all_vec16 ? 16 : 8;
+  if (P.itype == TBE_I32 && (P.total_rows > INT32_MAX || P.num_indices > INT32_MAX)) return TBE_ERR_RANGE;
+  if (P.B >= (int64_t(1) << 31) || P.num_indices >= (int64_t(1) << 31) ||
+      P.total_rows >= (int64_t(1) << 31))
+    return TBE_ERR_UNSUPPORTED;
+  return TBE_OK;
+}
+
+tbe_status device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static int sms_by_dev[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_status(cudaGetLastError());
+  out->id = dev;
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (sms_by_dev[dev] == 0) {
+      int sms = 0;
+      cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_status(e);
+      sms_by_dev[dev] = sms;
+    }
+    out->sms = sms_by_dev[dev];
+  } else {
+    int sms = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    out->sms = sms;
+  }
+  return TBE_OK;
+}
+
+BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const DeviceInfo& dev) {
+  BwdLayout L;
+  const uint32_t n_cap = static_cast<uint32_t>(P.num_indices);
+  L.n_cap = n_cap;
+  // key range [0, total_rows]: total_rows is the sentinel of an out-of-range id
+  int bits = 1;
+  while ((int64_t(1) << bits) <= P.total_rows) ++bits;
+  L.key_bits = bits;
+  L.passes = (bits + kRadixBits - 1) / kRadixBits;
+  L.final_buf = L.passes & 1;
+  const int64_t tiles = (static_cast<int64_t>(n_cap) + kSortTile - 1) / kSortTile;
+  int64_t sg = dev.sms * 3;
+  if (sg > 1024) sg = 1024;
+  if (tiles < sg) sg = tiles;
+  L.sort_grid = static_cast<int>(sg < 1 ? 1 : sg);
+  int64_t rg = dev.sms * 4;
+  if (rg > 1024) rg = 1024;
+  const int64_t rtiles = (static_cast<int64_t>(n_cap) + 4095) / 4096;
+  if (rtiles < rg) rg = rtiles;
+  L.rle_grid = static_cast<int>(rg < 1 ? 1 : rg);
+  const int64_t u = std::min<int64_t>(n_cap, P.total_rows + 1);
+  L.u_cap = static_cast<uint32_t>(u < 1 ? 1 : u);
+  int64_t rows_in_bucket[kNumBuckets] = {0};
+  for (int t = 0; t < P.T; ++t) rows_in_bucket[bucket_of(P.D[t])] += P.E[t];
+  for (int k = 0; k < kNumBuckets; ++k)
+    L.short_cap[k] = static_cast<uint32_t>(std::min<int64_t>(rows_in_bucket[k], n_cap));
+  L.long_cap = n_cap / static_cast<uint32_t>(opt.long_threshold);
+  L.chunk_cap = L.long_cap == 0 ? 0 : L.long_cap + n_cap / static_cast<uint32_t>(opt.chunk) + 1;
+  L.acc_bytes = P.wdtype == TBE_F32 ? 8 : 4;
+
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.counters = take(sizeof(uint32_t) * TBE_NUM_COUNTERS);
+  for (int b = 0; b < 2; ++b) {
+    L.keys[b] = take(sizeof(uint32_t) * n_cap);
+    L.vals[b] = take(sizeof(uint32_t) * n_cap);
+    L.psw[b] = P.weighted ? take(sizeof(float) * n_cap) : 0;
+  }
+  L.sort_counts = take(sizeof(uint32_t) * kRadix * L.sort_grid);
+  L.rle_counts = take(sizeof(uint32_t) * L.rle_grid);
+  L.unique = take(sizeof(uint32_t) * L.u_cap);
+  L.run_off = take(sizeof(uint32_t) * (L.u_cap + 1));
+  L.run_len = take(sizeof(uint32_t) * L.u_cap);
+  for (int k = 0; k < kNumBuckets; ++k) L.short_list[k] = take(sizeof(uint32_t) * L.short_cap[k]);
+  L.long_list = take(sizeof(uint32_t) * L.long_cap);
+  L.chunks = take(sizeof(uint2) * L.chunk_cap);
+  L.countdown = take(sizeof(uint32_t) * L.long_cap);
+  L.ws_rows = take(static_cast<size_t>(L.long_cap) * P.max_D * L.acc_bytes);
+  L.total = off;
+  return L;
+}
+
+namespace {
+
+BwdCtx make_ctx(const Problem& P, const tbe_options& o, const BwdLayout& L, const tbe_tables* tab,
+                void* weights, float* state, const void* indices, const void* offsets,
+                const float* psw, const float* grad_out, float lr, float eps, void* ws,
+                int64_t* d_stats) {
+  BwdCtx c;
+  std::memset(&c, 0, sizeof(c));
+  char* base = static_cast<char*>(ws);
+  c.T = P.T;
+  c.B = P.B;
+  c.TB = P.TB;
+  c.num_indices = P.num_indices;
+  c.total_rows = P.total_rows;
+  c.total_D = P.total_D;
+  c.max_D = P.max_D;
+  c.threshold = o.long_threshold;
+  c.chunk = o.chunk;
+  c.woff = tab ? tab->weight_offsets : nullptr;
+  c.doff = tab ? tab->D_offsets : nullptr;
+  c.roff = tab ? tab->row_offsets : nullptr;
+  c.weights = weights;
+  c.state = state;
+  c.indices = indices;
+  c.offsets = offsets;
+  c.psw = psw;
+  c.grad_out = grad_out;
+  c.lr = lr;
+  c.eps = eps;
+  c.counters = reinterpret_cast<uint32_t*>(base + L.counters);
+  for (int b = 0; b < 2; ++b) {
+    c.keys[b] = reinterpret_cast<uint32_t*>(base + L.keys[b]);
+    c.vals[b] = reinterpret_cast<uint32_t*>(base + L.vals[b]);
+    c.pswbuf[b] = P.weighted ? reinterpret_cast<float*>(base + L.psw[b]) : nullptr;
+  }
+  c.sort_counts = reinterpret_cast<uint32_t*>(base + L.sort_counts);
+  c.rle_counts = reinterpret_cast<uint32_t*>(base + L.rle_counts);
+  c.unique = reinterpret_cast<uint32_t*>(base + L.unique);
+  c.run_off = reinterpret_cast<uint32_t*>(base + L.run_off);
+  c.run_len = reinterpret_cast<uint32_t*>(base + L.run_len);
+  for (int k = 0; k < kNumBuckets; ++k) {
+    c.short_list[k] = reinterpret_cast<uint32_t*>(base + L.short_list[k]);
+    c.short_cap[k] = L.short_cap[k];
+  }
+  c.long_list = reinterpret_cast<uint32_t*>(base + L.long_list);
+  c.chunks = reinterpret_cast<uint2*>(base + L.chunks);
+  c.countdown = reinterpret_cast<uint32_t*>(base + L.countdown);
+  c.ws_rows = base + L.ws_rows;
+  c.long_cap = L.long_cap;
+  c.chunk_cap = L.chunk_cap;
+  c.u_cap = L.u_cap;
+  c.sort_grid = L.sort_grid;
+  c.rle_grid = L.rle_grid;
+  c.stats = reinterpret_cast<unsigned long long*>(d_stats);
+  return c;
+}
+
+bool tables_ok(const tbe_tables* tab) {
+  return tab != nullptr && tab->weight_offsets != nullptr && tab->D_offsets != nullptr &&
+         tab->row_offsets != nullptr;
+}
+
+}  // namespace
+}  // namespace tbe
+
+using namespace tbe;
+
+extern "C" {
+
+int tbe_version(void) { return TBE_VERSION; }
+
+int tbe_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* tbe_status_string(tbe_status status) {
+  switch (status) {
+    case TBE_OK: return "ok";
+    case TBE_ERR_INVALID_ARG: return "invalid argument";
+    case TBE_ERR_UNSUPPORTED: return "unsupported shape, dtype or size";
+    case TBE_ERR_WORKSPACE: return "workspace too small";
+    case TBE_ERR_CUDA: return "CUDA error";
+    case TBE_ERR_RANGE: return "int32 indices requested but the range does not fit int32";
+    default: return "unknown status";
+  }
+}
+
+void tbe_default_options(tbe_options* opt) {
+  if (opt == nullptr) return;
+  std::memset(opt, 0, sizeof(*opt));
+  opt->long_threshold = 256;
+  opt->chunk = 256;
+  opt->long_mode = TBE_LONG_AUTO;
+  opt->scheduler = TBE_SCHED_GRID;
+  opt->histogram = 1;
+  opt->fused_bounds = 0;
+  opt->events = nullptr;
+  opt->num_events = 0;
+}
+
+tbe_status tbe_table_layout(const tbe_problem* prob, int64_t* weight_offsets, int32_t* D_offsets,
+                            int64_t* row_offsets) {
+  Problem P;
+  tbe_status st = make_problem(prob, &P);
+  if (st != TBE_OK) return st;
+  int64_t w = 0, r = 0;
+  int32_t d = 0;
+  for (int t = 0; t <= P.T; ++t) {
+    if (weight_offsets) weight_offsets[t] = w;
+    if (D_offsets) D_offsets[t] = d;
+    if (row_offsets) row_offsets[t] = r;
+    if (t < P.T) {
+      w += P.E[t] * P.D[t];
+      d += P.D[t];
+      r += P.E[t];
+    }
+  }
+  return TBE_OK;
+}
+
+size_t tbe_bounds_workspace_size(const tbe_problem* prob) {
+  Problem P;
+  if (make_problem(prob, &P) != TBE_OK) return 0;
+  DeviceInfo dev;
+  if (device_info(&dev) != TBE_OK) return 0;
+  return align_up(sizeof(int64_t) * (1 + bounds_grid(dev)), 256);
+}
+
+tbe_status tbe_bounds_check(const tbe_problem* prob, const tbe_tables* tables, void* indices,
+                            void* offsets, void* ws, size_t ws_bytes, int64_t* d_stats,
+                            void* stream) {
+  Problem P;
+  tbe_status st = make_problem(prob, &P);
+  if (st != TBE_OK) return st;
+  if (!tables_ok(tables) || offsets == nullptr || (P.num_indices > 0 && indices == nullptr))
+    return TBE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != TBE_OK) return st;
+  const int grid = bounds_grid(dev);
+  if (ws == nullptr || ws_bytes < sizeof(int64_t) * (1 + grid)) return TBE_ERR_WORKSPACE;
+  if (!aligned(ws, 8)) return TBE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch_bounds(P, *tables, indices, offsets, static_cast<int64_t*>(ws), grid,
+                                   reinterpret_cast<unsigned long long*>(d_stats), s));
+}
+
+size_t tbe_forward_workspace_size(const tbe_problem* prob, const tbe_options* opt) {
+  (void)prob;
+  (void)opt;
+  return 0;
+}
+
+tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tbe_tables* tables,
+                       const void* weights, void* indices, const void* offsets, const float* psw,
+                       float* out, void* ws, size_t ws_bytes, int64_t* d_stats, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  Problem P;
+  tbe_status st = make_problem(prob, &P);
+  if (st != TBE_OK) return st;
+  const tbe_options o = resolve(opt);
+  if ((st = check_options(o)) != TBE_OK) return st;
+  if (!tables_ok(tables) || weights == nullptr || offsets == nullptr || out == nullptr ||
+      (P.num_indices > 0 && indices == nullptr))
+    return TBE_ERR_INVALID_ARG;
+  if (P.weighted != (psw != nullptr)) return TBE_ERR_INVALID_ARG;
+  if (!aligned(weights, 16) || !aligned(out, 16)) return TBE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != TBE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long* stats = reinterpret_cast<unsigned long long*>(d_stats);
+  record(o, TBE_FWD_EV_START, s);
+
+  // Tables on the counts x table path are skipped by the gather, which walks the remaining
+  // contiguous table ranges.
+  std::vector<int> hist;
+  if (o.histogram) {
+    for (int t = 0; t < P.T; ++t) {
+      const bool eligible = P.wdtype == TBE_F16 && !P.weighted && P.E[t] <= 64 && P.D[t] >= 64 &&
+                            P.D[t] <= 128 && P.long_bags[t] != 0 && !o.fused_bounds;
+      if (eligible && histogram_supported()) hist.push_back(t);
+    }
+  }
+  int t0 = 0;
+  size_t h = 0;
+  while (t0 < P.T) {
+    while (h < hist.size() && hist[h] == t0) {
+      ++t0;
+      ++h;
+    }
+    if (t0 >= P.T) break;
+    int t1 = t0;
+    while (t1 < P.T && !(h < hist.size() && hist[h] == t1)) ++t1;
+    cudaError_t e = launch_forward_gather(P, *tables, weights, indices, offsets, psw, out, t0 * P.B,
+                                          t1 * P.B, o.fused_bounds != 0, stats, dev, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    t0 = t1;
+  }
+  record(o, TBE_FWD_EV_GATHER, s);
+  for (int t : hist) {
+    cudaError_t e = launch_forward_histogram(P, *tables, weights, indices, offsets, out, t, stats, dev, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  record(o, TBE_FWD_EV_HISTOGRAM, s);
+  return TBE_OK;
+}
+
+size_t tbe_backward_workspace_size(const tbe_problem* prob, const tbe_options* opt) {
+  Problem P;
+  if (make_problem(prob, &P) != TBE_OK) return 0;
+  const tbe_options o = resolve(opt);
+  if (check_options(o) != TBE_OK) return 0;
+  DeviceInfo dev;
+  if (device_info(&dev) != TBE_OK) return 0;
+  return make_bwd_layout(P, o, dev).total;
+}
+
+tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
+                               const tbe_tables* tables, void* weights, float* state,
+                               const void* indices, const void* offsets, const float* psw,
+                               const float* grad_out, tbe_optimizer optimizer, float lr, float eps,
+                               void* ws, size_t ws_bytes, int64_t* d_stats, void* stream) {
+  Problem P;
+  tbe_status st = make_problem(prob, &P);
+  if (st != TBE_OK) return st;
+  const tbe_options o = resolve(opt);
+  if ((st = check_options(o)) != TBE_OK) return st;
+  if (optimizer != TBE_OPT_SGD && optimizer != TBE_OPT_ROWWISE_ADAGRAD) return TBE_ERR_INVALID_ARG;
+  if (!tables_ok(tables) || weights == nullptr || offsets == nullptr || grad_out == nullptr ||
+      (P.num_indices > 0 && indices == nullptr) ||
+      (optimizer == TBE_OPT_ROWWISE_ADAGRAD && state == nullptr))
+    return TBE_ERR_INVALID_ARG;
+  if (P.weighted != (psw != nullptr)) return TBE_ERR_INVALID_ARG;
+  if (!aligned(weights, 16) || !aligned(grad_out, 16) || !aligned(ws, 256)) return TBE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != TBE_OK) return st;
+  const BwdLayout L = make_bwd_layout(P, o, dev);
+  if (ws == nullptr || ws_bytes < L.total) return TBE_ERR_WORKSPACE;
+  const BwdCtx c = make_ctx(P, o, L, tables, weights, state, indices, offsets, psw, grad_out, lr,
+                            eps, ws, d_stats);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool fused = o.long_mode != TBE_LONG_TWO_KERNEL;
+  cudaError_t e;
+  record(o, TBE_BWD_EV_START, s);
+  if ((e = cudaMemsetAsync(c.counters, 0, sizeof(uint32_t) * TBE_NUM_COUNTERS, s)) != cudaSuccess)
+    return cuda_status(e);
+  if ((e = launch_expand(P, c, s)) != cudaSuccess) return cuda_status(e);
+  record(o, TBE_BWD_EV_EXPAND, s);
+  if ((e = launch_sort(P, c, L, s)) != cudaSuccess) return cuda_status(e);
+  record(o, TBE_BWD_EV_SORT, s);
+  if ((e = launch_rle(P, c, L, s)) != cudaSuccess) return cuda_status(e);
+  record(o, TBE_BWD_EV_RLE, s);
+  if ((e = launch_classify(P, c, dev, s)) != cudaSuccess) return cuda_status(e);
+  record(o, TBE_BWD_EV_CLASSIFY, s);
+  if ((e = launch_short_updates(P, c, L, optimizer, o.scheduler, dev, s)) != cudaSuccess)
+    return cuda_status(e);
+  record(o, TBE_BWD_EV_SHORT, s);
+  if ((e = launch_long_updates(P, c, L, optimizer, fused, o.scheduler, dev, s)) != cudaSuccess)
+    return cuda_status(e);
+  record(o, TBE_BWD_EV_LONG, s);
+  if (!fused && (e = launch_long_apply(P, c, L, optimizer, dev, s)) != cudaSuccess) return cuda_status(e);
+  record(o, TBE_BWD_EV_APPLY, s);
+  return TBE_OK;
+}
+
+tbe_status tbe_backward_metadata(const tbe_problem* prob, const tbe_options* opt, const void* ws,
+                                 size_t ws_bytes, tbe_run_metadata* meta) {
+  Problem P;
+  tbe_status st = make_problem(prob, &P);
+  if (st != TBE_OK) return st;
+  const tbe_options o = resolve(opt);
+  if ((st = check_options(o)) != TBE_OK) return st;
+  if (meta == nullptr || ws == nullptr) return TBE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != TBE_OK) return st;
+  const BwdLayout L = make_bwd_layout(P, o, dev);
+  if (ws_bytes < L.total) return TBE_ERR_WORKSPACE;
+  const char* base = static_cast<const char*>(ws);
+  meta->counters = reinterpret_cast<const uint32_t*>(base + L.counters);
+  meta->sorted_keys = reinterpret_cast<const uint32_t*>(base + L.keys[L.final_buf]);
+  meta->sorted_bags = reinterpret_cast<const uint32_t*>(base + L.vals[L.final_buf]);
+  meta->sorted_psw = P.weighted ? reinterpret_cast<const float*>(base + L.psw[L.final_buf]) : nullptr;
+  meta->unique_keys = reinterpret_cast<const uint32_t*>(base + L.unique);
+  meta->run_offsets = reinterpret_cast<const uint32_t*>(base + L.run_off);
+  meta->run_lengths = reinterpret_cast<const uint32_t*>(base + L.run_len);
+  meta->long_runs = reinterpret_cast<const uint32_t*>(base + L.long_list);
+  return TBE_OK;
+}
+
+}  // extern "C"

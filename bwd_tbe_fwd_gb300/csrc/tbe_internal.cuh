@@ -1,0 +1,273 @@
+// tbe_internal.cuh -- internal types, device helpers and launcher declarations shared by the
+// translation units of the TBE library.  Nothing here is part of the C interface (tbe.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <type_traits>
+#include <vector>
+
+#include "tbe.h"
+
+namespace tbe {
+
+constexpr int kWarp = 32;
+constexpr int kMaxTables = 4096;
+constexpr int kNumBuckets = TBE_NUM_BUCKETS;  // short-run buckets: next_pow2(D) = 2^k
+constexpr int kMaxD = 1024;
+constexpr int kSortThreads = 256;
+constexpr int kSortItems = 16;
+constexpr int kSortTile = kSortThreads * kSortItems;  // keys per radix-sort tile
+constexpr int kRadixBits = 8;
+constexpr int kRadix = 1 << kRadixBits;
+constexpr int kExpandBags = 512;                        // bags per expand CTA
+
+// ------------------------------------------------------------------------------------------
+// Host-side validated problem and device description
+// ------------------------------------------------------------------------------------------
+struct Problem {
+  int T = 0;
+  int64_t B = 0, TB = 0, num_indices = 0;
+  int wdtype = 0, itype = 0;
+  bool weighted = false;
+  std::vector<int> D;
+  std::vector<int64_t> E;
+  std::vector<uint8_t> long_bags;
+  int64_t total_rows = 0;
+  int total_D = 0, max_D = 0;
+  int wbytes = 0;           // bytes per weight element
+  int vec_bytes = 16;       // width of one weight-row load (16 or 8 bytes)
+};
+
+struct DeviceInfo {
+  int id = 0;
+  int sms = 0;
+};
+
+tbe_status make_problem(const tbe_problem* p, Problem* out);
+tbe_status device_info(DeviceInfo* out);
+
+// Layout of the backward workspace (byte offsets from the 256-aligned base).
+struct BwdLayout {
+  size_t counters = 0, keys[2] = {0, 0}, vals[2] = {0, 0}, psw[2] = {0, 0};
+  size_t sort_counts = 0, rle_counts = 0, unique = 0, run_off = 0, run_len = 0;
+  size_t short_list[kNumBuckets] = {0};
+  size_t long_list = 0, chunks = 0, countdown = 0, ws_rows = 0;
+  size_t total = 0;
+  uint32_t short_cap[kNumBuckets] = {0};
+  uint32_t long_cap = 0, chunk_cap = 0, u_cap = 0, n_cap = 0;
+  int sort_grid = 1, rle_grid = 1, key_bits = 1, passes = 1, final_buf = 0;
+  int acc_bytes = 4;  // fp32 workspace rows (fp64 for fp32 tables)
+};
+
+BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const DeviceInfo& dev);
+
+// Grid size of a persistent launch: resident blocks per SM (occupancy) x SMs, at most `cap`.
+template <typename K>
+int persistent_grid(K kernel, int threads, size_t smem, const DeviceInfo& dev, int64_t cap) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  int64_t g = static_cast<int64_t>(per_sm) * dev.sms;
+  if (cap < g) g = cap;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
+// ------------------------------------------------------------------------------------------
+// Device pointers for the backward pipeline
+// ------------------------------------------------------------------------------------------
+struct BwdCtx {
+  // problem
+  int T;
+  int64_t B, TB, num_indices, total_rows;
+  int total_D, max_D;
+  int threshold, chunk;
+  // tables
+  const int64_t* woff;
+  const int32_t* doff;
+  const int64_t* roff;
+  // inputs / state
+  void* weights;
+  float* state;
+  const void* indices;
+  const void* offsets;
+  const float* psw;
+  const float* grad_out;
+  float lr, eps;
+  // workspace
+  uint32_t* counters;
+  uint32_t* keys[2];
+  uint32_t* vals[2];
+  float* pswbuf[2];
+  uint32_t* sort_counts;
+  uint32_t* rle_counts;
+  uint32_t* unique;
+  uint32_t* run_off;
+  uint32_t* run_len;
+  uint32_t* short_list[kNumBuckets];
+  uint32_t short_cap[kNumBuckets];
+  uint32_t* long_list;
+  uint2* chunks;
+  uint32_t* countdown;
+  void* ws_rows;
+  uint32_t long_cap, chunk_cap, u_cap;
+  int sort_grid, rle_grid;
+  unsigned long long* stats;
+};
+
+// ------------------------------------------------------------------------------------------
+// Launchers (one translation unit each group); all asynchronous on `s`
+// ------------------------------------------------------------------------------------------
+cudaError_t launch_bounds(const Problem& P, const tbe_tables& tab, void* indices, void* offsets,
+                          int64_t* ws, int grid, unsigned long long* stats, cudaStream_t s);
+int bounds_grid(const DeviceInfo& dev);
+
+cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const void* weights,
+                                  void* indices, const void* offsets, const float* psw, float* out,
+                                  int64_t unit_begin, int64_t unit_end, bool fused_bounds,
+                                  unsigned long long* stats, const DeviceInfo& dev, cudaStream_t s);
+
+bool histogram_supported();
+cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, const void* weights,
+                                     const void* indices, const void* offsets, float* out, int table,
+                                     unsigned long long* stats, const DeviceInfo& dev, cudaStream_t s);
+
+cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s);
+cudaError_t launch_sort(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s);
+cudaError_t launch_rle(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s);
+cudaError_t launch_classify(const Problem& P, const BwdCtx& c, const DeviceInfo& dev, cudaStream_t s);
+cudaError_t launch_short_updates(const Problem& P, const BwdCtx& c, const BwdLayout& L,
+                                 tbe_optimizer opt, int scheduler, const DeviceInfo& dev,
+                                 cudaStream_t s);
+cudaError_t launch_long_updates(const Problem& P, const BwdCtx& c, const BwdLayout& L,
+                                tbe_optimizer opt, bool fused, int scheduler, const DeviceInfo& dev,
+                                cudaStream_t s);
+cudaError_t launch_long_apply(const Problem& P, const BwdCtx& c, const BwdLayout& L,
+                              tbe_optimizer opt, const DeviceInfo& dev, cudaStream_t s);
+
+// ------------------------------------------------------------------------------------------
+// Device helpers
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ int lane_id() { return threadIdx.x & (kWarp - 1); }
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+template <typename IT>
+__device__ __forceinline__ int64_t ld_int(const void* p, int64_t i) {
+  return static_cast<int64_t>(__ldg(static_cast<const IT*>(p) + i));
+}
+
+__device__ __forceinline__ int64_t clamp64(int64_t v, int64_t lo, int64_t hi) {
+  return v < lo ? lo : (v > hi ? hi : v);
+}
+
+__device__ __forceinline__ void stat_add(unsigned long long* stats, int k, unsigned long long v) {
+  if (stats != nullptr && v != 0) atomicAdd(stats + k, v);
+}
+
+// Table of a linear row id: the t with row_offsets[t] <= key < row_offsets[t+1].
+__device__ __forceinline__ int table_of_row(const int64_t* roff, int T, int64_t key) {
+  int lo = 0, hi = T;  // invariant: roff[lo] <= key < roff[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(roff + mid) <= key) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Weight element traits: accumulation type (fp32 for 16-bit tables, fp64 for fp32 tables,
+// as the forward's accumulation rule states) and vector conversions.
+template <typename WT> struct WTraits;
+template <> struct WTraits<float> {
+  using Acc = double;
+};
+template <> struct WTraits<__half> {
+  using Acc = float;
+};
+template <> struct WTraits<__nv_bfloat16> {
+  using Acc = float;
+};
+
+template <int BYTES> struct RawVec;
+template <> struct RawVec<16> { using T = uint4; };
+template <> struct RawVec<8> { using T = uint2; };
+template <> struct RawVec<4> { using T = uint32_t; };
+
+__device__ __forceinline__ void raw_words(const uint4& v, uint32_t (&w)[4]) { w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w; }
+__device__ __forceinline__ void raw_words(const uint2& v, uint32_t (&w)[2]) { w[0] = v.x; w[1] = v.y; }
+__device__ __forceinline__ void raw_words(const uint32_t& v, uint32_t (&w)[1]) { w[0] = v; }
+__device__ __forceinline__ uint4 make_raw(const uint32_t (&w)[4]) { return make_uint4(w[0], w[1], w[2], w[3]); }
+__device__ __forceinline__ uint2 make_raw(const uint32_t (&w)[2]) { return make_uint2(w[0], w[1]); }
+__device__ __forceinline__ uint32_t make_raw(const uint32_t (&w)[1]) { return w[0]; }
+
+// Unpack a raw vector of weights into N accumulator values.
+template <typename WT, int BYTES>
+struct VecIO {
+  static constexpr int N = BYTES / static_cast<int>(sizeof(WT));
+  static constexpr int W = BYTES / 4;
+  using Raw = typename RawVec<BYTES>::T;
+  using Acc = typename WTraits<WT>::Acc;
+
+  __device__ __forceinline__ static void unpack(const Raw& r, float (&f)[N]) {
+    uint32_t w[W];
+    raw_words(r, w);
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      if constexpr (sizeof(WT) == 2) {
+        float2 p;
+        if constexpr (std::is_same<WT, __half>::value) {
+          __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+          p = __half22float2(h);
+        } else {
+          __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+          p = __bfloat1622float2(h);
+        }
+        f[2 * i] = p.x;
+        f[2 * i + 1] = p.y;
+      } else {
+        f[i] = __uint_as_float(w[i]);
+      }
+    }
+  }
+
+  // Round-to-nearest-even store of N values.
+  __device__ __forceinline__ static Raw pack(const float (&f)[N]) {
+    uint32_t w[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      if constexpr (sizeof(WT) == 2) {
+        if constexpr (std::is_same<WT, __half>::value) {
+          __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+          w[i] = *reinterpret_cast<uint32_t*>(&h);
+        } else {
+          __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+          w[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+      } else {
+        w[i] = __float_as_uint(f[i]);
+      }
+    }
+    return make_raw(w);
+  }
+};
+
+template <typename Raw>
+__device__ __forceinline__ Raw ldg_raw(const Raw* p) {
+  return __ldg(p);
+}
+template <>
+__device__ __forceinline__ uint32_t ldg_raw<uint32_t>(const uint32_t* p) {
+  return __ldg(p);
+}
+
+}  // namespace tbe

@@ -1,0 +1,219 @@
+/*
+ * tbe.h -- C interface of the GB300 (sm_103a) table-batched embedding (TBE) library.
+ *
+ * What is computed (source pages by title and section):
+ *   [FBT] "Modernizing Table Batched Embeddings with FBTriton"
+ *   [TUT] "Table-Batched Embeddings in Triton: Gather, Pool, and Run-Length Backward"
+ *
+ *   Forward ([FBT] section 2; layout of [TUT] section 1): for every table t and bag b,
+ *     out[b, D_offsets[t] + d] = sum over lookups p of bag (t, b) of psw[p] * W_t[indices[p], d]
+ *   accumulated in fp32 (fp64 when the tables are fp32) and stored as fp32.
+ *   Backward ([FBT] section 3): for every distinct (table, row) touched by the batch, the sum
+ *   over its lookups of psw[p] * grad_out[b(p), D_offsets[t] + d], then exactly one SGD or
+ *   row-wise Adagrad update of that row ([TUT] section 5 gives the Adagrad rule:
+ *   state += mean_d(g_d^2); w -= lr * g / (sqrt(state) + eps)).
+ *
+ * Data layout (all device memory, caller-owned, row-major):
+ *   weights        all tables packed back to back: table t starts at element
+ *                  weight_offsets[t] = sum_{t'<t} E[t'] * D[t'];  row i of table t is the D[t]
+ *                  contiguous elements at weight_offsets[t] + i * D[t].  fp32, fp16 or bf16.
+ *   indices        [num_indices] table-local row ids, int32 or int64 (tbe_problem.itype).
+ *   offsets        [T*B + 1] same integer type as indices, table-major: bag (t, b) owns
+ *                  indices[offsets[t*B + b] .. offsets[t*B + b + 1]).  N = offsets[T*B].
+ *   psw            [num_indices] fp32 per-sample weights, or NULL (unweighted).
+ *   out, grad_out  [B, sum_t D[t]] fp32; table t occupies columns [D_offsets[t], +D[t]).
+ *   state          [sum_t E[t]] fp32 row-wise Adagrad state, one per row, indexed by the linear
+ *                  row id row_offsets[t] + i; NULL for SGD.
+ *   tbe_tables     three device arrays the caller fills once with tbe_table_layout():
+ *                  weight_offsets[T+1] (int64), D_offsets[T+1] (int32), row_offsets[T+1] (int64).
+ *
+ * Conventions:
+ *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy default stream).
+ *     None of tbe_bounds_check, tbe_forward, tbe_backward_update synchronizes with the host,
+ *     allocates memory, or copies device data to the host; every launch is sized from the
+ *     host-side tbe_problem and the data-dependent counts stay on the device.
+ *   - Return values report what the host can see: bad arguments, unsupported shapes, a
+ *     workspace that is too small, and CUDA launch errors.  Problems found in the data
+ *     (out-of-range ids, bad offsets, a bounded wait that gave up) are counted in the
+ *     optional device array d_stats[TBE_NUM_STATS] (int64, accumulated; the caller zeroes it
+ *     and reads it whenever it likes).  Kernels never dereference an id outside its table.
+ *   - The workspace is caller-owned device memory of at least the size the matching
+ *     *_workspace_size() call returns for the same problem and options; 256-byte aligned.
+ *   - Limits: 1 <= T <= 4096, 0 <= B, D[t] % 4 == 0 and 4 <= D[t] <= 1024, num_indices < 2^31,
+ *     sum_t E[t] < 2^31, B < 2^31; TBE_I32 additionally needs sum_t E[t] and num_indices to fit in
+ *     int32 ([FBT] section 2: int32 indices/offsets when the linearized range fits below 2^31).
+ */
+#ifndef TBE_H
+#define TBE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TBE_VERSION 1
+
+typedef enum {
+  TBE_OK = 0,
+  TBE_ERR_INVALID_ARG = 1,   /* a NULL pointer, a negative size, a misaligned buffer */
+  TBE_ERR_UNSUPPORTED = 2,   /* a width, dtype or size outside the limits above */
+  TBE_ERR_WORKSPACE = 3,     /* ws_bytes below the size the *_workspace_size query returns */
+  TBE_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed */
+  TBE_ERR_RANGE = 5          /* TBE_I32 requested but the rows or lookups do not fit int32 */
+} tbe_status;
+
+typedef enum { TBE_F32 = 0, TBE_F16 = 1, TBE_BF16 = 2 } tbe_dtype;
+typedef enum { TBE_I32 = 0, TBE_I64 = 1 } tbe_itype;
+typedef enum { TBE_OPT_SGD = 0, TBE_OPT_ROWWISE_ADAGRAD = 1 } tbe_optimizer;
+
+/* Long-run update ([FBT] section 3 and section 4, Problem 5): runs of at least
+ * long_threshold lookups are split into chunks of `chunk` lookups whose partial sums meet in a
+ * workspace row; the optimizer then runs either in a second kernel (TWO_KERNEL) or in the
+ * same launch, by the chunk that finishes last after a device-scope fence and a countdown
+ * (FUSED).  AUTO picks FUSED. */
+typedef enum { TBE_LONG_AUTO = 0, TBE_LONG_TWO_KERNEL = 1, TBE_LONG_FUSED = 2 } tbe_long_mode;
+
+/* Work distribution of the backward update kernels ([FBT] section 4, Problem 1, Solution 1.2):
+ * GRID = each warp takes a fixed stride of the device-side run/chunk lists; PERSISTENT = a
+ * persistent grid whose warps claim the next run or chunk from an atomic counter until none
+ * is left. */
+typedef enum { TBE_SCHED_GRID = 0, TBE_SCHED_PERSISTENT = 1 } tbe_scheduler;
+
+/* Host description of the problem.  Nothing here is read from the device. */
+typedef struct {
+  int32_t T;                  /* tables */
+  int64_t B;                  /* bags per table (batch size) */
+  int64_t num_indices;        /* length of the indices (and psw) buffers; N = offsets[T*B] <= it */
+  const int32_t* D;           /* host [T] row width of each table */
+  const int64_t* E;           /* host [T] rows of each table */
+  tbe_dtype wdtype;           /* weight storage type; outputs and gradients are fp32 */
+  tbe_itype itype;            /* type of indices AND offsets */
+  int32_t weighted;           /* nonzero: per-sample weights are passed (psw must be non-NULL) */
+  /* host [T] or NULL: nonzero declares that table t's bags usually hold at least 64 lookups.
+   * It only steers the choice of the counts x table path ([FBT] section 2, "The small-table
+   * histogram and tensor-core path"); results do not depend on it. */
+  const uint8_t* long_bags;
+} tbe_problem;
+
+/* Device arrays describing the packed layout (see tbe_table_layout). */
+typedef struct {
+  const int64_t* weight_offsets;  /* [T+1] first weight element of each table */
+  const int32_t* D_offsets;       /* [T+1] first output column of each table */
+  const int64_t* row_offsets;     /* [T+1] first linear row of each table */
+} tbe_tables;
+
+/* Stage boundaries recorded into tbe_options.events (cudaEvent_t handles, caller-created). */
+enum {
+  TBE_FWD_EV_START = 0, TBE_FWD_EV_GATHER = 1, TBE_FWD_EV_HISTOGRAM = 2, TBE_FWD_NUM_EVENTS = 3
+};
+enum {
+  TBE_BWD_EV_START = 0, TBE_BWD_EV_EXPAND = 1, TBE_BWD_EV_SORT = 2, TBE_BWD_EV_RLE = 3,
+  TBE_BWD_EV_CLASSIFY = 4, TBE_BWD_EV_SHORT = 5, TBE_BWD_EV_LONG = 6, TBE_BWD_EV_APPLY = 7,
+  TBE_BWD_NUM_EVENTS = 8
+};
+
+typedef struct {
+  int32_t long_threshold;     /* runs with at least this many lookups take the long path (256) */
+  int32_t chunk;              /* lookups per long-run chunk (256) */
+  int32_t long_mode;          /* tbe_long_mode */
+  int32_t scheduler;          /* tbe_scheduler */
+  int32_t histogram;          /* 1: use the counts x table path where eligible; 0: never */
+  int32_t fused_bounds;       /* 1: tbe_forward repairs out-of-range ids in flight (writing 0 back) */
+  void* const* events;        /* NULL, or cudaEvent_t[TBE_*_NUM_EVENTS] recorded at stage ends */
+  int32_t num_events;
+} tbe_options;
+
+/* Indices into d_stats (int64).  Counts accumulate over calls. */
+enum {
+  TBE_STAT_BAD_INDICES = 0,   /* out-of-range ids repaired (bounds check or fused forward) */
+  TBE_STAT_BAD_OFFSETS = 1,   /* offsets changed by the offsets repair */
+  TBE_STAT_UNREPAIRED = 2,    /* out-of-range ids or decreasing offsets met by a kernel that does
+                                 not repair them; such lookups are skipped */
+  TBE_STAT_WAIT_TIMEOUT = 3,  /* a bounded device-side wait gave up */
+  TBE_NUM_STATS = 8
+};
+
+/* The defaults: threshold 256, chunk 256, AUTO long mode, GRID scheduler, histogram on,
+ * fused bounds off, no events. */
+void tbe_default_options(tbe_options* opt);
+
+/* Fills the host arrays of the canonical packed layout for the problem; the caller copies
+ * them to the device arrays of tbe_tables.  Any pointer may be NULL. */
+tbe_status tbe_table_layout(const tbe_problem* prob, int64_t* weight_offsets /* [T+1] */,
+                            int32_t* D_offsets /* [T+1] */, int64_t* row_offsets /* [T+1] */);
+
+/* Validates and repairs indices and offsets in place ([FBT] section 2, "Bounds checking":
+ * a validation step before the forward; offsets get their own small kernel).  The rule:
+ * offsets[T*B] is clamped into [0, num_indices], offsets[0] becomes 0, every other offset is
+ * clamped into [0, offsets[T*B]] and raised to the previous one (so bags never overlap), and
+ * every id of bag (t, b) outside [0, E[t]) becomes 0.  Counts go to d_stats (nullable).
+ * ws: tbe_bounds_workspace_size() bytes (may be 0 -> ws may be NULL). */
+size_t tbe_bounds_workspace_size(const tbe_problem* prob);
+tbe_status tbe_bounds_check(const tbe_problem* prob, const tbe_tables* tables, void* indices,
+                            void* offsets, void* ws, size_t ws_bytes, int64_t* d_stats,
+                            void* stream);
+
+/* Pooled forward.  With opt->fused_bounds the kernel repairs out-of-range ids as it reads
+ * them (writing 0 back into indices, so the backward sees the repaired id); without it the
+ * ids must be valid (out-of-range ones are skipped and counted as TBE_STAT_UNREPAIRED).
+ * Offsets must be non-decreasing (tbe_bounds_check makes them so).  out: [B, sum D] fp32. */
+size_t tbe_forward_workspace_size(const tbe_problem* prob, const tbe_options* opt);
+tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tbe_tables* tables,
+                       const void* weights, void* indices, const void* offsets, const float* psw,
+                       float* out, void* ws, size_t ws_bytes, int64_t* d_stats, void* stream);
+
+/* Backward with the optimizer applied in place: linearize the (table, row) of every lookup,
+ * radix-sort the keys with their bags, run-length encode into runs, classify the runs on the
+ * device (short runs bucketed by next_pow2(D), long runs split into chunks), then update each
+ * touched row exactly once.  weights and state are updated in place; untouched rows are not
+ * written.  lr and eps are fp32; eps is ignored for SGD. */
+size_t tbe_backward_workspace_size(const tbe_problem* prob, const tbe_options* opt);
+tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
+                               const tbe_tables* tables, void* weights, float* state,
+                               const void* indices, const void* offsets, const float* psw,
+                               const float* grad_out, tbe_optimizer optimizer, float lr, float eps,
+                               void* ws, size_t ws_bytes, int64_t* d_stats, void* stream);
+
+/* Device counters kept in the backward workspace (uint32), for the metadata view below. */
+enum {
+  TBE_CNT_N = 0,              /* lookups of the batch (offsets[T*B], clamped) */
+  TBE_CNT_RUNS = 1,           /* U: distinct (table, row) keys */
+  TBE_CNT_LONG = 2,           /* runs on the long path */
+  TBE_CNT_CHUNKS = 3,         /* chunks of the long runs */
+  TBE_CNT_SHORT0 = 4,         /* TBE_CNT_SHORT0 + k: short runs whose next_pow2(D) is 2^k */
+  TBE_NUM_BUCKETS = 11,
+  TBE_NUM_COUNTERS = 32
+};
+
+/* Where the last tbe_backward_update on this workspace left its run metadata (device
+ * pointers into ws; valid until the workspace is reused).  Sizes are the device counters:
+ *   sorted_keys[N], sorted_bags[N] (and sorted_psw[N] when weighted): lookups ordered by key,
+ *     stable, so a run keeps its lookups in batch order; key = row_offsets[t] + row;
+ *   unique_keys[U], run_offsets[U+1] (run_offsets[U] = N), run_lengths[U];
+ *   long_runs[counters[TBE_CNT_LONG]]: run ids of the long runs. */
+typedef struct {
+  const uint32_t* counters;       /* [TBE_NUM_COUNTERS] */
+  const uint32_t* sorted_keys;
+  const uint32_t* sorted_bags;
+  const float* sorted_psw;        /* NULL when unweighted */
+  const uint32_t* unique_keys;
+  const uint32_t* run_offsets;
+  const uint32_t* run_lengths;
+  const uint32_t* long_runs;
+} tbe_run_metadata;
+
+tbe_status tbe_backward_metadata(const tbe_problem* prob, const tbe_options* opt, const void* ws,
+                                 size_t ws_bytes, tbe_run_metadata* meta);
+
+const char* tbe_status_string(tbe_status status);
+int tbe_version(void);
+/* The cudaError_t code of the last CUDA failure reported as TBE_ERR_CUDA on this thread. */
+int tbe_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TBE_H */

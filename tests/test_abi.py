@@ -1,0 +1,106 @@
+"""The C-ABI library on the host: it loads, exports every function include/tbe.h declares, and
+its host-only entry points (layout, options, argument validation) behave as documented.
+No call here launches GPU work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bwd_tbe_fwd_gb300 import build as tbe_build
+from bwd_tbe_fwd_gb300 import tbe
+
+HEADER = os.path.join(tbe_build.INCLUDE, "tbe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tbe_build.build()
+    return tbe.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tbe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in tbe.h but not exported"
+    assert set(names) == set(tbe.EXPORTED)
+
+
+def _problem(D, E, B=4, n=16, wdtype=tbe.TBE_F16, itype=tbe.TBE_I64, weighted=0):
+    Da = (ctypes.c_int32 * len(D))(*D)
+    Ea = (ctypes.c_int64 * len(E))(*E)
+    p = tbe.Problem(len(D), B, n, Da, Ea, wdtype, itype, weighted, None)
+    return p, (Da, Ea)
+
+
+def test_version_status_and_defaults(lib):
+    assert lib.tbe_version() == 1
+    assert lib.tbe_status_string(tbe.TBE_ERR_WORKSPACE) == b"workspace too small"
+    o = tbe.Options()
+    lib.tbe_default_options(ctypes.byref(o))
+    assert (o.long_threshold, o.chunk, o.long_mode, o.scheduler, o.histogram, o.fused_bounds) == \
+        (256, 256, tbe.TBE_LONG_AUTO, tbe.TBE_SCHED_GRID, 1, 0)
+
+
+def test_table_layout(lib):
+    p, keep = _problem([8, 16, 4], [10, 3, 7])
+    w = (ctypes.c_int64 * 4)()
+    d = (ctypes.c_int32 * 4)()
+    r = (ctypes.c_int64 * 4)()
+    assert lib.tbe_table_layout(ctypes.byref(p), w, d, r) == tbe.TBE_OK
+    assert list(w) == [0, 80, 128, 156]
+    assert list(d) == [0, 8, 24, 28]
+    assert list(r) == [0, 10, 13, 20]
+
+
+@pytest.mark.parametrize("D,E,itype,n,expect", [
+    ([6], [10], tbe.TBE_I64, 16, tbe.TBE_ERR_UNSUPPORTED),        # D not a multiple of 4
+    ([2048], [10], tbe.TBE_I64, 16, tbe.TBE_ERR_UNSUPPORTED),     # D above 1024
+    ([8], [0], tbe.TBE_I64, 16, tbe.TBE_ERR_INVALID_ARG),         # empty table
+    ([8], [2 ** 31], tbe.TBE_I32, 16, tbe.TBE_ERR_RANGE),         # int32 ids cannot address the rows
+    ([8], [2 ** 31], tbe.TBE_I64, 16, tbe.TBE_ERR_UNSUPPORTED),   # linear keys are 31-bit
+    ([8], [10], tbe.TBE_I64, 2 ** 31, tbe.TBE_ERR_UNSUPPORTED),   # lookups beyond 2^31
+])
+def test_layout_rejects(lib, D, E, itype, n, expect):
+    p, keep = _problem(D, E, itype=itype, n=n)
+    assert lib.tbe_table_layout(ctypes.byref(p), None, None, None) == expect
+
+
+def test_entry_points_validate_before_touching_the_device(lib):
+    p, keep = _problem([8], [10])
+    t = tbe.Tables(None, None, None)
+    # NULL tables / buffers are rejected on the host
+    assert lib.tbe_forward(ctypes.byref(p), None, ctypes.byref(t), None, None, None, None, None, None, 0,
+                           None, None) == tbe.TBE_ERR_INVALID_ARG
+    assert lib.tbe_backward_update(ctypes.byref(p), None, ctypes.byref(t), None, None, None, None, None,
+                                   None, tbe.TBE_OPT_SGD, 0.1, 0.0, None, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
+    assert lib.tbe_bounds_check(ctypes.byref(p), ctypes.byref(t), None, None, None, 0, None,
+                                None) == tbe.TBE_ERR_INVALID_ARG
+    # T = 0
+    p0, keep0 = _problem([8], [10])
+    p0.T = 0
+    assert lib.tbe_table_layout(ctypes.byref(p0), None, None, None) == tbe.TBE_ERR_INVALID_ARG
+    # bad options
+    o = tbe.Options()
+    lib.tbe_default_options(ctypes.byref(o))
+    o.chunk = 0
+    fake = ctypes.c_void_p(256)
+    t2 = tbe.Tables(fake, fake, fake)
+    assert lib.tbe_forward(ctypes.byref(p), ctypes.byref(o), ctypes.byref(t2), fake, fake, fake, None, fake,
+                           None, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
+    # psw must be given exactly when the problem is weighted
+    lib.tbe_default_options(ctypes.byref(o))
+    assert lib.tbe_forward(ctypes.byref(p), ctypes.byref(o), ctypes.byref(t2), fake, fake, fake, fake, fake,
+                           None, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
+
+
+def test_library_refuses_to_hide_a_missing_build(tmp_path):
+    with pytest.raises(tbe.TBEError):
+        tbe.load(str(tmp_path / "missing.so"))

@@ -1,0 +1,198 @@
+"""CUDA library vs the CPU oracle, through the C-ABI, on the five workloads (at sizes the
+oracle finishes in seconds that still span many tiles, CTAs and a ragged tail) and on the
+edge cases of the method."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bwd_tbe_fwd_gb300 import TBEOptions
+from synth import examples, get_config
+from tbe_harness import Case, check_forward, weights_to_oracle
+
+pytestmark = pytest.mark.gpu
+
+# Shrunk workloads: same kind (dtypes, widths, length and id laws, psw, bad ids), fewer bags,
+# and rows divided so that the skew still produces runs past the 256-lookup threshold.
+SMALL = {
+    "c1": get_config("c1"),
+    "c2": get_config("c2").shrink(B=1024, E_div=100),
+    "c3": get_config("c3").shrink(B=4096, T=6, E_div=400),
+    "c4": get_config("c4").shrink(B=2048, E_div=100),
+    "c5": get_config("c5").shrink(B=512, E_div=100),
+}
+
+
+@pytest.fixture(scope="module", params=sorted(SMALL))
+def case(request):
+    return Case(SMALL[request.param])
+
+
+def test_forward_matches_oracle(case):
+    case.forward()
+
+
+def test_backward_matches_oracle(case):
+    res = case.backward()
+    assert res["num_lookups"] > 0
+
+
+def test_paths_exercised(case):
+    """Every skewed workload reaches both the short and the long path."""
+    m = case.tbe.metadata()
+    if case.cfg.name.startswith("c1"):
+        return  # uniform ids over 1000 rows: runs of length 1-2 only
+    assert m["num_long"] > 0 and m["short_per_bucket"].sum() > 0, m["short_per_bucket"]
+
+
+def test_bounds_repair_counts_the_injected_ids():
+    cfg = SMALL["c5"]
+    c = Case(cfg, bounds_check=False)
+    n_bad = len(c.batch.bad_positions)
+    assert n_bad > 0
+    per_table, n_off = c.run_bounds()
+    assert int(per_table.sum()) == n_bad and n_off == 0
+    assert c.stats[0].item() == n_bad
+
+
+@pytest.mark.parametrize("threshold,chunk", [(10 ** 9, 8), (8, 8), (4, 2), (1, 1), (256, 256), (64, 16)])
+def test_threshold_sweep_same_answer(threshold, chunk):
+    """Routing every run short, mixed, finely split or all long must not change the result."""
+    c = Case(SMALL["c3"], threshold=threshold, chunk=chunk)
+    c.backward()
+
+
+@pytest.mark.parametrize("long_mode", ["two_kernel", "fused"])
+@pytest.mark.parametrize("scheduler", ["grid", "persistent"])
+def test_long_modes_and_schedulers(long_mode, scheduler):
+    opts = TBEOptions(long_mode={"two_kernel": 1, "fused": 2}[long_mode],
+                      scheduler={"grid": 0, "persistent": 1}[scheduler])
+    for name in ("c3", "c5"):
+        c = Case(SMALL[name], options=opts)
+        c.backward(options=opts)
+
+
+def test_skewed_example_batch_routes_as_printed():
+    """The tutorial's skewed batch (T=3, E=50, B=16, D=24, seed 1): the device classifier must
+    produce the printed short/long/chunk counts for each threshold and chunk size."""
+    import oracle_pins
+    gold = oracle_pins.read_golden("skewed_batch_runs.txt")
+    ex = examples.skewed_batch(seed=1)
+    from bwd_tbe_fwd_gb300 import TableBatchedEmbedding
+    T, E, B, D = ex["T"], ex["E"], ex["B"], ex["D"]
+    grad = torch.from_numpy(examples.skewed_batch_grad(B, T * D)).cuda()
+    idx = torch.from_numpy(ex["indices"]).cuda()
+    off = torch.from_numpy(ex["offsets"]).cuda()
+    for thr, chunk, n_short, n_long, n_chunks in gold["sweep"]:
+        opts = TBEOptions(long_threshold=int(thr), chunk=int(chunk))
+        tbe = TableBatchedEmbedding([D] * T, [E] * T, B, idx.numel(), torch.float32, torch.int64, options=opts)
+        w = torch.from_numpy(ex["W"].reshape(-1).copy()).cuda()
+        tbe.backward_update(w, None, idx, off, grad, optimizer="sgd", lr=0.05)
+        torch.cuda.synchronize()
+        m = tbe.metadata()
+        assert m["N"] == gold["lookups"][0][0] and m["U"] == gold["unique_rows"][0][0]
+        assert int(m["run_lengths"].max()) == gold["max_run"][0][0]
+        assert (int(m["short_per_bucket"].sum()), m["num_long"], m["num_chunks"]) == (n_short, n_long, n_chunks)
+        # and the update equals the oracle's
+        w_h = ex["W"].reshape(-1).copy()
+        res = oracle.backward(oracle.Tables([D] * T, [E] * T), B, w_h, None, ex["indices"], ex["offsets"],
+                              grad.cpu().numpy(), optimizer="sgd", lr=0.05)
+        assert np.allclose(w.cpu().numpy().astype(np.float64), w_h.astype(np.float64), rtol=1e-5, atol=1e-7)
+        assert np.array_equal(m["sorted_keys"].cpu().numpy(), res["sorted_keys"])
+
+
+def test_adagrad_two_steps_fp32():
+    """State carried across calls (non-zero initial state) on fp32 tables with Adagrad."""
+    cfg = get_config("c1").shrink(B=64, name="c1_adagrad")
+    import dataclasses
+    cfg = dataclasses.replace(cfg, optimizer="adagrad", lr=0.05)
+    c = Case(cfg)
+    c.backward(steps=2)
+
+
+def test_fused_bounds_forward_repairs_in_flight():
+    cfg = SMALL["c5"]
+    c = Case(cfg, bounds_check=False)
+    # offsets are valid in this workload; only ids are bad
+    oracle.bounds_repair(c.tables, cfg.B, c.idx_h, c.off_h)
+    opts = TBEOptions(fused_bounds=1)
+    w_d = c.w0.cuda()
+    out = c.tbe.forward(w_d, c.idx_d, c.off_d, psw=c.psw_d, stats=c.stats, options=opts)
+    torch.cuda.synchronize()
+    assert np.array_equal(c.idx_d.cpu().numpy(), c.idx_h)
+    assert c.stats[0].item() == len(c.batch.bad_positions)
+    _, exact, absterms = oracle.forward(c.tables, cfg.B, weights_to_oracle(c.w0, cfg.wdtype), c.idx_h, c.off_h,
+                                        psw=c.psw_h, wdtype=cfg.wdtype)
+    check_forward(out.cpu().numpy(), exact, absterms, cfg.wdtype)
+
+
+def test_unrepaired_ids_are_skipped_not_dereferenced():
+    cfg = SMALL["c5"]
+    c = Case(cfg, bounds_check=False)
+    c.tbe.forward(c.w0.cuda(), c.idx_d, c.off_d, psw=c.psw_d, stats=c.stats)
+    torch.cuda.synchronize()
+    n_bad = len(c.batch.bad_positions)
+    assert c.stats[2].item() == n_bad
+    # backward: the bad lookups form a sentinel run that is skipped
+    w = c.w0.cuda()
+    state = torch.zeros(cfg.total_rows, device="cuda")
+    c.tbe.backward_update(w, state, c.idx_d, c.off_d, c.grad.cuda(), psw=c.psw_d, stats=c.stats)
+    torch.cuda.synchronize()
+    assert c.stats[2].item() == 2 * n_bad
+
+
+@pytest.mark.parametrize("kind", ["all_empty", "one_bag", "single_lookup", "ragged"])
+def test_edge_batches(kind):
+    import dataclasses
+    from synth.configs import LengthSpec
+    base = get_config("c5").shrink(B=8, T=5, E_div=1000)
+    if kind == "all_empty":
+        tables = tuple(dataclasses.replace(t, lengths=LengthSpec("fixed", 0)) for t in base.tables)
+        cfg = dataclasses.replace(base, tables=tables, bad_id_frac=0.0, name="all_empty")
+    elif kind == "one_bag":
+        cfg = dataclasses.replace(base.shrink(B=1, T=1), bad_id_frac=0.0, name="one_bag")
+    elif kind == "single_lookup":
+        tables = tuple(dataclasses.replace(t, lengths=LengthSpec("fixed", 1)) for t in base.tables[:1])
+        cfg = dataclasses.replace(base, B=1, tables=tables, bad_id_frac=0.0, name="single_lookup")
+    else:
+        cfg = get_config("c3").shrink(B=333, T=3, E_div=4000, name="ragged")
+    c = Case(cfg)
+    c.forward()
+    c.backward()
+
+
+def test_graph_capture_no_host_sync():
+    """Bounds check, forward and backward captured in one CUDA graph: capture fails on any host
+    synchronization, and replays must give the eager results."""
+    cfg = SMALL["c3"]
+    c = Case(cfg, bounds_check=False)
+    w = c.w0.cuda()
+    state = torch.zeros(cfg.total_rows, device="cuda")
+    grad = c.grad.cuda()
+    idx0, off0 = c.idx_d.clone(), c.off_d.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up (attributes, occupancy queries) outside capture
+        c.tbe.bounds_check(c.idx_d, c.off_d, stream=s)
+        out = c.tbe.forward(w, c.idx_d, c.off_d, stream=s)
+        c.tbe.backward_update(w, state, c.idx_d, c.off_d, grad, lr=cfg.lr, eps=cfg.eps, stream=s)
+    torch.cuda.synchronize()
+    w_eager, s_eager, out_eager = w.clone(), state.clone(), out.clone()
+    w.copy_(c.w0.cuda())
+    state.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        c.tbe.bounds_check(c.idx_d, c.off_d, stream=s)
+        c.tbe.forward(w, c.idx_d, c.off_d, out=out, stream=s)
+        c.tbe.backward_update(w, state, c.idx_d, c.off_d, grad, lr=cfg.lr, eps=cfg.eps, stream=s)
+    w.copy_(c.w0.cuda())
+    state.zero_()
+    c.idx_d.copy_(idx0)
+    c.off_d.copy_(off0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_eager)
+    # the long path merges partial sums with atomics, so only the short-run rows are bitwise
+    # reproducible; compare within the fp16 tolerance
+    assert torch.allclose(w.float(), w_eager.float(), rtol=2e-3, atol=1e-6)
+    assert torch.allclose(state, s_eager, rtol=1e-5, atol=0)
