@@ -153,13 +153,16 @@ cudaError_t launch_typed(const Problem& P, const tbe_tables& tab, void* indices,
                          int64_t* ws, int grid, unsigned long long* stats, cudaStream_t s) {
   IT* off = static_cast<IT*>(offsets);
   offsets_max_kernel<IT><<<grid, kThreads, 0, s>>>(off, P.TB, P.num_indices, ws);
+  note_launch();
   offsets_fix_kernel<IT><<<grid, kThreads, 0, s>>>(off, P.TB, ws, stats);
+  note_launch();
   if (P.num_indices > 0) {
     const size_t smem = sizeof(int64_t) * (P.T + 1);
     int64_t want = (P.num_indices + kThreads - 1) / kThreads;
     const int g = static_cast<int>(want < grid ? (want < 1 ? 1 : want) : grid);
     indices_fix_kernel<IT><<<g, kThreads, smem, s>>>(static_cast<IT*>(indices), off, P.T, P.B,
                                                      tab.row_offsets, ws, stats);
+    note_launch();
   }
   return cudaGetLastError();
 }

@@ -164,6 +164,7 @@ cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   const int64_t want = (units + (threads / kWarp) - 1) / (threads / kWarp);
   const int grid = persistent_grid(k, threads, 0, dev, want);
   k<<<grid, threads, 0, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 

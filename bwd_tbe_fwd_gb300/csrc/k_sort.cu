@@ -384,17 +384,6 @@ cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s) {
   const int64_t grid64 = (c.TB + kExpandBags - 1) / kExpandBags;
   const int grid = static_cast<int>(grid64 < 1 ? 1 : grid64);
   const bool psw = P.weighted;
-  if (c.TB == 0) {
-    // no bags: only the lookup count (0) is recorded
-    if (P.itype == TBE_I32) {
-      if (psw) expand_kernel<int32_t, true><<<1, kThreads, 0, s>>>(a);
-      else expand_kernel<int32_t, false><<<1, kThreads, 0, s>>>(a);
-    } else {
-      if (psw) expand_kernel<int64_t, true><<<1, kThreads, 0, s>>>(a);
-      else expand_kernel<int64_t, false><<<1, kThreads, 0, s>>>(a);
-    }
-    return cudaGetLastError();
-  }
   if (P.itype == TBE_I32) {
     if (psw) expand_kernel<int32_t, true><<<grid, kThreads, 0, s>>>(a);
     else expand_kernel<int32_t, false><<<grid, kThreads, 0, s>>>(a);
@@ -402,6 +391,7 @@ cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s) {
     if (psw) expand_kernel<int64_t, true><<<grid, kThreads, 0, s>>>(a);
     else expand_kernel<int64_t, false><<<grid, kThreads, 0, s>>>(a);
   }
+  note_launch();  // a single CTA when there are no bags: it records the lookup count (0)
   return cudaGetLastError();
 }
 
@@ -429,7 +419,9 @@ cudaError_t launch_sort(const Problem& P, const BwdCtx& c, const BwdLayout& L, c
   for (int pass = 0; pass < L.passes; ++pass) {
     const int shift = pass * kRadixBits;
     radix_upsweep_kernel<<<G, kThreads, 0, s>>>(c.keys[cur], c.counters, shift, c.sort_counts, G);
+    note_launch();
     exclusive_scan_kernel<<<1, 1024, 0, s>>>(c.sort_counts, kRadix * G);
+    note_launch();
     if (psw)
       radix_downsweep_kernel<true><<<G, kThreads, smem, s>>>(
           c.keys[cur], c.vals[cur], c.pswbuf[cur], c.keys[cur ^ 1], c.vals[cur ^ 1], c.pswbuf[cur ^ 1],
@@ -438,6 +430,7 @@ cudaError_t launch_sort(const Problem& P, const BwdCtx& c, const BwdLayout& L, c
       radix_downsweep_kernel<false><<<G, kThreads, smem, s>>>(
           c.keys[cur], c.vals[cur], nullptr, c.keys[cur ^ 1], c.vals[cur ^ 1], nullptr, c.counters,
           c.sort_counts, shift, G);
+    note_launch();
     cur ^= 1;
   }
   return cudaGetLastError();
@@ -447,8 +440,10 @@ cudaError_t launch_rle(const Problem& P, const BwdCtx& c, const BwdLayout& L, cu
   (void)P;
   const uint32_t* keys = c.keys[L.final_buf];
   rle_count_kernel<<<L.rle_grid, kThreads, 0, s>>>(keys, c.counters, c.rle_counts, L.rle_grid);
+  note_launch();
   rle_write_kernel<<<L.rle_grid, kThreads, 0, s>>>(keys, c.counters, c.rle_counts, L.rle_grid,
                                                    c.unique, c.run_off, c.u_cap);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -437,10 +437,12 @@ cudaError_t launch_short_t(const BwdCtx& c, int bucket, const uint32_t* vals, co
     auto k = short_run_kernel<WT, PSW, OPT, LPR, VPL, true>;
     const int grid = persistent_grid(k, kThreads, 0, dev, want);
     k<<<grid, kThreads, 0, s>>>(c, bucket, vals, psw);
+    note_launch();
   } else {
     auto k = short_run_kernel<WT, PSW, OPT, LPR, VPL, false>;
     const int grid = persistent_grid(k, kThreads, 0, dev, want);
     k<<<grid, kThreads, 0, s>>>(c, bucket, vals, psw);
+    note_launch();
   }
   return cudaGetLastError();
 }
@@ -471,6 +473,7 @@ cudaError_t launch_long_t(const BwdCtx& c, const uint32_t* vals, const float* ps
     auto k = long_chunk_kernel<WT, PSW, OPT, MAXV, F, P>;                \
     const int grid = persistent_grid(k, kThreads, 0, dev, want);         \
     k<<<grid, kThreads, 0, s>>>(c, vals, psw);                           \
+    note_launch();                                                   \
   }
   if (fused) {
     if (persist) TBE_LONG_LAUNCH(true, true) else TBE_LONG_LAUNCH(true, false)
@@ -500,6 +503,7 @@ cudaError_t launch_apply_maxv(const BwdCtx& c, int maxv, const DeviceInfo& dev, 
     auto k = long_apply_kernel<WT, OPT, M>;                          \
     const int grid = persistent_grid(k, kThreads, 0, dev, want);     \
     k<<<grid, kThreads, 0, s>>>(c);                                  \
+    note_launch();                                                   \
     return cudaGetLastError();                                       \
   }
   switch (maxv) {
@@ -533,9 +537,11 @@ cudaError_t launch_classify(const Problem& P, const BwdCtx& c, const DeviceInfo&
   if (P.wdtype == TBE_F32) {  // fp64 workspace rows for fp32 tables
     const int grid = persistent_grid(classify_kernel<double>, kThreads, 0, dev, want);
     classify_kernel<double><<<grid, kThreads, 0, s>>>(c);
+    note_launch();
   } else {
     const int grid = persistent_grid(classify_kernel<float>, kThreads, 0, dev, want);
     classify_kernel<float><<<grid, kThreads, 0, s>>>(c);
+    note_launch();
   }
   return cudaGetLastError();
 }

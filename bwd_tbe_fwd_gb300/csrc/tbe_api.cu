@@ -12,6 +12,16 @@ namespace tbe {
 
 namespace {
 thread_local int g_last_cuda_error = 0;
+thread_local int64_t g_launches = 0;
+
+// Adds the launches of the current call to the caller's host counter, if any.
+struct LaunchTally {
+  const tbe_options& o;
+  explicit LaunchTally(const tbe_options& opt) : o(opt) { g_launches = 0; }
+  ~LaunchTally() {
+    if (o.launch_counter != nullptr) *o.launch_counter += g_launches;
+  }
+};
 
 tbe_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return TBE_OK;
@@ -49,6 +59,8 @@ tbe_status check_options(const tbe_options& o) {
   return TBE_OK;
 }
 }  // namespace
+
+void note_launch(int n) { g_launches += n; }
 
 tbe_status make_problem(const tbe_problem* p, Problem* out) {
   if (p == nullptr || out == nullptr) return TBE_ERR_INVALID_ARG;
@@ -332,12 +344,14 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
   if (!tables_ok(tables) || weights == nullptr || offsets == nullptr || out == nullptr ||
       (P.num_indices > 0 && indices == nullptr))
     return TBE_ERR_INVALID_ARG;
-  if (P.weighted != (psw != nullptr)) return TBE_ERR_INVALID_ARG;
+  if ((P.weighted && psw == nullptr && P.num_indices > 0) || (!P.weighted && psw != nullptr))
+    return TBE_ERR_INVALID_ARG;
   if (!aligned(weights, 16) || !aligned(out, 16)) return TBE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != TBE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned long long* stats = reinterpret_cast<unsigned long long*>(d_stats);
+  LaunchTally tally(o);
   record(o, TBE_FWD_EV_START, s);
 
   // Tables on the counts x table path are skipped by the gather, which walks the remaining
@@ -399,7 +413,8 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
       (P.num_indices > 0 && indices == nullptr) ||
       (optimizer == TBE_OPT_ROWWISE_ADAGRAD && state == nullptr))
     return TBE_ERR_INVALID_ARG;
-  if (P.weighted != (psw != nullptr)) return TBE_ERR_INVALID_ARG;
+  if ((P.weighted && psw == nullptr && P.num_indices > 0) || (!P.weighted && psw != nullptr))
+    return TBE_ERR_INVALID_ARG;
   if (!aligned(weights, 16) || !aligned(grad_out, 16) || !aligned(ws, 256)) return TBE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != TBE_OK) return st;
@@ -410,6 +425,7 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool fused = o.long_mode != TBE_LONG_TWO_KERNEL;
   cudaError_t e;
+  LaunchTally tally(o);
   record(o, TBE_BWD_EV_START, s);
   if ((e = cudaMemsetAsync(c.counters, 0, sizeof(uint32_t) * TBE_NUM_COUNTERS, s)) != cudaSuccess)
     return cuda_status(e);

@@ -49,6 +49,10 @@ struct DeviceInfo {
 };
 
 tbe_status make_problem(const tbe_problem* p, Problem* out);
+
+// Counts kernel launches of the current call on this host thread (reported through
+// tbe_options.launch_counter).
+void note_launch(int n = 1);
 tbe_status device_info(DeviceInfo* out);
 
 // Layout of the backward workspace (byte offsets from the 256-aligned base).

@@ -54,7 +54,7 @@ class Tables(ctypes.Structure):
 class Options(ctypes.Structure):
     _fields_ = [("long_threshold", c_i32), ("chunk", c_i32), ("long_mode", c_i32), ("scheduler", c_i32),
                 ("histogram", c_i32), ("fused_bounds", c_i32), ("events", ctypes.POINTER(vp)),
-                ("num_events", c_i32)]
+                ("num_events", c_i32), ("launch_counter", ctypes.POINTER(c_i64))]
 
 
 class RunMetadata(ctypes.Structure):
@@ -144,6 +144,12 @@ class TBEOptions:
                 raise TypeError(f"unknown option {k}")
             setattr(self.c, k, v)
 
+    def count_launches(self, counter: "ctypes.c_int64 | None"):
+        """Have the library add its kernel launches to a host int64 (ctypes.c_int64)."""
+        self._counter = counter
+        self.c.launch_counter = None if counter is None else ctypes.pointer(counter)
+        return self
+
     def with_events(self, events: list | None):
         """Record CUDA events (torch.cuda.Event) at stage ends; None clears."""
         if events is None:
@@ -151,6 +157,9 @@ class TBEOptions:
             self.c.num_events = 0
             self._events = None
         else:
+            for e in events:  # torch creates the CUDA event on its first record
+                if e is not None and e.cuda_event == 0:
+                    e.record()
             arr = (vp * len(events))(*[vp(e.cuda_event) if e is not None else None for e in events])
             self._events = (arr, events)
             self.c.events = ctypes.cast(arr, ctypes.POINTER(vp))
@@ -166,7 +175,10 @@ class TableBatchedEmbedding:
                  index_dtype: torch.dtype = torch.int64, weighted: bool = False, long_bags=None,
                  device="cuda", options: TBEOptions | None = None):
         self.lib = load()
-        self.device = torch.device(device)
+        dev = torch.device(device)
+        if dev.type == "cuda" and dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
         self.D = [int(d) for d in D]
         self.E = [int(e) for e in E]
         self.T = len(self.D)

@@ -20,7 +20,8 @@
  *   indices        [num_indices] table-local row ids, int32 or int64 (tbe_problem.itype).
  *   offsets        [T*B + 1] same integer type as indices, table-major: bag (t, b) owns
  *                  indices[offsets[t*B + b] .. offsets[t*B + b + 1]).  N = offsets[T*B].
- *   psw            [num_indices] fp32 per-sample weights, or NULL (unweighted).
+ *   psw            [num_indices] fp32 per-sample weights (weighted problems; may be NULL when
+ *                  num_indices is 0), NULL for unweighted problems.
  *   out, grad_out  [B, sum_t D[t]] fp32; table t occupies columns [D_offsets[t], +D[t]).
  *   state          [sum_t E[t]] fp32 row-wise Adagrad state, one per row, indexed by the linear
  *                  row id row_offsets[t] + i; NULL for SGD.
@@ -123,6 +124,7 @@ typedef struct {
   int32_t fused_bounds;       /* 1: tbe_forward repairs out-of-range ids in flight (writing 0 back) */
   void* const* events;        /* NULL, or cudaEvent_t[TBE_*_NUM_EVENTS] recorded at stage ends */
   int32_t num_events;
+  int64_t* launch_counter;    /* NULL, or a HOST counter to which each call adds its kernel launches */
 } tbe_options;
 
 /* Indices into d_stats (int64).  Counts accumulate over calls. */
