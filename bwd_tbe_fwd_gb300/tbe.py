@@ -37,8 +37,9 @@ EXPORTED = (
     "tbe_default_options", "tbe_table_layout", "tbe_bounds_workspace_size", "tbe_bounds_check",
     "tbe_forward_workspace_size", "tbe_forward", "tbe_backward_workspace_size",
     "tbe_backward_update", "tbe_backward_metadata", "tbe_status_string", "tbe_version",
-    "tbe_last_cuda_error",
+    "tbe_last_cuda_error", "tbe_backward_update_noalloc",
 )
+TBE_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class Problem(ctypes.Structure):
@@ -318,3 +319,29 @@ def tbe_backward_update(tbe: TableBatchedEmbedding, *a, **k):
 
 def tbe_backward_metadata(tbe: TableBatchedEmbedding):
     return tbe.metadata()
+
+
+def tbe_backward_update_noalloc(tbe: TableBatchedEmbedding, weights, state, indices, offsets, grad_out,
+                                psw=None, optimizer="adagrad", lr=0.01, eps=1e-8, stats=None, stream=None,
+                                options: TBEOptions | None = None):
+    """The backward update for callers that cannot allocate device memory: same arguments as
+    TableBatchedEmbedding.backward_update, but the library uses its built-in scratch array
+    (TBE_STATIC_SCRATCH_BYTES) instead of a workspace.  Problems whose workspace would exceed
+    that size raise; calls on one device share the array and must not overlap on the GPU."""
+    lib = tbe.lib
+    fn = lib.tbe_backward_update_noalloc
+    fn.argtypes = [ctypes.POINTER(Problem), ctypes.POINTER(Options), ctypes.POINTER(Tables), vp, vp, vp, vp,
+                   vp, vp, ctypes.c_int, c_f32, c_f32, vp, vp]
+    fn.restype = ctypes.c_int
+    tbe._idx(indices, offsets)
+    tbe._dev(weights, "weights", tbe.weight_dtype, tbe.num_weights)
+    tbe._dev(state, "state", torch.float32, tbe.total_rows)
+    tbe._dev(grad_out, "grad_out", torch.float32, tbe.B * tbe.total_D)
+    tbe._dev(psw, "psw", torch.float32, tbe.num_indices)
+    tbe._dev(stats, "stats", torch.int64, TBE_NUM_STATS)
+    opt = {"sgd": TBE_OPT_SGD, "adagrad": TBE_OPT_ROWWISE_ADAGRAD}[optimizer]
+    o = (options or tbe.options).c
+    st = fn(ctypes.byref(tbe.prob), ctypes.byref(o), ctypes.byref(tbe.tables), _ptr(weights), _ptr(state),
+            _ptr(indices), _ptr(offsets), _ptr(psw), _ptr(grad_out), opt, c_f32(lr), c_f32(eps), _ptr(stats),
+            _stream(stream))
+    _check(lib, st, "tbe_backward_update_noalloc")

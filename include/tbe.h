@@ -209,6 +209,32 @@ typedef struct {
 tbe_status tbe_backward_metadata(const tbe_problem* prob, const tbe_options* opt, const void* ws,
                                  size_t ws_bytes, tbe_run_metadata* meta);
 
+/* Size of the scratch array built into the library for tbe_backward_update_noalloc. */
+#define TBE_STATIC_SCRATCH_BYTES ((size_t)64 * 1024 * 1024)
+
+/* tbe_backward_update for callers that cannot allocate device memory (the pages have no
+ * counterpart of this entry point).  Some callers cannot hand the library a workspace: a
+ * runtime whose device allocations are all planned at start-up, an allocator the calling
+ * layer cannot reach, or code that must not call cudaMalloc.  This variant takes the same
+ * arguments minus the workspace and uses instead a TBE_STATIC_SCRATCH_BYTES array compiled into
+ * the library; it allocates nothing itself.
+ *   - Limit: problems whose tbe_backward_workspace_size() exceeds TBE_STATIC_SCRATCH_BYTES are
+ *     rejected with TBE_ERR_WORKSPACE (an invalid problem or options: TBE_ERR_INVALID_ARG or the
+ *     status tbe_backward_update would return).
+ *   - Memory: the array occupies device memory on every GPU where the entry point is used,
+ *     until the process exits.
+ *   - Set-up: the first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - Sharing: all calls on one device use the same array, which keeps the last call's
+ *     contents; each call zeroes what must start at zero.  Calls whose GPU work overlaps (other
+ *     streams, other host threads) race on it; the caller must order them.
+ * Results equal those of tbe_backward_update on the same inputs. */
+tbe_status tbe_backward_update_noalloc(const tbe_problem* prob, const tbe_options* opt,
+                                       const tbe_tables* tables, void* weights, float* state,
+                                       const void* indices, const void* offsets, const float* psw,
+                                       const float* grad_out, tbe_optimizer optimizer, float lr,
+                                       float eps, int64_t* d_stats, void* stream);
+
 const char* tbe_status_string(tbe_status status);
 int tbe_version(void);
 /* The cudaError_t code of the last CUDA failure reported as TBE_ERR_CUDA on this thread. */
