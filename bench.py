@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--scheduler", choices=["grid", "persistent"], default="grid")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tables", type=int, default=0,
+                    help="keep only the first T tables of the workload (small cases for profiling)")
     ap.add_argument("--cpu-sample-bags", type=int, default=0,
                     help="bags per table in the CPU oracle sample (0: sized for ~15 s)")
     return ap.parse_args()
@@ -122,9 +124,11 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None):
     pw = 4 if cfg.weighted else 0
     fwd = int(np.sum(st["per_table"] * (D * wb + ib + pw)) + TB * ib + cfg.B * int(D.sum()) * 4)
     bounds = (TB + 1) * ib + N * ib
-    if passes is None:
-        bits = int(np.ceil(np.log2(cfg.total_rows + 1)))
-        passes = (bits + 7) // 8
+    if passes is None:  # the library's choice: digits of 8-10 bits, ceil(bits / 10) passes
+        bits = 1
+        while (1 << bits) <= cfg.total_rows:
+            bits += 1
+        passes = (bits + 9) // 10
     expand = N * (ib + 8 + 2 * pw) + TB * ib
     sort = passes * N * (20 + 2 * pw)
     rle = N * 8 + st["U"] * 8
@@ -322,6 +326,8 @@ def run_ours(args):
     build.build()
     dev = torch.device("cuda", local)
     cfg = get_config(args.config)
+    if args.tables:
+        cfg = cfg.shrink(T=args.tables, name=f"{cfg.name}[T={args.tables}]")
     batch = make_batch(cfg)
     st = batch_stats(cfg, batch)
     opts = TBEOptions(long_mode={"auto": 0, "two_kernel": 1, "fused": 2}[args.long_mode],

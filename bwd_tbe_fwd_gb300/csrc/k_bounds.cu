@@ -129,19 +129,30 @@ __global__ void __launch_bounds__(kThreads) indices_fix_kernel(IT* indices, cons
   __syncthreads();
   const int64_t N = ws[0];
   unsigned long long bad = 0;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; p < N; p += stride) {
-    int lo = 0, hi = T;  // tstart[lo] <= p < tstart[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (tstart[mid] <= p) lo = mid;
-      else hi = mid;
+  constexpr int U = 4;  // ids per thread in flight
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * U;
+  for (int64_t pb = static_cast<int64_t>(blockIdx.x) * blockDim.x * U; pb < N; pb += stride) {
+    int64_t id[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t p = pb + u * blockDim.x + threadIdx.x;
+      id[u] = p < N ? static_cast<int64_t>(indices[p]) : 0;
     }
-    const int64_t E = __ldg(roff + lo + 1) - __ldg(roff + lo);
-    const int64_t id = static_cast<int64_t>(indices[p]);
-    if (id < 0 || id >= E) {
-      indices[p] = IT(0);
-      ++bad;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t p = pb + u * blockDim.x + threadIdx.x;
+      if (p >= N) continue;
+      int lo = 0, hi = T;  // tstart[lo] <= p < tstart[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tstart[mid] <= p) lo = mid;
+        else hi = mid;
+      }
+      const int64_t E = __ldg(roff + lo + 1) - __ldg(roff + lo);
+      if (id[u] < 0 || id[u] >= E) {
+        indices[p] = IT(0);
+        ++bad;
+      }
     }
   }
   bad = block_sum(bad, shc);
@@ -158,7 +169,7 @@ cudaError_t launch_typed(const Problem& P, const tbe_tables& tab, void* indices,
   note_launch();
   if (P.num_indices > 0) {
     const size_t smem = sizeof(int64_t) * (P.T + 1);
-    int64_t want = (P.num_indices + kThreads - 1) / kThreads;
+    int64_t want = (P.num_indices + 4 * kThreads - 1) / (4 * kThreads);
     const int g = static_cast<int>(want < grid ? (want < 1 ? 1 : want) : grid);
     indices_fix_kernel<IT><<<g, kThreads, smem, s>>>(static_cast<IT*>(indices), off, P.T, P.B,
                                                      tab.row_offsets, ws, stats);

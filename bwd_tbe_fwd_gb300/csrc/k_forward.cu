@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(256) fwd_gather_kernel(FwdArgs a) {
           stat_add(a.stats, TBE_STAT_UNREPAIRED, 1);
         }
       }
+      const int32_t row_id = my_ok ? static_cast<int32_t>(my_id) : -1;  // E < 2^31
       for (int j = 0; j < n; j += rps * UNROLL) {
         Raw v[UNROLL][MAXV];
         float w[UNROLL];
@@ -106,10 +107,10 @@ __global__ void __launch_bounds__(256) fwd_gather_kernel(FwdArgs a) {
         for (int q = 0; q < UNROLL; ++q) {
           const int r = j + q * rps + slot;
           const int src = r & (kWarp - 1);
-          const int64_t id = __shfl_sync(FULL, my_id, src);
-          const bool ok = __shfl_sync(FULL, my_ok, src) && r < n;
+          const int32_t id = __shfl_sync(FULL, row_id, src);
+          const bool ok = id >= 0 && r < n;
           w[q] = PSW ? __shfl_sync(FULL, my_w, src) : 1.0f;
-          const Raw* row = table + id * nvec;
+          const Raw* row = table + static_cast<int64_t>(ok ? id : 0) * nvec;
 #pragma unroll
           for (int k = 0; k < MAXV; ++k) {
             const int vv = vi + k * kWarp;

@@ -70,29 +70,42 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
   const int64_t r0 = i0 - t0 * a.B;
   const uint32_t B32 = static_cast<uint32_t>(a.B);
   const int64_t p0 = s_off[0], p1 = max(s_off[0], s_off[nb]);
-  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-    int lo = 0, hi = nb;  // s_off[lo] <= p < s_off[hi] (for non-decreasing offsets)
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_off[mid] <= p) lo = mid;
-      else hi = mid;
+  constexpr int U = 4;  // lookups per thread in flight
+  for (int64_t pb = p0; pb < p1; pb += U * blockDim.x) {
+    int64_t id[U];
+    float w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t p = pb + u * blockDim.x + threadIdx.x;
+      id[u] = p < p1 ? ld_int<IT>(a.indices, p) : 0;
+      if (PSW) w[u] = p < p1 ? __ldg(a.psw + p) : 0.f;
     }
-    const uint32_t rel = static_cast<uint32_t>(r0 + lo);
-    const int t = static_cast<int>(t0 + rel / B32);
-    const uint32_t b = rel % B32;
-    const int64_t rb = __ldg(a.roff + t);
-    const int64_t E = __ldg(a.roff + t + 1) - rb;
-    const int64_t id = ld_int<IT>(a.indices, p);
-    uint32_t key;
-    if (id >= 0 && id < E) {
-      key = static_cast<uint32_t>(rb + id);
-    } else {
-      key = a.sentinel;
-      ++bad;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t p = pb + u * blockDim.x + threadIdx.x;
+      if (p >= p1) continue;
+      int lo = 0, hi = nb;  // s_off[lo] <= p < s_off[hi] (for non-decreasing offsets)
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= p) lo = mid;
+        else hi = mid;
+      }
+      const uint32_t rel = static_cast<uint32_t>(r0 + lo);
+      const int t = static_cast<int>(t0 + rel / B32);
+      const uint32_t b = rel % B32;
+      const int64_t rb = __ldg(a.roff + t);
+      const int64_t E = __ldg(a.roff + t + 1) - rb;
+      uint32_t key;
+      if (id[u] >= 0 && id[u] < E) {
+        key = static_cast<uint32_t>(rb + id[u]);
+      } else {
+        key = a.sentinel;
+        ++bad;
+      }
+      a.keys[p] = key;
+      a.vals[p] = b;
+      if (PSW) a.psw_out[p] = w[u];
     }
-    a.keys[p] = key;
-    a.vals[p] = b;
-    if (PSW) a.psw_out[p] = __ldg(a.psw + p);
   }
   if (bad) atomicAdd(&s_bad, bad);
   __syncthreads();
@@ -102,6 +115,8 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
 // ------------------------------------------------------------------------------------------
 // radix sort
 // ------------------------------------------------------------------------------------------
+constexpr int kWarpsPerBlock = kThreads / kWarp;
+
 // The contiguous range of positions owned by CTA c of G: whole tiles, balanced.
 __device__ __forceinline__ void segment_of(int64_t N, int c, int G, int64_t* b0, int64_t* b1) {
   const int64_t nt = (N + kSortTile - 1) / kSortTile;
@@ -110,93 +125,142 @@ __device__ __forceinline__ void segment_of(int64_t N, int c, int G, int64_t* b0,
   *b1 = min(N, t1 * kSortTile);
 }
 
+// Per-CTA digit histogram of its segment -> counts[digit * G + c].
+template <int RB>
 __global__ void __launch_bounds__(kThreads) radix_upsweep_kernel(const uint32_t* keys,
                                                                 const uint32_t* counters, int shift,
                                                                 uint32_t* counts, int G) {
-  __shared__ uint32_t hist[kThreads / kWarp][kRadix];
+  constexpr int R = 1 << RB;
+  __shared__ uint32_t hist[kWarpsPerBlock][R];
   const int w = threadIdx.x / kWarp;
-  for (int j = threadIdx.x; j < (kThreads / kWarp) * kRadix; j += blockDim.x) (&hist[0][0])[j] = 0;
+  for (int j = threadIdx.x; j < kWarpsPerBlock * R; j += blockDim.x) (&hist[0][0])[j] = 0;
   __syncthreads();
   int64_t b0, b1;
   segment_of(counters[TBE_CNT_N], blockIdx.x, G, &b0, &b1);
-  // b0 is a multiple of the tile (16-byte aligned); vector loads for the bulk
-  const int64_t nvec = (b1 - b0) / 4;
+  const int64_t nvec = (b1 - b0) / 4;  // b0 is a multiple of the tile: 16-byte aligned
   const uint4* kv = reinterpret_cast<const uint4*>(keys + b0);
-  for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
-    const uint4 k = kv[i];
-    atomicAdd(&hist[w][(k.x >> shift) & (kRadix - 1)], 1u);
-    atomicAdd(&hist[w][(k.y >> shift) & (kRadix - 1)], 1u);
-    atomicAdd(&hist[w][(k.z >> shift) & (kRadix - 1)], 1u);
-    atomicAdd(&hist[w][(k.w >> shift) & (kRadix - 1)], 1u);
+  int64_t i = threadIdx.x;
+  for (; i + blockDim.x < nvec; i += 2 * blockDim.x) {
+    const uint4 k0 = kv[i], k1 = kv[i + blockDim.x];
+    atomicAdd(&hist[w][(k0.x >> shift) & (R - 1)], 1u);
+    atomicAdd(&hist[w][(k0.y >> shift) & (R - 1)], 1u);
+    atomicAdd(&hist[w][(k0.z >> shift) & (R - 1)], 1u);
+    atomicAdd(&hist[w][(k0.w >> shift) & (R - 1)], 1u);
+    atomicAdd(&hist[w][(k1.x >> shift) & (R - 1)], 1u);
+    atomicAdd(&hist[w][(k1.y >> shift) & (R - 1)], 1u);
+    atomicAdd(&hist[w][(k1.z >> shift) & (R - 1)], 1u);
+    atomicAdd(&hist[w][(k1.w >> shift) & (R - 1)], 1u);
   }
-  for (int64_t i = b0 + nvec * 4 + threadIdx.x; i < b1; i += blockDim.x)
-    atomicAdd(&hist[w][(keys[i] >> shift) & (kRadix - 1)], 1u);
+  for (; i < nvec; i += blockDim.x) {
+    const uint4 k0 = kv[i];
+    atomicAdd(&hist[w][(k0.x >> shift) & (R - 1)], 1u);
+    atomicAdd(&hist[w][(k0.y >> shift) & (R - 1)], 1u);
+    atomicAdd(&hist[w][(k0.z >> shift) & (R - 1)], 1u);
+    atomicAdd(&hist[w][(k0.w >> shift) & (R - 1)], 1u);
+  }
+  for (int64_t p = b0 + nvec * 4 + threadIdx.x; p < b1; p += blockDim.x)
+    atomicAdd(&hist[w][(keys[p] >> shift) & (R - 1)], 1u);
   __syncthreads();
-  for (int d = threadIdx.x; d < kRadix; d += blockDim.x) {
+  for (int d = threadIdx.x; d < R; d += blockDim.x) {
     uint32_t s = 0;
-    for (int k = 0; k < kThreads / kWarp; ++k) s += hist[k][d];
+#pragma unroll
+    for (int k = 0; k < kWarpsPerBlock; ++k) s += hist[k][d];
     counts[static_cast<int64_t>(d) * G + blockIdx.x] = s;
   }
 }
 
-// Exclusive scan, in place, of n counters (one CTA of 1024 threads; n <= 256 * 1024).
-__global__ void __launch_bounds__(1024) exclusive_scan_kernel(uint32_t* data, int n) {
-  __shared__ uint32_t warp_tot[32];
-  const int per = (n + blockDim.x - 1) / blockDim.x;
-  const int beg = min(n, static_cast<int>(threadIdx.x) * per), end = min(n, beg + per);
-  uint32_t local = 0;
-  for (int i = beg; i < end; ++i) local += data[i];
-  // block exclusive scan of `local`
+// Block-wide exclusive scan of one value per thread; returns the prefix, *total the sum.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* s_wsum, uint32_t* total) {
   const int lane = lane_id(), w = threadIdx.x / kWarp;
-  uint32_t v = local;
+  uint32_t x = v;
   for (int d = 1; d < kWarp; d <<= 1) {
-    const uint32_t o = __shfl_up_sync(FULL, v, d);
-    if (lane >= d) v += o;
-  }
-  if (lane == kWarp - 1) warp_tot[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    uint32_t x = lane < static_cast<int>(blockDim.x / kWarp) ? warp_tot[lane] : 0;
-    for (int d = 1; d < kWarp; d <<= 1) {
-      const uint32_t o = __shfl_up_sync(FULL, x, d);
-      if (lane >= d) x += o;
-    }
-    warp_tot[lane] = x;  // inclusive over warps
+    const uint32_t o = __shfl_up_sync(FULL, x, d);
+    if (lane >= d) x += o;
   }
   __syncthreads();
-  uint32_t run = v - local + (w > 0 ? warp_tot[w - 1] : 0);
-  for (int i = beg; i < end; ++i) {
-    const uint32_t c = data[i];
-    data[i] = run;
-    run += c;
+  if (lane == kWarp - 1) s_wsum[w] = x;
+  __syncthreads();
+  uint32_t before = 0, tot = 0;
+  for (int q = 0; q < static_cast<int>(blockDim.x / kWarp); ++q) {
+    const uint32_t c = s_wsum[q];
+    if (q < w) before += c;
+    tot += c;
   }
+  if (total) *total = tot;
+  return before + x - v;
 }
 
-template <bool PSW>
-__global__ void __launch_bounds__(kThreads) radix_downsweep_kernel(
+// One CTA per digit: exclusive scan, in place, of that digit's G per-CTA counts, and the
+// digit's total.
+__global__ void __launch_bounds__(kThreads) digit_scan_kernel(uint32_t* counts, uint32_t* totals, int G) {
+  __shared__ uint32_t s_wsum[kWarpsPerBlock];
+  uint32_t* row = counts + static_cast<int64_t>(blockIdx.x) * G;
+  const int per = (G + blockDim.x - 1) / blockDim.x;  // G <= 1024: at most 4
+  const int beg = min(G, static_cast<int>(threadIdx.x) * per), end = min(G, beg + per);
+  uint32_t c[4] = {0, 0, 0, 0}, local = 0;
+  for (int i = beg; i < end; ++i) {
+    c[i - beg] = row[i];
+    local += c[i - beg];
+  }
+  uint32_t total;
+  uint32_t run = block_exclusive_scan(local, s_wsum, &total);
+  for (int i = beg; i < end; ++i) {
+    row[i] = run;
+    run += c[i - beg];
+  }
+  if (threadIdx.x == 0) totals[blockIdx.x] = total;
+}
+
+size_t downsweep_smem_bytes(int rb, bool psw) {
+  const size_t R = size_t(1) << rb;
+  return sizeof(uint32_t) * kSortTile * (psw ? 3 : 2) + sizeof(uint16_t) * kWarpsPerBlock * R +
+         sizeof(uint32_t) * 3 * R;
+}
+
+// Stable scatter of each CTA's segment, tile by tile, to its digits' output ranges.
+template <int RB, bool PSW>
+__global__ void __launch_bounds__(kThreads, 3) radix_downsweep_kernel(
     const uint32_t* keys_in, const uint32_t* vals_in, const float* psw_in, uint32_t* keys_out,
     uint32_t* vals_out, float* psw_out, const uint32_t* counters, const uint32_t* scanned,
-    int shift, int G) {
+    const uint32_t* totals, int shift, int G) {
+  constexpr int R = 1 << RB;
+  constexpr int DPT = R / kThreads;  // digits per thread
   extern __shared__ __align__(16) uint32_t s_dyn[];
   uint32_t* s_keys = s_dyn;
   uint32_t* s_vals = s_dyn + kSortTile;
   float* s_psw = reinterpret_cast<float*>(s_dyn + 2 * kSortTile);
-  __shared__ uint32_t s_whist[kThreads / kWarp][kRadix];
-  __shared__ uint32_t s_run[kRadix];
-  __shared__ uint32_t s_dstart[kRadix];
-  __shared__ uint32_t s_tcount[kRadix];
-  __shared__ uint32_t s_wsum[kThreads / kWarp];
+  uint16_t* s_whist = reinterpret_cast<uint16_t*>(s_dyn + (PSW ? 3 : 2) * kSortTile);  // [warps][R]
+  uint32_t* s_run = reinterpret_cast<uint32_t*>(s_whist + kWarpsPerBlock * R);
+  uint32_t* s_dstart = s_run + R;
+  uint32_t* s_tcount = s_dstart + R;
+  __shared__ uint32_t s_wsum[kWarpsPerBlock];
 
   const int lane = lane_id(), w = threadIdx.x / kWarp;
   const unsigned lt = lanemask_lt();
   int64_t b0, b1;
   segment_of(counters[TBE_CNT_N], blockIdx.x, G, &b0, &b1);
-  for (int d = threadIdx.x; d < kRadix; d += blockDim.x)
-    s_run[d] = scanned[static_cast<int64_t>(d) * G + blockIdx.x];
+  {
+    // output base of each digit for this CTA: exclusive prefix over the digit totals plus the
+    // CTA's prefix within the digit
+    uint32_t tt[DPT], tsum = 0;
+#pragma unroll
+    for (int q = 0; q < DPT; ++q) {
+      tt[q] = totals[threadIdx.x * DPT + q];
+      tsum += tt[q];
+    }
+    uint32_t run = block_exclusive_scan(tsum, s_wsum, nullptr);
+#pragma unroll
+    for (int q = 0; q < DPT; ++q) {
+      const int d = threadIdx.x * DPT + q;
+      s_run[d] = run + scanned[static_cast<int64_t>(d) * G + blockIdx.x];
+      run += tt[q];
+    }
+  }
 
   for (int64_t tb = b0; tb < b1; tb += kSortTile) {
     const int n = static_cast<int>(min(static_cast<int64_t>(kSortTile), b1 - tb));
-    for (int j = threadIdx.x; j < (kThreads / kWarp) * kRadix; j += blockDim.x) (&s_whist[0][0])[j] = 0;
+    uint32_t* wh32 = reinterpret_cast<uint32_t*>(s_whist);
+    for (int j = threadIdx.x; j < kWarpsPerBlock * R / 2; j += blockDim.x) wh32[j] = 0;
     __syncthreads();
 
     uint32_t k[kSortItems], v[kSortItems], rank[kSortItems];
@@ -204,65 +268,59 @@ __global__ void __launch_bounds__(kThreads) radix_downsweep_kernel(
 #pragma unroll
     for (int i = 0; i < kSortItems; ++i) {
       const int e = w * (kSortItems * kWarp) + i * kWarp + lane;
-      if (e < n) {
-        k[i] = keys_in[tb + e];
-        v[i] = vals_in[tb + e];
-        if (PSW) pw[i] = psw_in[tb + e];
-      } else {
-        k[i] = 0;
-        v[i] = 0;
-        pw[i] = 0.f;
-      }
+      const bool ok = e < n;
+      k[i] = ok ? keys_in[tb + e] : 0u;
+      v[i] = ok ? vals_in[tb + e] : 0u;
+      if (PSW) pw[i] = ok ? psw_in[tb + e] : 0.f;
     }
+    uint16_t* my_hist = s_whist + w * R;
 #pragma unroll
     for (int i = 0; i < kSortItems; ++i) {
       const int e = w * (kSortItems * kWarp) + i * kWarp + lane;
-      const uint32_t d = e < n ? ((k[i] >> shift) & (kRadix - 1)) : static_cast<uint32_t>(kRadix);
+      const uint32_t d = e < n ? ((k[i] >> shift) & (R - 1)) : static_cast<uint32_t>(R);
       const unsigned peers = __match_any_sync(FULL, d);
       const int leader = __ffs(peers) - 1;
       uint32_t base = 0;
-      if (lane == leader && d < kRadix) {
-        base = s_whist[w][d];
-        s_whist[w][d] = base + __popc(peers);
+      if (lane == leader && d < R) {
+        base = my_hist[d];
+        my_hist[d] = static_cast<uint16_t>(base + __popc(peers));
       }
       base = __shfl_sync(FULL, base, leader);
       rank[i] = base + __popc(peers & lt);
       __syncwarp();
     }
     __syncthreads();
-    // per digit: exclusive prefix over warps, tile count
-    for (int d = threadIdx.x; d < kRadix; d += blockDim.x) {
-      uint32_t s = 0;
+    // per digit: exclusive prefix over the warps (in place) and the tile count, then the
+    // exclusive scan of the tile counts over the digits
+    uint32_t tc[DPT], tsum = 0;
 #pragma unroll
-      for (int q = 0; q < kThreads / kWarp; ++q) {
-        const uint32_t c = s_whist[q][d];
-        s_whist[q][d] = s;
-        s += c;
+    for (int q = 0; q < DPT; ++q) {
+      const int d = threadIdx.x * DPT + q;
+      uint32_t sacc = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < kWarpsPerBlock; ++w2) {
+        const uint32_t c = s_whist[w2 * R + d];
+        s_whist[w2 * R + d] = static_cast<uint16_t>(sacc);
+        sacc += c;
       }
-      s_tcount[d] = s;
+      tc[q] = sacc;
+      tsum += sacc;
     }
-    __syncthreads();
-    // exclusive scan of tile counts over digits (kRadix == kThreads: one digit per thread)
-    {
-      const uint32_t c = s_tcount[threadIdx.x];
-      uint32_t x = c;
-      for (int d = 1; d < kWarp; d <<= 1) {
-        const uint32_t o = __shfl_up_sync(FULL, x, d);
-        if (lane >= d) x += o;
-      }
-      if (lane == kWarp - 1) s_wsum[w] = x;
-      __syncthreads();
-      uint32_t before = 0;
-      for (int q = 0; q < w; ++q) before += s_wsum[q];
-      s_dstart[threadIdx.x] = before + x - c;
+    uint32_t run = block_exclusive_scan(tsum, s_wsum, nullptr);
+#pragma unroll
+    for (int q = 0; q < DPT; ++q) {
+      const int d = threadIdx.x * DPT + q;
+      s_dstart[d] = run;
+      s_tcount[d] = tc[q];
+      run += tc[q];
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kSortItems; ++i) {
       const int e = w * (kSortItems * kWarp) + i * kWarp + lane;
       if (e < n) {
-        const uint32_t d = (k[i] >> shift) & (kRadix - 1);
-        const uint32_t pos = s_dstart[d] + s_whist[w][d] + rank[i];
+        const uint32_t d = (k[i] >> shift) & (R - 1);
+        const uint32_t pos = s_dstart[d] + s_whist[w * R + d] + rank[i];
         s_keys[pos] = k[i];
         s_vals[pos] = v[i];
         if (PSW) s_psw[pos] = pw[i];
@@ -271,25 +329,60 @@ __global__ void __launch_bounds__(kThreads) radix_downsweep_kernel(
     __syncthreads();
     for (int j = threadIdx.x; j < n; j += blockDim.x) {
       const uint32_t key = s_keys[j];
-      const uint32_t d = (key >> shift) & (kRadix - 1);
+      const uint32_t d = (key >> shift) & (R - 1);
       const uint32_t g = s_run[d] + (static_cast<uint32_t>(j) - s_dstart[d]);
       keys_out[g] = key;
       vals_out[g] = s_vals[j];
       if (PSW) psw_out[g] = s_psw[j];
     }
     __syncthreads();
-    for (int d = threadIdx.x; d < kRadix; d += blockDim.x) s_run[d] += s_tcount[d];
+#pragma unroll
+    for (int q = 0; q < DPT; ++q) {
+      const int d = threadIdx.x * DPT + q;
+      s_run[d] += s_tcount[d];
+    }
     __syncthreads();
   }
 }
 
 // ------------------------------------------------------------------------------------------
-// run-length encoding
+// run-length encoding: each thread owns 16 consecutive sorted keys of a 4096-key tile
 // ------------------------------------------------------------------------------------------
+constexpr int kRleItems = 16;
+constexpr int kRleTile = kThreads * kRleItems;
+
 __device__ __forceinline__ void rle_segment(int64_t N, int c, int G, int64_t* b0, int64_t* b1) {
-  const int64_t per = (N + G - 1) / G;
-  *b0 = min(N, per * c);
-  *b1 = min(N, *b0 + per);
+  const int64_t nt = (N + kRleTile - 1) / kRleTile;
+  *b0 = min(N, (nt * c / G) * kRleTile);
+  *b1 = min(N, (nt * (c + 1) / G) * kRleTile);
+}
+
+// Loads keys[p0 .. p0+16) (clipped to n valid) and the key before p0; returns the head mask.
+__device__ __forceinline__ uint32_t load_heads(const uint32_t* keys, int64_t p0, int64_t b1,
+                                               uint32_t (&k)[kRleItems]) {
+  const int64_t nvalid = b1 - p0;
+  if (nvalid >= kRleItems) {
+    const uint4* v = reinterpret_cast<const uint4*>(keys + p0);
+#pragma unroll
+    for (int q = 0; q < kRleItems / 4; ++q) {
+      const uint4 x = v[q];
+      k[4 * q] = x.x;
+      k[4 * q + 1] = x.y;
+      k[4 * q + 2] = x.z;
+      k[4 * q + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kRleItems; ++i) k[i] = i < nvalid ? keys[p0 + i] : 0u;
+  }
+  uint32_t prev = p0 > 0 ? keys[p0 - 1] : ~k[0];
+  uint32_t mask = 0;
+#pragma unroll
+  for (int i = 0; i < kRleItems; ++i) {
+    if (i < nvalid && k[i] != prev) mask |= 1u << i;
+    prev = k[i];
+  }
+  return mask;
 }
 
 __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* sh) {
@@ -307,13 +400,18 @@ __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* sh) {
 __global__ void __launch_bounds__(kThreads) rle_count_kernel(const uint32_t* keys,
                                                             const uint32_t* counters,
                                                             uint32_t* rle_counts, int G) {
-  __shared__ uint32_t sh[kThreads / kWarp];
+  __shared__ uint32_t sh[kWarpsPerBlock];
   const int64_t N = counters[TBE_CNT_N];
   int64_t b0, b1;
   rle_segment(N, blockIdx.x, G, &b0, &b1);
   uint32_t heads = 0;
-  for (int64_t i = b0 + threadIdx.x; i < b1; i += blockDim.x)
-    heads += (i == 0 || keys[i] != keys[i - 1]) ? 1u : 0u;
+  for (int64_t tb = b0; tb < b1; tb += kRleTile) {
+    const int64_t p0 = tb + static_cast<int64_t>(threadIdx.x) * kRleItems;
+    if (p0 < b1) {
+      uint32_t k[kRleItems];
+      heads += __popc(load_heads(keys, p0, b1, k));
+    }
+  }
   heads = block_sum_u32(heads, sh);
   if (threadIdx.x == 0) rle_counts[blockIdx.x] = heads;
 }
@@ -323,40 +421,30 @@ __global__ void __launch_bounds__(kThreads) rle_write_kernel(const uint32_t* key
                                                             const uint32_t* rle_counts, int G,
                                                             uint32_t* unique, uint32_t* run_off,
                                                             uint32_t u_cap) {
-  __shared__ uint32_t sh[kThreads / kWarp];
-  __shared__ uint32_t s_wcnt[kThreads / kWarp];
-  const int lane = lane_id(), w = threadIdx.x / kWarp;
+  __shared__ uint32_t sh[kWarpsPerBlock];
   const int64_t N = counters[TBE_CNT_N];
   uint32_t before = 0;
   for (int c = threadIdx.x; c < static_cast<int>(blockIdx.x); c += blockDim.x) before += rle_counts[c];
   uint32_t base = block_sum_u32(before, sh);
   int64_t b0, b1;
   rle_segment(N, blockIdx.x, G, &b0, &b1);
-  for (int64_t tb = b0; tb < b1; tb += blockDim.x) {
-    const int64_t i = tb + threadIdx.x;
-    bool head = false;
-    uint32_t key = 0;
-    if (i < b1) {
-      key = keys[i];
-      head = (i == 0) || key != keys[i - 1];
-    }
-    const unsigned bal = __ballot_sync(FULL, head);
-    if (lane == 0) s_wcnt[w] = __popc(bal);
-    __syncthreads();
-    uint32_t pre = 0, tot = 0;
-    for (int q = 0; q < static_cast<int>(blockDim.x / kWarp); ++q) {
-      if (q < w) pre += s_wcnt[q];
-      tot += s_wcnt[q];
-    }
-    if (head) {
-      const uint32_t r = base + pre + __popc(bal & lanemask_lt());
-      if (r < u_cap) {
-        unique[r] = key;
-        run_off[r] = static_cast<uint32_t>(i);
+  for (int64_t tb = b0; tb < b1; tb += kRleTile) {
+    const int64_t p0 = tb + static_cast<int64_t>(threadIdx.x) * kRleItems;
+    uint32_t k[kRleItems];
+    const uint32_t mask = p0 < b1 ? load_heads(keys, p0, b1, k) : 0u;
+    uint32_t total;
+    uint32_t r = base + block_exclusive_scan(__popc(mask), sh, &total);
+#pragma unroll
+    for (int i = 0; i < kRleItems; ++i) {
+      if (mask & (1u << i)) {
+        if (r < u_cap) {
+          unique[r] = k[i];
+          run_off[r] = static_cast<uint32_t>(p0 + i);
+        }
+        ++r;
       }
     }
-    base += tot;
-    __syncthreads();
+    base += total;
   }
   if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
     counters[TBE_CNT_RUNS] = base;
@@ -395,11 +483,10 @@ cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-size_t sort_smem_bytes(bool psw) { return sizeof(uint32_t) * kSortTile * (psw ? 3 : 2); }
-
-cudaError_t launch_sort(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s) {
+template <int RB>
+cudaError_t launch_sort_rb(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s) {
   const bool psw = P.weighted;
-  const size_t smem = sort_smem_bytes(psw);
+  const size_t smem = downsweep_smem_bytes(RB, psw);
   // the opt-in shared memory size is a per-device function attribute: set it once per device
   static std::atomic<uint64_t> attr_set[2] = {{0}, {0}};
   int dev = 0;
@@ -407,9 +494,9 @@ cudaError_t launch_sort(const Problem& P, const BwdCtx& c, const BwdLayout& L, c
   if (e != cudaSuccess) return e;
   const uint64_t bit = uint64_t(1) << (dev & 63);
   if ((attr_set[psw ? 1 : 0].load() & bit) == 0) {
-    e = psw ? cudaFuncSetAttribute(radix_downsweep_kernel<true>,
+    e = psw ? cudaFuncSetAttribute(radix_downsweep_kernel<RB, true>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-            : cudaFuncSetAttribute(radix_downsweep_kernel<false>,
+            : cudaFuncSetAttribute(radix_downsweep_kernel<RB, false>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set[psw ? 1 : 0].fetch_or(bit);
@@ -417,23 +504,31 @@ cudaError_t launch_sort(const Problem& P, const BwdCtx& c, const BwdLayout& L, c
   const int G = L.sort_grid;
   int cur = 0;
   for (int pass = 0; pass < L.passes; ++pass) {
-    const int shift = pass * kRadixBits;
-    radix_upsweep_kernel<<<G, kThreads, 0, s>>>(c.keys[cur], c.counters, shift, c.sort_counts, G);
+    const int shift = pass * RB;
+    radix_upsweep_kernel<RB><<<G, kThreads, 0, s>>>(c.keys[cur], c.counters, shift, c.sort_counts, G);
     note_launch();
-    exclusive_scan_kernel<<<1, 1024, 0, s>>>(c.sort_counts, kRadix * G);
+    digit_scan_kernel<<<1 << RB, kThreads, 0, s>>>(c.sort_counts, c.sort_totals, G);
     note_launch();
     if (psw)
-      radix_downsweep_kernel<true><<<G, kThreads, smem, s>>>(
+      radix_downsweep_kernel<RB, true><<<G, kThreads, smem, s>>>(
           c.keys[cur], c.vals[cur], c.pswbuf[cur], c.keys[cur ^ 1], c.vals[cur ^ 1], c.pswbuf[cur ^ 1],
-          c.counters, c.sort_counts, shift, G);
+          c.counters, c.sort_counts, c.sort_totals, shift, G);
     else
-      radix_downsweep_kernel<false><<<G, kThreads, smem, s>>>(
+      radix_downsweep_kernel<RB, false><<<G, kThreads, smem, s>>>(
           c.keys[cur], c.vals[cur], nullptr, c.keys[cur ^ 1], c.vals[cur ^ 1], nullptr, c.counters,
-          c.sort_counts, shift, G);
+          c.sort_counts, c.sort_totals, shift, G);
     note_launch();
     cur ^= 1;
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_sort(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s) {
+  switch (L.radix_bits) {
+    case 8: return launch_sort_rb<8>(P, c, L, s);
+    case 9: return launch_sort_rb<9>(P, c, L, s);
+    default: return launch_sort_rb<10>(P, c, L, s);
+  }
 }
 
 cudaError_t launch_rle(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s) {

@@ -54,14 +54,15 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(BwdCtx c) {
     if (threadIdx.x == 0) s_chunks = 0;
     __syncthreads();
     int list = -1;
-    uint32_t nch = 0, my_off = 0, my_choff = 0, len = 0;
-    int D = 0;
+    uint32_t nch = 0, my_off = 0, my_choff = 0, len = 0, key = 0, start = 0;
+    int D = 0, t = 0;
     if (r < U) {
-      const uint32_t key = c.unique[r];
-      len = c.run_off[r + 1] - c.run_off[r];
+      key = c.unique[r];
+      start = c.run_off[r];
+      len = c.run_off[r + 1] - start;
       c.run_len[r] = len;
       if (key < c.total_rows) {
-        const int t = table_of_row(c.roff, c.T, key);
+        t = table_of_row(c.roff, c.T, key);
         D = __ldg(c.doff + t + 1) - __ldg(c.doff + t);
         if (len >= static_cast<uint32_t>(c.threshold)) {
           list = kNumBuckets;
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(BwdCtx c) {
     if (list >= 0) {
       const uint32_t slot = s_base[list] + my_off;
       if (list < kNumBuckets) {
-        if (slot < c.short_cap[list]) c.short_list[list][slot] = static_cast<uint32_t>(r);
+        if (slot < c.short_cap[list]) c.short_list[list][slot] = make_uint4(start, len, key, static_cast<uint32_t>(t));
       } else if (slot < c.long_cap) {
         c.long_list[slot] = static_cast<uint32_t>(r);
         c.countdown[slot] = nch;
@@ -92,8 +93,12 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(BwdCtx c) {
         const int n16 = D * static_cast<int>(sizeof(Acc)) / 16;
         for (int i = 0; i < n16; ++i) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         const uint32_t cb = s_chunk_base + my_choff;
-        for (uint32_t k = 0; k < nch; ++k)
-          if (cb + k < c.chunk_cap) c.chunks[cb + k] = make_uint2(slot, k);
+        const uint32_t run_end = start + len;
+        for (uint32_t k = 0; k < nch; ++k) {
+          const uint32_t s0 = start + k * static_cast<uint32_t>(c.chunk);
+          const uint32_t e0 = min(s0 + static_cast<uint32_t>(c.chunk), run_end);
+          if (cb + k < c.chunk_cap) c.chunks[cb + k] = make_uint4(s0, e0, key, slot);
+        }
       }
     }
     __syncthreads();
@@ -141,6 +146,46 @@ __device__ __forceinline__ void apply_row_group(WT* wrow, float* state_ptr, Acc 
   }
 }
 
+// The same optimizer step for a row whose weights (raw vectors wv) and state (s_old) were
+// loaded before the gradient sum.
+template <typename WT, int OPT, typename Acc, int VPL>
+__device__ __forceinline__ void apply_row_prefetched(
+    WT* wrow, float* state_ptr, float s_old,
+    const typename VecIO<WT, 4 * sizeof(WT)>::Raw (&wv)[VPL], Acc (&g)[VPL][4], int li, int lanes,
+    int nv, int D, float lr, float eps, unsigned mask) {
+  using IO = VecIO<WT, 4 * sizeof(WT)>;
+  using Raw = typename IO::Raw;
+  Acc scale = static_cast<Acc>(lr);
+  if (OPT == TBE_OPT_ROWWISE_ADAGRAD) {
+    Acc ss = 0;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      if (li + j * lanes < nv)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ss += g[j][i] * g[j][i];
+    for (int m = lanes >> 1; m > 0; m >>= 1) ss += __shfl_xor_sync(mask, ss, m);
+    const Acc s_new = static_cast<Acc>(s_old) + ss / static_cast<Acc>(D);
+    if (li == 0) *state_ptr = static_cast<float>(s_new);
+    if constexpr (sizeof(Acc) == 8)
+      scale = static_cast<Acc>(lr) / (sqrt(s_new) + static_cast<Acc>(eps));
+    else
+      scale = lr / (sqrtf(s_new) + eps);
+  }
+  Raw* out = reinterpret_cast<Raw*>(wrow);
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int vec = li + j * lanes;
+    if (vec < nv) {
+      float f[4];
+      IO::unpack(wv[j], f);
+      float o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = static_cast<float>(static_cast<Acc>(f[i]) - scale * g[j][i]);
+      out[vec] = IO::pack(o);
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // short runs
 // ------------------------------------------------------------------------------------------
@@ -150,14 +195,16 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
                                                             const float* __restrict__ sorted_psw) {
   using Acc = typename WTraits<WT>::Acc;
   constexpr int GPW = kWarp / LPR;  // runs per warp
-  constexpr int UNROLL = 4;
+  constexpr int UNROLL = 4;  // gradient rows in flight per run
   const int lane = lane_id();
   const int g = lane / LPR, li = lane % LPR;
   const unsigned gmask = LPR == kWarp ? FULL : (((1u << LPR) - 1u) << (g * LPR));
   const uint32_t count = min(c.counters[TBE_CNT_SHORT0 + bucket], c.short_cap[bucket]);
-  const uint32_t* list = c.short_list[bucket];
+  const uint4* list = c.short_list[bucket];
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / kWarp;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) / kWarp;
+  using IO = VecIO<WT, 4 * sizeof(WT)>;
+  using Raw = typename IO::Raw;
 
   int64_t claim_base = 0, claim_left = 0;
   int64_t it = 0;
@@ -179,18 +226,26 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
     }
     if (base >= count) break;  // warp-uniform
     const int64_t i = base + g;
-    uint32_t key = 0, off = 0, len = 0;
-    if (i < count) {
-      const uint32_t r = list[i];
-      key = c.unique[r];
-      off = c.run_off[r];
-      len = c.run_off[r + 1] - off;
-    }
-    const int t = table_of_row(c.roff, c.T, key);
+    uint4 rec = make_uint4(0, 0, 0, 0);  // {first lookup, length, key, table}
+    if (i < count) rec = __ldg(list + i);
+    const uint32_t off = rec.x, len = rec.y, key = rec.z;
+    const int t = static_cast<int>(rec.w);
     const int col0 = __ldg(c.doff + t);
     const int D = __ldg(c.doff + t + 1) - col0;
     const int nv = D / 4;
     const uint32_t maxlen = __reduce_max_sync(FULL, len);
+
+    // the row and its state do not depend on the gradient: fetch them first
+    WT* wrow = static_cast<WT*>(c.weights) + __ldg(c.woff + t) +
+               (static_cast<int64_t>(key) - __ldg(c.roff + t)) * D;
+    Raw wv[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int vec = li + j * LPR;
+      wv[j] = (len > 0 && vec < nv) ? reinterpret_cast<const Raw*>(wrow)[vec] : Raw{};
+    }
+    float s_old = 0.f;
+    if (OPT == TBE_OPT_ROWWISE_ADAGRAD && len > 0) s_old = c.state[key];
 
     Acc acc[VPL][4];
 #pragma unroll
@@ -237,11 +292,8 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
           }
       }
     }
-    if (len > 0) {
-      const int64_t row = static_cast<int64_t>(key) - __ldg(c.roff + t);
-      WT* wrow = static_cast<WT*>(c.weights) + __ldg(c.woff + t) + row * D;
-      apply_row_group<WT, OPT, Acc, VPL>(wrow, c.state + key, acc, li, LPR, nv, D, c.lr, c.eps, gmask);
-    }
+    if (len > 0) apply_row_prefetched<WT, OPT, Acc, VPL>(wrow, c.state + key, s_old, wv, acc, li, LPR, nv, D,
+                                                        c.lr, c.eps, gmask);
   }
 }
 
@@ -299,11 +351,11 @@ __device__ __forceinline__ void apply_from_workspace(const BwdCtx& c, uint32_t k
 }
 
 template <typename WT, bool PSW, int OPT, int MAXV, bool FUSED, bool PERSIST>
-__global__ void __launch_bounds__(kThreads) long_chunk_kernel(BwdCtx c,
-                                                             const uint32_t* __restrict__ sorted_vals,
-                                                             const float* __restrict__ sorted_psw) {
+__global__ void __launch_bounds__(kThreads, 4) long_chunk_kernel(BwdCtx c,
+                                                                const uint32_t* __restrict__ sorted_vals,
+                                                                const float* __restrict__ sorted_psw) {
   using Acc = typename WTraits<WT>::Acc;
-  constexpr int UNROLL = 4;
+  constexpr int UNROLL = MAXV == 1 ? 8 : 4;  // rows in flight per lane
   const int lane = lane_id();
   const uint32_t nchunks = min(c.counters[TBE_CNT_CHUNKS], c.chunk_cap);
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / kWarp;
@@ -321,14 +373,9 @@ __global__ void __launch_bounds__(kThreads) long_chunk_kernel(BwdCtx c,
       ++it;
     }
     if (ci >= nchunks) break;
-    const uint2 desc = c.chunks[ci];
-    const uint32_t slot = desc.x;
+    const uint4 rec = __ldg(c.chunks + ci);  // {first lookup, end, key, slot}
+    const uint32_t s = rec.x, e = rec.y, key = rec.z, slot = rec.w;
     if (slot >= c.long_cap) continue;
-    const uint32_t r = c.long_list[slot];
-    const uint32_t key = c.unique[r];
-    const uint32_t run_beg = c.run_off[r], run_end = c.run_off[r + 1];
-    const uint32_t s = run_beg + desc.y * static_cast<uint32_t>(c.chunk);
-    const uint32_t e = min(s + static_cast<uint32_t>(c.chunk), run_end);
     const int t = table_of_row(c.roff, c.T, key);
     const int col0 = __ldg(c.doff + t);
     const int D = __ldg(c.doff + t + 1) - col0;
@@ -352,17 +399,17 @@ __global__ void __launch_bounds__(kThreads) long_chunk_kernel(BwdCtx c,
         if (PSW) my_w = __ldg(sorted_psw + base + lane);
         my_ok = my_b < c.B;
       }
+      const int32_t bag = my_ok ? static_cast<int32_t>(my_b) : -1;
       for (int j = 0; j < n; j += rps * UNROLL) {
         float4 v[UNROLL][MAXV];
         float w[UNROLL];
 #pragma unroll
         for (int q = 0; q < UNROLL; ++q) {
           const int rr = j + q * rps + rs;
-          const int src = rr & (kWarp - 1);
-          const uint32_t b = __shfl_sync(FULL, my_b, src);
-          const bool ok = __shfl_sync(FULL, static_cast<int>(my_ok), src) && rr < n;
-          w[q] = PSW ? __shfl_sync(FULL, my_w, src) : 1.f;
-          const float4* grow = reinterpret_cast<const float4*>(c.grad_out + static_cast<int64_t>(b) * c.total_D + col0);
+          const int32_t b = __shfl_sync(FULL, bag, rr & (kWarp - 1));
+          const bool ok = b >= 0 && rr < n;
+          w[q] = PSW ? __shfl_sync(FULL, my_w, rr & (kWarp - 1)) : 1.f;
+          const float4* grow = reinterpret_cast<const float4*>(c.grad_out + static_cast<int64_t>(ok ? b : 0) * c.total_D + col0);
 #pragma unroll
           for (int k = 0; k < MAXV; ++k) {
             const int vec = vi + k * kWarp;
@@ -450,7 +497,8 @@ cudaError_t launch_short_t(const BwdCtx& c, int bucket, const uint32_t* vals, co
 template <typename WT, bool PSW, int OPT>
 cudaError_t launch_short_bucket(const BwdCtx& c, int bucket, const uint32_t* vals, const float* psw,
                                 bool persist, const DeviceInfo& dev, cudaStream_t s) {
-  switch (bucket) {  // next_pow2(D) = 2^bucket; float4 slices per row = 2^(bucket-2)
+  // next_pow2(D) = 2^bucket; float4 slices per row = 2^(bucket-2): min(32, slices) lanes per run
+  switch (bucket) {
     case 2: return launch_short_t<WT, PSW, OPT, 1, 1>(c, bucket, vals, psw, persist, dev, s);
     case 3: return launch_short_t<WT, PSW, OPT, 2, 1>(c, bucket, vals, psw, persist, dev, s);
     case 4: return launch_short_t<WT, PSW, OPT, 4, 1>(c, bucket, vals, psw, persist, dev, s);

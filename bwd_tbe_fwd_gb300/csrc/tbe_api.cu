@@ -133,7 +133,9 @@ BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const Device
   int bits = 1;
   while ((int64_t(1) << bits) <= P.total_rows) ++bits;
   L.key_bits = bits;
-  L.passes = (bits + kRadixBits - 1) / kRadixBits;
+  L.passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
+  L.radix_bits = (bits + L.passes - 1) / L.passes;
+  if (L.radix_bits < 8) L.radix_bits = 8;
   L.final_buf = L.passes & 1;
   const int64_t tiles = (static_cast<int64_t>(n_cap) + kSortTile - 1) / kSortTile;
   int64_t sg = dev.sms * 3;
@@ -167,14 +169,15 @@ BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const Device
     L.vals[b] = take(sizeof(uint32_t) * n_cap);
     L.psw[b] = P.weighted ? take(sizeof(float) * n_cap) : 0;
   }
-  L.sort_counts = take(sizeof(uint32_t) * kRadix * L.sort_grid);
+  L.sort_counts = take(sizeof(uint32_t) * (size_t(1) << L.radix_bits) * L.sort_grid);
+  L.sort_totals = take(sizeof(uint32_t) * (size_t(1) << L.radix_bits));
   L.rle_counts = take(sizeof(uint32_t) * L.rle_grid);
   L.unique = take(sizeof(uint32_t) * L.u_cap);
   L.run_off = take(sizeof(uint32_t) * (L.u_cap + 1));
   L.run_len = take(sizeof(uint32_t) * L.u_cap);
-  for (int k = 0; k < kNumBuckets; ++k) L.short_list[k] = take(sizeof(uint32_t) * L.short_cap[k]);
+  for (int k = 0; k < kNumBuckets; ++k) L.short_list[k] = take(sizeof(uint4) * L.short_cap[k]);
   L.long_list = take(sizeof(uint32_t) * L.long_cap);
-  L.chunks = take(sizeof(uint2) * L.chunk_cap);
+  L.chunks = take(sizeof(uint4) * L.chunk_cap);
   L.countdown = take(sizeof(uint32_t) * L.long_cap);
   L.ws_rows = take(static_cast<size_t>(L.long_cap) * P.max_D * L.acc_bytes);
   L.total = off;
@@ -217,16 +220,17 @@ BwdCtx make_ctx(const Problem& P, const tbe_options& o, const BwdLayout& L, cons
     c.pswbuf[b] = P.weighted ? reinterpret_cast<float*>(base + L.psw[b]) : nullptr;
   }
   c.sort_counts = reinterpret_cast<uint32_t*>(base + L.sort_counts);
+  c.sort_totals = reinterpret_cast<uint32_t*>(base + L.sort_totals);
   c.rle_counts = reinterpret_cast<uint32_t*>(base + L.rle_counts);
   c.unique = reinterpret_cast<uint32_t*>(base + L.unique);
   c.run_off = reinterpret_cast<uint32_t*>(base + L.run_off);
   c.run_len = reinterpret_cast<uint32_t*>(base + L.run_len);
   for (int k = 0; k < kNumBuckets; ++k) {
-    c.short_list[k] = reinterpret_cast<uint32_t*>(base + L.short_list[k]);
+    c.short_list[k] = reinterpret_cast<uint4*>(base + L.short_list[k]);
     c.short_cap[k] = L.short_cap[k];
   }
   c.long_list = reinterpret_cast<uint32_t*>(base + L.long_list);
-  c.chunks = reinterpret_cast<uint2*>(base + L.chunks);
+  c.chunks = reinterpret_cast<uint4*>(base + L.chunks);
   c.countdown = reinterpret_cast<uint32_t*>(base + L.countdown);
   c.ws_rows = base + L.ws_rows;
   c.long_cap = L.long_cap;

@@ -22,8 +22,8 @@ constexpr int kMaxD = 1024;
 constexpr int kSortThreads = 256;
 constexpr int kSortItems = 16;
 constexpr int kSortTile = kSortThreads * kSortItems;  // keys per radix-sort tile
-constexpr int kRadixBits = 8;
-constexpr int kRadix = 1 << kRadixBits;
+constexpr int kMaxRadixBits = 10;                     // digits of 8..10 bits: passes = ceil(bits/10)
+constexpr int kMaxRadix = 1 << kMaxRadixBits;
 constexpr int kExpandBags = 512;                        // bags per expand CTA
 
 // ------------------------------------------------------------------------------------------
@@ -58,13 +58,13 @@ tbe_status device_info(DeviceInfo* out);
 // Layout of the backward workspace (byte offsets from the 256-aligned base).
 struct BwdLayout {
   size_t counters = 0, keys[2] = {0, 0}, vals[2] = {0, 0}, psw[2] = {0, 0};
-  size_t sort_counts = 0, rle_counts = 0, unique = 0, run_off = 0, run_len = 0;
+  size_t sort_counts = 0, sort_totals = 0, rle_counts = 0, unique = 0, run_off = 0, run_len = 0;
   size_t short_list[kNumBuckets] = {0};
   size_t long_list = 0, chunks = 0, countdown = 0, ws_rows = 0;
   size_t total = 0;
   uint32_t short_cap[kNumBuckets] = {0};
   uint32_t long_cap = 0, chunk_cap = 0, u_cap = 0, n_cap = 0;
-  int sort_grid = 1, rle_grid = 1, key_bits = 1, passes = 1, final_buf = 0;
+  int sort_grid = 1, rle_grid = 1, key_bits = 1, passes = 1, radix_bits = 8, final_buf = 0;
   int acc_bytes = 4;  // fp32 workspace rows (fp64 for fp32 tables)
 };
 
@@ -109,14 +109,15 @@ struct BwdCtx {
   uint32_t* vals[2];
   float* pswbuf[2];
   uint32_t* sort_counts;
+  uint32_t* sort_totals;
   uint32_t* rle_counts;
   uint32_t* unique;
   uint32_t* run_off;
   uint32_t* run_len;
-  uint32_t* short_list[kNumBuckets];
+  uint4* short_list[kNumBuckets];  // per short run: {first lookup, length, key, table}
   uint32_t short_cap[kNumBuckets];
-  uint32_t* long_list;
-  uint2* chunks;
+  uint32_t* long_list;              // run id of each long run (its slot)
+  uint4* chunks;                    // per chunk: {first lookup, end, key, slot}
   uint32_t* countdown;
   void* ws_rows;
   uint32_t long_cap, chunk_cap, u_cap;
