@@ -122,7 +122,14 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None):
     D = cfg.D.astype(np.int64)
     N, TB = st["N"], cfg.T * cfg.B
     pw = 4 if cfg.weighted else 0
-    fwd = int(np.sum(st["per_table"] * (D * wb + ib + pw)) + TB * ib + cfg.B * int(D.sum()) * 4)
+    # tables served by the counts x table path (the library's eligibility rule)
+    hist = np.array([t.histogram and cfg.wdtype == "f16" and not cfg.weighted and t.E <= 64 and 64 <= t.D <= 128
+                     for t in cfg.tables])
+    per_lookup = st["per_table"] * (D * wb + ib + pw)
+    fwd = int(np.sum(per_lookup[~hist]) + int((~hist).sum()) * cfg.B * ib + cfg.B * int(D[~hist].sum()) * 4)
+    hist_bytes = int(np.sum(st["per_table"][hist] * ib) + int(hist.sum()) * cfg.B * ib
+                     + cfg.B * int(D[hist].sum()) * 4 + int(np.sum(cfg.E[hist] * D[hist] * wb)))
+    hist_flops = int(np.sum(2 * cfg.B * cfg.E[hist] * D[hist]))
     bounds = (TB + 1) * ib + N * ib
     if passes is None:  # the library's choice: digits of 8-10 bits, ceil(bits / 10) passes
         bits = 1
@@ -140,8 +147,8 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None):
     nch = -(-L[~short] // chunk)
     upd_long = int(np.sum(L[~short] * (4 + pw + Dr[~short] * 4) + nch * Dr[~short] * 8
                           + 2 * Dr[~short] * wb + 8 + Dr[~short] * 4))
-    return dict(bounds=bounds, gather=fwd, expand=expand, sort=sort, rle=rle, classify=classify,
-                short=upd_short, long=upd_long, apply=0,
+    return dict(bounds=bounds, gather=fwd, histogram=hist_bytes, histogram_flops=hist_flops, expand=expand,
+                sort=sort, rle=rle, classify=classify, short=upd_short, long=upd_long, apply=0,
                 lookups_short=int(L[short].sum()), lookups_long=int(L[~short].sum()),
                 runs_short=int(short.sum()), runs_long=int((~short).sum()), passes=passes)
 
@@ -407,7 +414,9 @@ def run_ours(args):
         stages[name] = {"ms": round(float(ms), 4), "algorithmic_GB": round(gb, 4),
                         "GBps": round(gb / (ms / 1e3), 1) if ms > 0 and gb > 0 else None,
                         "frac": round(gb / (ms / 1e3) / peak, 4) if ms > 0 and gb > 0 else None}
-    kernel_stages = ("gather", "short", "long")
+    if model["histogram_flops"] > 0 and stage_ms["histogram"] > 0:
+        stages["histogram"]["tensor_TFLOPs"] = round(model["histogram_flops"] / (stage_ms["histogram"] / 1e3) / 1e12, 3)
+    kernel_stages = ("gather", "histogram", "short", "long")
     dom = max(kernel_stages, key=lambda n: stage_ms[n])
     achieved = model[dom] / 1e9 / (stage_ms[dom] / 1e3)
     traffic = profiled_traffic(dom, cfg.name)

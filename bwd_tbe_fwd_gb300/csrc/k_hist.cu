@@ -7,16 +7,18 @@
 // where count[b, e] counts the bag's first 256 ids equal to e; ids after the 256th are added by a
 // scalar path.  The pages evaluate counts x table with a Triton dot over 16 bags per program.
 //
-// GB300 design: a persistent CTA of 128 threads (4 warps) owns TMEM columns for one 128 x D fp32
+// GB300 design: a persistent CTA of 256 threads owns TMEM columns for one 128 x D fp32
 // accumulator and keeps the table in shared memory as the B operand.  Per tile of 128 bags:
-//   1. each warp histograms 32 bags: coalesced loads of 32 ids at a time, shared-memory atomics
-//      into uint32 counters [128 bags][64 rows];
-//   2. each thread converts its bag's 64 counts to fp16 (exact: counts <= 256) into the A tile,
-//      in the canonical K-major layout without swizzle (8 x 16-byte core matrices);
-//   3. one thread issues four tcgen05.mma.cta_group::1.kind::f16 (M=128, N=D rounded up to 16,
+//   1. the tile's 129 offsets go to shared memory; all 256 threads stream the tile's contiguous
+//      id range with 16 coalesced loads in flight each, find every id's bag by binary search over
+//      the offsets, and for ids among the first 256 of their bag count them with 32-bit
+//      shared-memory atomics on packed 16-bit pairs; the counts are then written as the fp16 A
+//      tile (counts <= 256 are exact in fp16) in the canonical K-major layout without swizzle
+//      (8 x 16-byte core matrices);
+//   2. one thread issues four tcgen05.mma.cta_group::1.kind::f16 (M=128, N=D rounded up to 16,
 //      K=16 each) and commits them to an mbarrier; the CTA waits on it (bounded);
-//   4. each warp reads its 32 accumulator lanes (one bag per thread) with tcgen05.ld 32x32b.x32,
-//      adds the rows of ids past the 256th, and stores the pooled row.
+//   3. warps 0-3 read their 32 accumulator lanes each (one bag per thread) with tcgen05.ld
+//      32x32b.x32, add the rows of ids past the 256th, and store the pooled row.
 // Counts x table is exact up to fp32 rounding, so the result equals the gather's sum.
 #include <atomic>
 
@@ -25,7 +27,8 @@
 namespace tbe {
 namespace {
 
-constexpr int kThreads = 128;       // one bag per thread; M = 128
+constexpr int kThreads = 256;       // 8 warps count; warps 0-3 (one bag per thread) read TMEM
+constexpr int kIdsPerThread = 16;   // ids in flight per thread while counting
 constexpr int kM = 128;
 constexpr int kK = 64;              // E padded to 64
 constexpr int kMaxN = 128;          // D <= 128
@@ -33,6 +36,7 @@ constexpr int kHistIds = 256;       // ids per bag counted by the histogram
 constexpr int kTileBytes = kM * kK * 2;  // A tile: 128 x 64 fp16 = 16 KB (B tile: 128 x 64 as well)
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr unsigned FULL = 0xffffffffu;
 // canonical K-major layout without swizzle: core matrices of 8 rows x 16 bytes; adjacent core
 // matrices are 128 B apart along K (LBO) and 8 * 128 = 1024 B apart along M/N (SBO)
 constexpr uint32_t kLBO = 128;
@@ -117,16 +121,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 template <typename IT>
-__global__ void __launch_bounds__(kThreads) hist_tc_kernel(HistArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   // tiles 1024-byte aligned within the shared window (the launch adds 1 KB of slack)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* a_tile = smem;                                   // 16 KB
-  uint8_t* b_tile = smem + kTileBytes;                      // 16 KB
-  uint32_t* counts = reinterpret_cast<uint32_t*>(smem + 2 * kTileBytes);  // [128][64] = 32 KB
+  uint8_t* a_tile = smem;                                   // 16 KB: counts as fp16
+  uint8_t* b_tile = smem + kTileBytes;                      // 16 KB: the table
+  uint32_t* pairs = reinterpret_cast<uint32_t*>(smem + 2 * kTileBytes);  // 16 KB: [128][32] count pairs
   __shared__ __align__(8) uint64_t mma_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_failed;
+  __shared__ int64_t s_off[kM + 1];
+  __shared__ int s_rel[kM + 1];
 
   const int tid = threadIdx.x, lane = lane_id(), warp = tid / kWarp;
   const int64_t tiles = (a.B + kM - 1) / kM;
@@ -162,34 +168,69 @@ __global__ void __launch_bounds__(kThreads) hist_tc_kernel(HistArgs a) {
 
   for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int64_t b0 = tile * kM;
-    // 1. histogram of the first 256 ids of each bag
-    for (int i = tid; i < kM * kK; i += kThreads) counts[i] = 0;
+    // 1. histogram of the first 256 ids of each bag, straight into the fp16 A tile
+    const int nb = static_cast<int>(min(static_cast<int64_t>(kM), a.B - b0));
+    for (int i = tid; i < kM * kK / 2 / 4; i += kThreads) reinterpret_cast<uint4*>(pairs)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i <= kM; i += kThreads) {
+      const int64_t o = clamp64(ld_int<IT>(a.offsets, a.bag0 + b0 + min(i, nb)), 0, a.num_indices);
+      s_off[i] = o;
+    }
     __syncthreads();
-    for (int m = warp * kWarp; m < warp * kWarp + kWarp; ++m) {
-      const int64_t b = b0 + m;
-      if (b >= a.B) break;
-      const int64_t s = clamp64(ld_int<IT>(a.offsets, a.bag0 + b), 0, a.num_indices);
-      const int64_t e = min(clamp64(ld_int<IT>(a.offsets, a.bag0 + b + 1), s, a.num_indices), s + kHistIds);
+    for (int i = 1; i <= nb; ++i) {  // guard: never let a bag end before it starts
+      if (tid == 0 && s_off[i] < s_off[i - 1]) s_off[i] = s_off[i - 1];
+    }
+    __syncthreads();
+    {
+      // positions relative to the tile's first lookup (32-bit), bag starts in shared memory
+      const int64_t p0 = s_off[0];
+      const int rel_end = static_cast<int>(s_off[nb] - p0);
+      for (int i = tid; i <= nb; i += kThreads) s_rel[i] = static_cast<int>(s_off[i] - p0);
+      __syncthreads();
+      const IT* ids = static_cast<const IT*>(a.indices) + p0;
       uint32_t bad = 0;
-      for (int64_t p = s + lane; p < e; p += kWarp) {
-        const int64_t id = ld_int<IT>(a.indices, p);
-        if (id >= 0 && id < a.E) atomicAdd(&counts[m * kK + id], 1u);
-        else ++bad;
+      int lo = 0, cur = 0, nxt = nb > 0 ? s_rel[1] : 0x7fffffff;  // this thread's bag and its bounds
+      for (int base = 0; base < rel_end; base += kThreads * kIdsPerThread) {
+        IT id[kIdsPerThread];
+#pragma unroll
+        for (int j = 0; j < kIdsPerThread; ++j) {
+          const int r = base + j * kThreads + tid;
+          id[j] = r < rel_end ? __ldg(ids + r) : IT(0);
+        }
+#pragma unroll
+        for (int j = 0; j < kIdsPerThread; ++j) {
+          const int r = base + j * kThreads + tid;
+          if (r >= rel_end) continue;
+          while (r >= nxt) {  // positions only increase: walk forward to r's bag
+            ++lo;
+            cur = nxt;
+            nxt = lo + 1 <= nb ? s_rel[lo + 1] : 0x7fffffff;
+          }
+          if (r - cur >= kHistIds) continue;  // the scalar path adds it
+          if (static_cast<uint64_t>(static_cast<int64_t>(id[j])) >= static_cast<uint64_t>(a.E)) {
+            ++bad;
+            continue;
+          }
+          const uint32_t k = static_cast<uint32_t>(id[j]);
+          // two 16-bit counts per word (counts <= 256 never carry into the neighbour)
+          atomicAdd(&pairs[lo * (kK / 2) + (k >> 1)], (k & 1u) << 16 | (~k & 1u));
+        }
       }
       if (bad) stat_add(a.stats, TBE_STAT_UNREPAIRED, bad);
     }
     __syncthreads();
-    // 2. counts -> fp16 A tile (row = bag = tid)
-#pragma unroll
-    for (int kb = 0; kb < kK; kb += 8) {
+    // counts -> fp16 A tile (exact: counts <= 256), 8 counts (one 16-byte row of a core matrix)
+    // per item
+    for (int q = tid; q < kM * (kK / 8); q += kThreads) {
+      const int m = q / (kK / 8), kb = (q % (kK / 8)) * 8;
+      const uint4 c = *reinterpret_cast<const uint4*>(&pairs[m * (kK / 2) + kb / 2]);
+      const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
       uint32_t w[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const __half h0 = __uint2half_rn(counts[tid * kK + kb + 2 * j]);
-        const __half h1 = __uint2half_rn(counts[tid * kK + kb + 2 * j + 1]);
+        const __half h0 = __uint2half_rn(cw[j] & 0xFFFFu), h1 = __uint2half_rn(cw[j] >> 16);
         w[j] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
       }
-      *reinterpret_cast<uint4*>(a_tile + kmajor_offset(tid, kb)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(a_tile + kmajor_offset(m, kb)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     fence_proxy_async_smem();  // the tensor core reads the tile through the async proxy
     tc_fence_before();
@@ -214,31 +255,32 @@ __global__ void __launch_bounds__(kThreads) hist_tc_kernel(HistArgs a) {
     }
     phase ^= 1u;
     tc_fence_after();
-    // 4. read this thread's bag row out of TMEM, add the ids past the 256th, store
-    const int64_t b = b0 + tid;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * kWarp) << 16);
-    int64_t ts = 0, te = 0;
-    if (b < a.B) {
-      const int64_t s = clamp64(ld_int<IT>(a.offsets, a.bag0 + b), 0, a.num_indices);
-      te = clamp64(ld_int<IT>(a.offsets, a.bag0 + b + 1), s, a.num_indices);
-      ts = min(te, s + kHistIds);
-    }
-    for (int c0 = 0; c0 < a.N; c0 += 32) {
-      float v[32];
-      tmem_ld32(lane_addr + c0, v);  // warp-wide: every lane takes part
-      if (b < a.B) {
-        for (int64_t p = ts; p < te; ++p) {  // the scalar path of ids past the 256th
-          const int64_t id = ld_int<IT>(a.indices, p);
-          if (id < 0 || id >= a.E) continue;
-          const __half* row = a.table + id * a.D + c0;
+    // 3. warps 0-3 read their bag rows out of TMEM, add the ids past the 256th, store
+    if (warp < kM / kWarp) {
+      const int64_t b = b0 + tid;
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * kWarp) << 16);
+      int64_t ts = 0, te = 0;
+      if (tid < nb) {
+        te = s_off[tid + 1];
+        ts = min(te, s_off[tid] + kHistIds);
+      }
+      for (int c0 = 0; c0 < a.N; c0 += 32) {
+        float v[32];
+        tmem_ld32(lane_addr + c0, v);  // warp-wide: every lane takes part
+        if (tid < nb) {
+          for (int64_t p = ts; p < te; ++p) {  // the scalar path of ids past the 256th
+            const int64_t id = ld_int<IT>(a.indices, p);
+            if (id < 0 || id >= a.E) continue;
+            const __half* row = a.table + id * a.D + c0;
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c0 + i < a.D) v[i] += __half2float(row[i]);
+            for (int i = 0; i < 32; ++i)
+              if (c0 + i < a.D) v[i] += __half2float(row[i]);
+          }
+          float* orow = a.out + b * a.total_D + a.col0 + c0;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            if (c0 + i < a.D) __stcs(reinterpret_cast<float4*>(orow + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
         }
-        float* orow = a.out + b * a.total_D + a.col0 + c0;
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          if (c0 + i < a.D) __stcs(reinterpret_cast<float4*>(orow + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
       }
     }
     tc_fence_before();
@@ -283,7 +325,7 @@ cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, co
   a.total_D = P.total_D;
   a.stats = stats;
   if (P.B == 0) return cudaSuccess;
-  const size_t smem = 2 * kTileBytes + sizeof(uint32_t) * kM * kK + 1024;  // + alignment slack
+  const size_t smem = 3 * kTileBytes + 1024;  // A, B, count pairs + alignment slack
   auto k = P.itype == TBE_I32 ? hist_tc_kernel<int32_t> : hist_tc_kernel<int64_t>;
   // opt-in shared memory is a per-device function attribute: set it once per device
   static std::atomic<uint64_t> attr_set[2] = {{0}, {0}};
@@ -298,8 +340,8 @@ cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, co
     flag.fetch_or(bit);
   }
   const int64_t tiles = (P.B + kM - 1) / kM;
-  // at most 3 CTAs per SM: 3 x 128 TMEM columns fit in the SM's 512 without waiting
-  int64_t grid = static_cast<int64_t>(dev.sms) * 3;
+  // at most 4 CTAs per SM: 4 x 128 TMEM columns fit in the SM's 512 without waiting
+  int64_t grid = static_cast<int64_t>(dev.sms) * 4;
   if (tiles < grid) grid = tiles;
   k<<<static_cast<int>(grid), kThreads, smem, s>>>(a);
   note_launch();

@@ -8,7 +8,8 @@
 // lengths and start offsets.
 //
 // GB300 design:
-//   expand      one CTA per 512 consecutive bags; their lookups are one contiguous range, read
+//   expand      one CTA per 32-512 consecutive bags (about 16K lookups from the mean bag length);
+//               their lookups are one contiguous range, read
 //               coalesced; each lookup finds its bag by binary search over the CTA's offsets in
 //               shared memory and writes key = row_offsets[t] + id (uint32) and its bag b
 //               (plus its per-sample weight when weighted).
@@ -42,6 +43,7 @@ struct ExpandArgs {
   const int64_t* roff;
   int64_t B, TB, num_indices;
   uint32_t sentinel;  // key of an out-of-range id: sum of E (sorts after every real row)
+  int bags_per_cta;   // <= kExpandBags
   uint32_t* keys;
   uint32_t* vals;
   float* psw_out;
@@ -54,8 +56,8 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
   __shared__ int64_t s_off[kExpandBags + 1];
   __shared__ unsigned long long s_bad;
   const int64_t N = clamp64(ld_int<IT>(a.offsets, a.TB), 0, a.num_indices);
-  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kExpandBags;
-  const int nb = static_cast<int>(min(static_cast<int64_t>(kExpandBags), a.TB - i0));
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * a.bags_per_cta;
+  const int nb = static_cast<int>(min(static_cast<int64_t>(a.bags_per_cta), a.TB - i0));
   if (threadIdx.x == 0) {
     s_bad = 0;
     if (blockIdx.x == 0) a.counters[TBE_CNT_N] = static_cast<uint32_t>(N);
@@ -469,7 +471,12 @@ cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s) {
   a.psw_out = c.pswbuf[0];
   a.counters = c.counters;
   a.stats = c.stats;
-  const int64_t grid64 = (c.TB + kExpandBags - 1) / kExpandBags;
+  // about 16K lookups per CTA: bags per CTA from the mean bag length the host can see
+  const int64_t mean_len = c.TB > 0 ? (c.num_indices + c.TB - 1) / c.TB : 1;
+  int bpc = kExpandBags;
+  while (bpc > 32 && static_cast<int64_t>(bpc) * mean_len > 16384) bpc >>= 1;
+  a.bags_per_cta = bpc;
+  const int64_t grid64 = (c.TB + bpc - 1) / bpc;
   const int grid = static_cast<int>(grid64 < 1 ? 1 : grid64);
   const bool psw = P.weighted;
   if (P.itype == TBE_I32) {
