@@ -44,6 +44,7 @@ def parse_args():
     ap.add_argument("--config", default="c3", help="workload: c1..c5 (default c3, the large skew batch)")
     ap.add_argument("--long-mode", choices=["auto", "two_kernel", "fused"], default="auto")
     ap.add_argument("--scheduler", choices=["grid", "persistent"], default="grid")
+    ap.add_argument("--classify", choices=["atomic", "ordered"], default="atomic")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tables", type=int, default=0,
@@ -338,7 +339,8 @@ def run_ours(args):
     batch = make_batch(cfg)
     st = batch_stats(cfg, batch)
     opts = TBEOptions(long_mode={"auto": 0, "two_kernel": 1, "fused": 2}[args.long_mode],
-                      scheduler={"grid": 0, "persistent": 1}[args.scheduler])
+                      scheduler={"grid": 0, "persistent": 1}[args.scheduler],
+                      classify_mode={"atomic": 0, "ordered": 1}[args.classify])
     itype = torch.int32 if cfg.itype == "i32" else torch.int64
     tbe = TableBatchedEmbedding(cfg.D, cfg.E, cfg.B, batch.N, torch_dtype(cfg.wdtype), itype,
                                 weighted=cfg.weighted, long_bags=[t.histogram for t in cfg.tables],
@@ -472,7 +474,7 @@ def run_ours(args):
                 "lookups_per_step": st["N"], "distinct_rows": st["U"], "hottest_row_hits": st["hottest"],
                 "long_runs": model["runs_long"], "lookups_in_long_runs": model["lookups_long"],
                 "weights_storage": cfg.wdtype, "step": "tbe_bounds_check + tbe_forward + tbe_backward_update",
-                "long_mode": args.long_mode, "scheduler": args.scheduler,
+                "long_mode": args.long_mode, "scheduler": args.scheduler, "classify": args.classify,
                 "parallelism": f"replicas x{world}",
                 "l2": "inputs larger than L2 (weights alone exceed 129 MB); no flush between steps",
                 "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),

@@ -56,6 +56,7 @@ tbe_status check_options(const tbe_options& o) {
   if (o.long_mode < TBE_LONG_AUTO || o.long_mode > TBE_LONG_FUSED) return TBE_ERR_INVALID_ARG;
   if (o.scheduler != TBE_SCHED_GRID && o.scheduler != TBE_SCHED_PERSISTENT) return TBE_ERR_INVALID_ARG;
   if (o.num_events < 0 || (o.num_events > 0 && o.events == nullptr)) return TBE_ERR_INVALID_ARG;
+  if (o.classify_mode != TBE_CLASSIFY_ORDERED && o.classify_mode != TBE_CLASSIFY_ATOMIC) return TBE_ERR_INVALID_ARG;
   return TBE_OK;
 }
 }  // namespace
@@ -156,6 +157,11 @@ BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const Device
   L.long_cap = n_cap / static_cast<uint32_t>(opt.long_threshold);
   L.chunk_cap = L.long_cap == 0 ? 0 : L.long_cap + n_cap / static_cast<uint32_t>(opt.chunk) + 1;
   L.acc_bytes = P.wdtype == TBE_F32 ? 8 : 4;
+  int64_t cg = dev.sms * 4;
+  if (cg > 1024) cg = 1024;
+  const int64_t ctiles = (static_cast<int64_t>(L.u_cap) + 255) / 256;
+  if (ctiles < cg) cg = ctiles;
+  L.cls_grid = static_cast<int>(cg < 1 ? 1 : cg);
 
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -180,6 +186,7 @@ BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const Device
   L.chunks = take(sizeof(uint4) * L.chunk_cap);
   L.countdown = take(sizeof(uint32_t) * L.long_cap);
   L.ws_rows = take(static_cast<size_t>(L.long_cap) * P.max_D * L.acc_bytes);
+  L.cls_counts = take(sizeof(uint32_t) * (kNumBuckets + 2) * L.cls_grid);
   L.total = off;
   return L;
 }
@@ -237,6 +244,8 @@ BwdCtx make_ctx(const Problem& P, const tbe_options& o, const BwdLayout& L, cons
   c.chunk_cap = L.chunk_cap;
   c.u_cap = L.u_cap;
   c.sort_grid = L.sort_grid;
+  c.cls_grid = L.cls_grid;
+  c.cls_counts = reinterpret_cast<uint32_t*>(base + L.cls_counts);
   c.rle_grid = L.rle_grid;
   c.stats = reinterpret_cast<unsigned long long*>(d_stats);
   return c;
@@ -281,6 +290,8 @@ void tbe_default_options(tbe_options* opt) {
   opt->fused_bounds = 0;
   opt->events = nullptr;
   opt->num_events = 0;
+  opt->launch_counter = nullptr;
+  opt->classify_mode = TBE_CLASSIFY_ATOMIC;
 }
 
 tbe_status tbe_table_layout(const tbe_problem* prob, int64_t* weight_offsets, int32_t* D_offsets,
@@ -439,7 +450,7 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
   record(o, TBE_BWD_EV_SORT, s);
   if ((e = launch_rle(P, c, L, s)) != cudaSuccess) return cuda_status(e);
   record(o, TBE_BWD_EV_RLE, s);
-  if ((e = launch_classify(P, c, dev, s)) != cudaSuccess) return cuda_status(e);
+  if ((e = launch_classify(P, c, dev, o.classify_mode, s)) != cudaSuccess) return cuda_status(e);
   record(o, TBE_BWD_EV_CLASSIFY, s);
   if ((e = launch_short_updates(P, c, L, optimizer, o.scheduler, dev, s)) != cudaSuccess)
     return cuda_status(e);

@@ -60,11 +60,11 @@ struct BwdLayout {
   size_t counters = 0, keys[2] = {0, 0}, vals[2] = {0, 0}, psw[2] = {0, 0};
   size_t sort_counts = 0, sort_totals = 0, rle_counts = 0, unique = 0, run_off = 0, run_len = 0;
   size_t short_list[kNumBuckets] = {0};
-  size_t long_list = 0, chunks = 0, countdown = 0, ws_rows = 0;
+  size_t long_list = 0, chunks = 0, countdown = 0, ws_rows = 0, cls_counts = 0;
   size_t total = 0;
   uint32_t short_cap[kNumBuckets] = {0};
   uint32_t long_cap = 0, chunk_cap = 0, u_cap = 0, n_cap = 0;
-  int sort_grid = 1, rle_grid = 1, key_bits = 1, passes = 1, radix_bits = 8, final_buf = 0;
+  int sort_grid = 1, rle_grid = 1, cls_grid = 1, key_bits = 1, passes = 1, radix_bits = 8, final_buf = 0;
   int acc_bytes = 4;  // fp32 workspace rows (fp64 for fp32 tables)
 };
 
@@ -121,7 +121,8 @@ struct BwdCtx {
   uint32_t* countdown;
   void* ws_rows;
   uint32_t long_cap, chunk_cap, u_cap;
-  int sort_grid, rle_grid;
+  int sort_grid, rle_grid, cls_grid;
+  uint32_t* cls_counts;             // [lists][cls_grid] per-block counts, then their prefixes
   unsigned long long* stats;
 };
 
@@ -145,7 +146,7 @@ cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, co
 cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s);
 cudaError_t launch_sort(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s);
 cudaError_t launch_rle(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s);
-cudaError_t launch_classify(const Problem& P, const BwdCtx& c, const DeviceInfo& dev, cudaStream_t s);
+cudaError_t launch_classify(const Problem& P, const BwdCtx& c, const DeviceInfo& dev, int mode, cudaStream_t s);
 cudaError_t launch_short_updates(const Problem& P, const BwdCtx& c, const BwdLayout& L,
                                  tbe_optimizer opt, int scheduler, const DeviceInfo& dev,
                                  cudaStream_t s);

@@ -82,6 +82,14 @@ typedef enum { TBE_LONG_AUTO = 0, TBE_LONG_TWO_KERNEL = 1, TBE_LONG_FUSED = 2 } 
  * is left. */
 typedef enum { TBE_SCHED_GRID = 0, TBE_SCHED_PERSISTENT = 1 } tbe_scheduler;
 
+/* How the run classifier compacts runs into its lists ([FBT] section 4: one reservation per
+ * block per list, offsets inside the block from prefix sums, counts kept on the device):
+ * ATOMIC reserves with one atomicAdd per block per list, so the lists come out in arbitrary
+ * block order; ORDERED reserves with a scan over the blocks' counts (no atomics), so the lists
+ * are in key order (three launches instead of one).  Both give the same updates and counts;
+ * ATOMIC, the pages' scheme, is the default. */
+typedef enum { TBE_CLASSIFY_ATOMIC = 0, TBE_CLASSIFY_ORDERED = 1 } tbe_classify_mode;
+
 /* Host description of the problem.  Nothing here is read from the device. */
 typedef struct {
   int32_t T;                  /* tables */
@@ -125,6 +133,7 @@ typedef struct {
   void* const* events;        /* NULL, or cudaEvent_t[TBE_*_NUM_EVENTS] recorded at stage ends */
   int32_t num_events;
   int64_t* launch_counter;    /* NULL, or a HOST counter to which each call adds its kernel launches */
+  int32_t classify_mode;      /* tbe_classify_mode */
 } tbe_options;
 
 /* Indices into d_stats (int64).  Counts accumulate over calls. */
@@ -138,7 +147,7 @@ enum {
 };
 
 /* The defaults: threshold 256, chunk 256, AUTO long mode, GRID scheduler, histogram on,
- * fused bounds off, no events. */
+ * fused bounds off, no events, ORDERED classifier. */
 void tbe_default_options(tbe_options* opt);
 
 /* Fills the host arrays of the canonical packed layout for the problem; the caller copies

@@ -72,6 +72,15 @@ def test_long_modes_and_schedulers(long_mode, scheduler):
         c.backward(options=opts)
 
 
+@pytest.mark.parametrize("name", ["c3", "c5", "c2"])
+def test_ordered_classifier(name):
+    """The order-preserving compaction (a scan over the blocks' counts, lists in key order) gives
+    the same updates and the same route counts as the default atomic one."""
+    opts = TBEOptions(classify_mode=1)
+    c = Case(SMALL[name], options=opts)
+    c.backward(options=opts)
+
+
 def test_skewed_example_batch_routes_as_printed():
     """The tutorial's skewed batch (T=3, E=50, B=16, D=24, seed 1): the device classifier must
     produce the printed short/long/chunk counts for each threshold and chunk size."""
