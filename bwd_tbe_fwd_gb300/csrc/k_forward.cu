@@ -4,16 +4,21 @@
 // path"): for each table and bag, gather the indexed rows, optionally scale them by the
 // per-sample weight, accumulate in fp32 (fp64 for fp32 tables) and write one D-wide pooled
 // output row.  The pages' design is a Triton program per group of bags looping over the tables
-// with four to eight row loads in flight; here the unit of work is one (table, bag) per warp:
-//   * the warp reads up to 32 ids of its bag with one coalesced load and broadcasts them with
-//     shuffles (the id -> row dependence is the latency to hide);
+// with four to eight row loads in flight; here a warp owns a work item of up to 32 consecutive
+// bags of one table:
+//   * the item's offsets come in with one coalesced load (lane k holds bag k's bounds), and
+//     its ids stream through three 32-position register windows, two in use and one in
+//     flight, so a bag's own critical path is only its row loads (offsets -> ids -> rows was
+//     three dependent round trips per bag when each bag fetched its own ids);
 //   * a row of D elements is split into 16-byte vectors; a group of next_pow2(vectors) lanes
 //     covers one row, so one warp-wide load instruction fetches 32/group rows, and UNROLL such
 //     instructions are issued before any is consumed (8 rows in flight per warp for fp16 D=128);
+//   * unweighted 16-bit rows are added into the fp32 sums with the mixed-precision add of
+//     sm_100+ (no separate widening instruction);
 //   * the row groups are reduced with xor-shuffles and one group writes the fp32 result with
 //     streaming 16-byte stores;
-//   * warps walk the (table, bag) units table-major with a grid stride, so the offsets and ids a
-//     CTA reads are contiguous and every warp of a CTA usually sees the same D.
+//   * items are walked table-major with a grid stride, so the CTAs in flight read neighbouring
+//     parts of the index array and mostly one table's rows.
 // Out-of-range ids are repaired to row 0 in flight when fused bounds checking is on (writing
 // the repaired id back), else skipped and counted; no id outside its table is dereferenced.
 #include "tbe_internal.cuh"
@@ -33,6 +38,7 @@ struct FwdArgs {
   int64_t B;
   int64_t num_indices;
   int64_t unit_begin, unit_end;
+  int bags_per_item;  // 1..32
   int total_D;
   int fused_bounds;
   unsigned long long* stats;
@@ -48,8 +54,83 @@ __device__ __forceinline__ void store_out(float* dst, const float (&v)[4]) {
   __stcs(reinterpret_cast<float4*>(dst), make_float4(v[0], v[1], v[2], v[3]));
 }
 
+// Accumulate one raw vector of weights into fp32 (16-bit tables) or fp64 (fp32 tables).
+// Unweighted 16-bit rows use the mixed-precision add of sm_100+ (an f16/bf16 operand added to
+// an f32 accumulator in one instruction; the widening is exact, so the sum is the same as
+// converting first and adding).
+template <typename WT, int VB, bool PSW>
+__device__ __forceinline__ void accumulate(typename VecIO<WT, VB>::Acc (&acc)[VecIO<WT, VB>::N],
+                                           const typename VecIO<WT, VB>::Raw& v, float w) {
+  using IO = VecIO<WT, VB>;
+  using Acc = typename IO::Acc;
+  constexpr int NE = IO::N;
+  if constexpr (!PSW && sizeof(WT) == 2) {
+    uint32_t words[IO::W];
+    raw_words(v, words);
+#pragma unroll
+    for (int i = 0; i < IO::W; ++i) {
+      if constexpr (std::is_same<WT, __half>::value) {
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+            : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
+            : "r"(words[i]));
+      } else {
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+            : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
+            : "r"(words[i]));
+      }
+    }
+  } else {
+    float f[NE];
+    IO::unpack(v, f);
+#pragma unroll
+    for (int i = 0; i < NE; ++i) {
+      if (PSW) acc[i] += static_cast<Acc>(f[i]) * static_cast<Acc>(w);
+      else acc[i] += static_cast<Acc>(f[i]);
+    }
+  }
+}
+
+// A 32-position window of the index stream, one position per lane: the row of the lookup
+// (or -1 when it is skipped) and its per-sample weight.  Only positions in [lo, hi), the span of
+// the lanes' own work item, are read; repairs (fused bounds) and counts happen here, so with
+// monotone offsets each position of the stream is repaired or counted exactly once.
+template <bool PSW> struct IdWindow {
+  int32_t id;
+  float w;
+};
+
+template <typename IT, bool PSW>
+__device__ __forceinline__ IdWindow<PSW> load_window(const FwdArgs& a, int pos, int lo, int hi, int E) {
+  IdWindow<PSW> r{-1, 0.0f};
+  if (pos < lo || pos >= hi) return r;
+  int64_t v = ld_int<IT>(a.indices, pos);
+  bool ok = v >= 0 && v < E;
+  if (PSW) r.w = __ldg(a.psw + pos);
+  if (!ok) {
+    if (a.fused_bounds) {
+      static_cast<IT*>(a.indices)[pos] = IT(0);
+      v = 0;
+      ok = true;
+      stat_add(a.stats, TBE_STAT_BAD_INDICES, 1);
+    } else {
+      stat_add(a.stats, TBE_STAT_UNREPAIRED, 1);
+    }
+  }
+  r.id = ok ? static_cast<int32_t>(v) : -1;  // E < 2^31
+  return r;
+}
+
+// Work item: up to 32 consecutive bags of one table (fewer when the batch is too small to give
+// every warp several items).  A warp streams the item's part of the index
+// array through three 32-position register windows (two in use, the third in flight), so the
+// only loads on the critical path of a bag are its row loads: offsets and ids are fetched once
+// per item and up to 64 positions ahead.  Offsets that are not monotone (not repaired) cost a
+// reload of the windows where the stream jumps back or far ahead.
 template <typename WT, typename IT, bool PSW, int VB, int MAXV, int UNROLL>
-__global__ void __launch_bounds__(256) fwd_gather_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(256, MAXV == 1 ? (sizeof(WT) == 4 ? 3 : 4) : (MAXV == 2 ? 2 : 1))
+fwd_gather_kernel(FwdArgs a) {
   using IO = VecIO<WT, VB>;
   using Raw = typename IO::Raw;
   using Acc = typename IO::Acc;
@@ -58,113 +139,149 @@ __global__ void __launch_bounds__(256) fwd_gather_kernel(FwdArgs a) {
   const int lane = lane_id();
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int K = a.bags_per_item;
+  const int64_t items_per_table = (a.B + K - 1) / K;
+  const int t_begin = static_cast<int>(a.unit_begin / a.B);
+  const int64_t items = static_cast<int64_t>(a.unit_end / a.B - t_begin) * items_per_table;
+  const int N = static_cast<int>(a.num_indices);
 
-  for (int64_t u = a.unit_begin + warp0; u < a.unit_end; u += nwarps) {
-    const int t = static_cast<int>(u / a.B);
-    const int64_t b = u - static_cast<int64_t>(t) * a.B;
+  for (int64_t g = warp0; g < items; g += nwarps) {
+    const int t = t_begin + static_cast<int>(g / items_per_table);
+    const int64_t b0 = (g % items_per_table) * K;
+    const int nb = static_cast<int>(min(static_cast<int64_t>(K), a.B - b0));
+    const int64_t u0 = static_cast<int64_t>(t) * a.B + b0;
     const int col0 = __ldg(a.doff + t);
     const int D = __ldg(a.doff + t + 1) - col0;
-    const int64_t E = __ldg(a.roff + t + 1) - __ldg(a.roff + t);
-    const Raw* table = reinterpret_cast<const Raw*>(static_cast<const WT*>(a.weights) + __ldg(a.woff + t));
+    const int E = static_cast<int>(__ldg(a.roff + t + 1) - __ldg(a.roff + t));  // < 2^31
     const int nvec = D / NE;
     const int lpr = nvec >= kWarp ? kWarp : next_pow2_int(nvec);  // lanes per row
     const int rps = kWarp / lpr;                                    // rows per load step
     const int slot = lane / lpr;
     const int vi = lane & (lpr - 1);
+    // this lane's first vector of row 0 of the table, and of the item's first output row
+    const Raw* table =
+        reinterpret_cast<const Raw*>(static_cast<const WT*>(a.weights) + __ldg(a.woff + t)) + vi;
+    float* orow = a.out + b0 * a.total_D + col0 + vi * NE;
+    const int qmax = min(UNROLL, kWarp / rps);  // a batch covers at most 32 positions
 
-    const int64_t s = clamp64(ld_int<IT>(a.offsets, u), 0, a.num_indices);
-    const int64_t e = clamp64(ld_int<IT>(a.offsets, u + 1), s, a.num_indices);
+    // bag k of the item owns positions [s_k, e_k): lane k holds s_k in off_s and e_k in off_e
+    int off_s = 0, off_e = 0;
+    if (lane < nb) {
+      off_s = static_cast<int>(clamp64(ld_int<IT>(a.offsets, u0 + lane), 0, N));
+      off_e = static_cast<int>(clamp64(ld_int<IT>(a.offsets, u0 + lane + 1), off_s, N));
+    }
+    // span of the item's positions (the first s and last e unless offsets are not monotone)
+    int lo = lane < nb ? off_s : N, hi = off_e;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      lo = min(lo, __shfl_xor_sync(FULL, lo, m));
+      hi = max(hi, __shfl_xor_sync(FULL, hi, m));
+    }
+    int w0 = __shfl_sync(FULL, off_s, 0);
+    IdWindow<PSW> wa = load_window<IT, PSW>(a, w0 + lane, lo, hi, E);
+    IdWindow<PSW> wb = load_window<IT, PSW>(a, w0 + kWarp + lane, lo, hi, E);
+    IdWindow<PSW> wc = load_window<IT, PSW>(a, w0 + 2 * kWarp + lane, lo, hi, E);
 
-    Acc acc[MAXV][NE];
+    for (int k = 0; k < nb; ++k) {
+      const int s = __shfl_sync(FULL, off_s, k);
+      const int e = __shfl_sync(FULL, off_e, k);
+      Acc acc[MAXV][NE];
 #pragma unroll
-    for (int k = 0; k < MAXV; ++k)
+      for (int m = 0; m < MAXV; ++m)
 #pragma unroll
-      for (int i = 0; i < NE; ++i) acc[k][i] = Acc(0);
+        for (int i = 0; i < NE; ++i) acc[m][i] = Acc(0);
 
-    for (int64_t base = s; base < e; base += kWarp) {
-      const int n = static_cast<int>(min(static_cast<int64_t>(kWarp), e - base));
-      int64_t my_id = 0;
-      bool my_ok = false;
-      float my_w = 1.0f;
-      if (lane < n) {
-        my_id = ld_int<IT>(a.indices, base + lane);
-        my_ok = my_id >= 0 && my_id < E;
-        if (PSW) my_w = __ldg(a.psw + base + lane);
-        if (!my_ok && a.fused_bounds) {
-          static_cast<IT*>(a.indices)[base + lane] = IT(0);
-          my_id = 0;
-          my_ok = true;
-          stat_add(a.stats, TBE_STAT_BAD_INDICES, 1);
-        } else if (!my_ok) {
-          stat_add(a.stats, TBE_STAT_UNREPAIRED, 1);
-        }
-      }
-      const int32_t row_id = my_ok ? static_cast<int32_t>(my_id) : -1;  // E < 2^31
-      for (int j = 0; j < n; j += rps * UNROLL) {
-        Raw v[UNROLL][MAXV];
-        float w[UNROLL];
-#pragma unroll
-        for (int q = 0; q < UNROLL; ++q) {
-          const int r = j + q * rps + slot;
-          const int src = r & (kWarp - 1);
-          const int32_t id = __shfl_sync(FULL, row_id, src);
-          const bool ok = id >= 0 && r < n;
-          w[q] = PSW ? __shfl_sync(FULL, my_w, src) : 1.0f;
-          const Raw* row = table + static_cast<int64_t>(ok ? id : 0) * nvec;
-#pragma unroll
-          for (int k = 0; k < MAXV; ++k) {
-            const int vv = vi + k * kWarp;
-            if (ok && vv < nvec) v[q][k] = ldg_raw(row + vv);
-            else v[q][k] = Raw{};
+      for (int c0 = s; c0 < e; c0 += kWarp) {  // 32 positions of the bag at a time
+        // slide the windows so that c0 - w0 is in [0, 32) (warp-uniform)
+        int rel0 = c0 - w0;
+        if (rel0 >= kWarp && rel0 < 3 * kWarp) {
+          while (rel0 >= kWarp) {
+            wa = wb;
+            wb = wc;
+            wc = load_window<IT, PSW>(a, w0 + 3 * kWarp + lane, lo, hi, E);
+            w0 += kWarp;
+            rel0 -= kWarp;
           }
+        } else if (rel0 < 0 || rel0 >= 3 * kWarp) {
+          w0 = c0;
+          rel0 = 0;
+          wa = load_window<IT, PSW>(a, w0 + lane, lo, hi, E);
+          wb = load_window<IT, PSW>(a, w0 + kWarp + lane, lo, hi, E);
+          wc = load_window<IT, PSW>(a, w0 + 2 * kWarp + lane, lo, hi, E);
         }
+        // lane l takes position c0 + l from the two windows in use
+        const int rel = rel0 + lane;  // in [0, 64)
+        const int32_t ida = __shfl_sync(FULL, wa.id, rel & (kWarp - 1));
+        const int32_t idb = __shfl_sync(FULL, wb.id, rel & (kWarp - 1));
+        const int n = min(kWarp, e - c0);
+        const int32_t my_id = lane < n ? (rel < kWarp ? ida : idb) : -1;
+        float my_w = 1.0f;
+        if (PSW) {
+          const float pa = __shfl_sync(FULL, wa.w, rel & (kWarp - 1));
+          const float pb = __shfl_sync(FULL, wb.w, rel & (kWarp - 1));
+          my_w = rel < kWarp ? pa : pb;
+        }
+        for (int j = 0; j < n; j += rps * qmax) {
+          Raw v[UNROLL][MAXV];
+          float w[UNROLL];
 #pragma unroll
-        for (int q = 0; q < UNROLL; ++q) {
+          for (int q = 0; q < UNROLL; ++q) {
+            const int r = j + q * rps + slot;  // < 64; lanes past n hold -1
+            const int32_t id = __shfl_sync(FULL, my_id, r & (kWarp - 1));
+            w[q] = PSW ? __shfl_sync(FULL, my_w, r & (kWarp - 1)) : 1.0f;
+            const bool ok = q < qmax && r < n && id >= 0;
+            const Raw* row = table + static_cast<int64_t>(ok ? id : 0) * nvec;
 #pragma unroll
-          for (int k = 0; k < MAXV; ++k) {
-            float f[NE];
-            IO::unpack(v[q][k], f);
-#pragma unroll
-            for (int i = 0; i < NE; ++i) {
-              if (PSW) acc[k][i] += static_cast<Acc>(f[i]) * static_cast<Acc>(w[q]);
-              else acc[k][i] += static_cast<Acc>(f[i]);
+            for (int m = 0; m < MAXV; ++m) {
+              const int vv = vi + m * kWarp;
+              if (ok && vv < nvec) v[q][m] = ldg_raw(row + m * kWarp);
+              else v[q][m] = Raw{};
             }
           }
+#pragma unroll
+          for (int q = 0; q < UNROLL; ++q)
+#pragma unroll
+            for (int m = 0; m < MAXV; ++m) accumulate<WT, VB, PSW>(acc[m], v[q][m], w[q]);
         }
       }
-    }
-    // reduce the row groups of the warp (lanes that share vi)
-    for (int m = lpr; m < kWarp; m <<= 1) {
+      // reduce the row groups of the warp (lanes that share vi)
+      for (int m = lpr; m < kWarp; m <<= 1) {
 #pragma unroll
-      for (int k = 0; k < MAXV; ++k)
+        for (int x = 0; x < MAXV; ++x)
 #pragma unroll
-        for (int i = 0; i < NE; ++i) acc[k][i] += __shfl_xor_sync(FULL, acc[k][i], m);
-    }
-    if (slot == 0) {
-      float* orow = a.out + b * a.total_D + col0;
+          for (int i = 0; i < NE; ++i) acc[x][i] += __shfl_xor_sync(FULL, acc[x][i], m);
+      }
+      if (slot == 0) {
 #pragma unroll
-      for (int k = 0; k < MAXV; ++k) {
-        const int vv = vi + k * kWarp;
-        if (vv < nvec) {
-          float o[NE];
+        for (int x = 0; x < MAXV; ++x) {
+          if (vi + x * kWarp < nvec) {
+            float o[NE];
 #pragma unroll
-          for (int i = 0; i < NE; ++i) o[i] = static_cast<float>(acc[k][i]);
-          store_out(orow + vv * NE, o);
+            for (int i = 0; i < NE; ++i) o[i] = static_cast<float>(acc[x][i]);
+            store_out(orow + x * kWarp * NE, o);
+          }
         }
       }
+      orow += a.total_D;
     }
   }
 }
 
 template <typename WT, typename IT, bool PSW, int VB, int MAXV>
 cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s) {
-  constexpr int UNROLL = 4;
+  constexpr int UNROLL = MAXV >= 4 ? 1 : (MAXV == 2 ? 2 : 4);  // 4 to 8 loads in flight per lane
   auto k = fwd_gather_kernel<WT, IT, PSW, VB, MAXV, UNROLL>;
   const int threads = 256;
-  const int64_t units = a.unit_end - a.unit_begin;
-  const int64_t want = (units + (threads / kWarp) - 1) / (threads / kWarp);
+  const int64_t tables = (a.unit_end - a.unit_begin) / a.B;
+  const int64_t warps = static_cast<int64_t>(persistent_grid(k, threads, 0, dev, INT64_MAX)) * (threads / kWarp);
+  // about eight items per warp, at most 32 bags per item
+  FwdArgs ak = a;
+  const int64_t per_item = tables * a.B / (8 * warps);
+  ak.bags_per_item = per_item < 1 ? 1 : (per_item > kWarp ? kWarp : static_cast<int>(per_item));
+  const int64_t items = tables * ((a.B + ak.bags_per_item - 1) / ak.bags_per_item);
+  const int64_t want = (items + (threads / kWarp) - 1) / (threads / kWarp);
   const int grid = persistent_grid(k, threads, 0, dev, want);
-  k<<<grid, threads, 0, s>>>(a);
+  k<<<grid, threads, 0, s>>>(ak);
   note_launch();
   return cudaGetLastError();
 }

@@ -169,7 +169,8 @@ tbe_status tbe_bounds_check(const tbe_problem* prob, const tbe_tables* tables, v
 /* Pooled forward.  With opt->fused_bounds the kernel repairs out-of-range ids as it reads
  * them (writing 0 back into indices, so the backward sees the repaired id); without it the
  * ids must be valid (out-of-range ones are skipped and counted as TBE_STAT_UNREPAIRED).
- * Offsets must be non-decreasing (tbe_bounds_check makes them so).  out: [B, sum D] fp32. */
+ * Offsets must be non-decreasing (tbe_bounds_check makes them so); others are clamped so that
+ * no read leaves the index array, and the bags they give are unspecified.  out: [B, sum D] fp32. */
 size_t tbe_forward_workspace_size(const tbe_problem* prob, const tbe_options* opt);
 tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tbe_tables* tables,
                        const void* weights, void* indices, const void* offsets, const float* psw,
