@@ -543,32 +543,72 @@ __global__ void __launch_bounds__(kThreads, 4) long_chunk_kernel(BwdCtx c,
     for (int j = 0; j < MAXV; ++j)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[j][i] = Acc(0);
+    // This lane's float4 slices of the table's columns in bag 0's gradient row.  Lanes whose
+    // slice lies past the row width re-read the last slice: their sums are never stored.
+    const float4* gbase = reinterpret_cast<const float4*>(c.grad_out + col0);
+    const int64_t gstride = c.total_D / 4;  // float4s per gradient row
+    int vk[MAXV];
+#pragma unroll
+    for (int k = 0; k < MAXV; ++k) vk[k] = min(vi + k * kWarp, nv - 1);
+    const bool fast = rps * UNROLL <= kWarp;  // a batch never wraps past 32 rows
+    const uint32_t last_bag = static_cast<uint32_t>(c.B - 1);
+    // The bags of the chunk's lookups, 32 at a time, with the next 32 in flight.  Bags come
+    // from the expand step and are < B; the clamp only keeps garbage (offsets that were not
+    // repaired) from reading outside grad_out.
+    uint32_t nxt_b = 0;
+    float nxt_w = 1.f;
+    if (s + lane < e) {
+      nxt_b = min(__ldg(sorted_vals + s + lane), last_bag);
+      if (PSW) nxt_w = __ldg(sorted_psw + s + lane);
+    }
     for (uint32_t base = s; base < e; base += kWarp) {
       const int n = static_cast<int>(min(static_cast<uint32_t>(kWarp), e - base));
-      uint32_t my_b = 0;
-      float my_w = 1.f;
-      bool my_ok = false;
-      if (lane < n) {
-        my_b = __ldg(sorted_vals + base + lane);
-        if (PSW) my_w = __ldg(sorted_psw + base + lane);
-        my_ok = my_b < c.B;
+      const uint32_t bag = nxt_b;
+      const float my_w = nxt_w;
+      nxt_b = 0;
+      if (base + kWarp + lane < e) {
+        nxt_b = min(__ldg(sorted_vals + base + kWarp + lane), last_bag);
+        if (PSW) nxt_w = __ldg(sorted_psw + base + kWarp + lane);
       }
-      const int32_t bag = my_ok ? static_cast<int32_t>(my_b) : -1;
+      if (fast && n == kWarp) {
+        // all 32 rows valid: unpredicated loads
+        for (int j = 0; j < kWarp; j += rps * UNROLL) {
+          float4 v[UNROLL][MAXV];
+          float w[UNROLL];
+#pragma unroll
+          for (int q = 0; q < UNROLL; ++q) {
+            const int rr = j + q * rps + rs;
+            const uint32_t b = __shfl_sync(FULL, bag, rr);
+            w[q] = PSW ? __shfl_sync(FULL, my_w, rr) : 1.f;
+            const float4* grow = gbase + static_cast<int64_t>(b) * gstride;
+#pragma unroll
+            for (int k = 0; k < MAXV; ++k) v[q][k] = __ldg(grow + vk[k]);
+          }
+#pragma unroll
+          for (int q = 0; q < UNROLL; ++q)
+#pragma unroll
+            for (int k = 0; k < MAXV; ++k) {
+              const Acc wq = static_cast<Acc>(w[q]);
+              acc[k][0] += PSW ? static_cast<Acc>(v[q][k].x) * wq : static_cast<Acc>(v[q][k].x);
+              acc[k][1] += PSW ? static_cast<Acc>(v[q][k].y) * wq : static_cast<Acc>(v[q][k].y);
+              acc[k][2] += PSW ? static_cast<Acc>(v[q][k].z) * wq : static_cast<Acc>(v[q][k].z);
+              acc[k][3] += PSW ? static_cast<Acc>(v[q][k].w) * wq : static_cast<Acc>(v[q][k].w);
+            }
+        }
+        continue;
+      }
       for (int j = 0; j < n; j += rps * UNROLL) {
         float4 v[UNROLL][MAXV];
         float w[UNROLL];
 #pragma unroll
         for (int q = 0; q < UNROLL; ++q) {
           const int rr = j + q * rps + rs;
-          const int32_t b = __shfl_sync(FULL, bag, rr & (kWarp - 1));
-          const bool ok = b >= 0 && rr < n;
+          const uint32_t b = __shfl_sync(FULL, bag, rr & (kWarp - 1));
+          const bool ok = rr < n;
           w[q] = PSW ? __shfl_sync(FULL, my_w, rr & (kWarp - 1)) : 1.f;
-          const float4* grow = reinterpret_cast<const float4*>(c.grad_out + static_cast<int64_t>(ok ? b : 0) * c.total_D + col0);
+          const float4* grow = gbase + static_cast<int64_t>(b) * gstride;
 #pragma unroll
-          for (int k = 0; k < MAXV; ++k) {
-            const int vec = vi + k * kWarp;
-            v[q][k] = (ok && vec < nv) ? __ldg(grow + vec) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
+          for (int k = 0; k < MAXV; ++k) v[q][k] = ok ? __ldg(grow + vk[k]) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int q = 0; q < UNROLL; ++q)
