@@ -17,8 +17,10 @@
 //     sm_100+ (no separate widening instruction);
 //   * the row groups are reduced with xor-shuffles and one group writes the fp32 result with
 //     streaming 16-byte stores;
-//   * items are walked table-major with a grid stride, so the CTAs in flight read neighbouring
-//     parts of the index array and mostly one table's rows.
+//   * one item per warp, CTAs launched table-major: the CTAs in flight read neighbouring parts of
+//     the index array and mostly one table's rows, and an SM takes the next CTA as soon as one
+//     retires (a resident grid-stride loop balanced uneven items worse: 3.1 vs 2.6 ms on the
+//     83.9M-lookup stress batch).
 // Out-of-range ids are repaired to row 0 in flight when fused bounds checking is on (writing
 // the repaired id back), else skipped and counted; no id outside its table is dereferenced.
 #include "tbe_internal.cuh"
@@ -279,8 +281,11 @@ cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   const int64_t per_item = tables * a.B / (8 * warps);
   ak.bags_per_item = per_item < 1 ? 1 : (per_item > kWarp ? kWarp : static_cast<int>(per_item));
   const int64_t items = tables * ((a.B + ak.bags_per_item - 1) / ak.bags_per_item);
+  // One item per warp: CTAs retire as their items finish and the block scheduler hands the SM
+  // to the next one, which balances items of uneven length better than a resident grid-stride
+  // loop (the loop stays for grids past the launch limit).
   const int64_t want = (items + (threads / kWarp) - 1) / (threads / kWarp);
-  const int grid = persistent_grid(k, threads, 0, dev, want);
+  const int grid = static_cast<int>(want < 0x7fffffff ? want : 0x7fffffff);
   k<<<grid, threads, 0, s>>>(ak);
   note_launch();
   return cudaGetLastError();

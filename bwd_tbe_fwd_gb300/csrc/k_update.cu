@@ -681,7 +681,10 @@ cudaError_t launch_short_t(const BwdCtx& c, int bucket, const uint32_t* vals, co
     note_launch();
   } else {
     auto k = short_run_kernel<WT, PSW, OPT, LPR, VPL, false>;
-    const int grid = persistent_grid(k, kThreads, 0, dev, want);
+    // sixteen waves of CTAs (capped by the list capacity): CTAs that finish early hand their SM
+    // to the next, which evens out runs of uneven length better than one resident wave
+    const int64_t g16 = static_cast<int64_t>(persistent_grid(k, kThreads, 0, dev, INT64_MAX)) * 16;
+    const int grid = static_cast<int>(g16 < want ? g16 : want);
     k<<<grid, kThreads, 0, s>>>(c, bucket, vals, psw);
     note_launch();
   }

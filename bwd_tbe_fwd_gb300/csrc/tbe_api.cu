@@ -57,6 +57,7 @@ tbe_status check_options(const tbe_options& o) {
   if (o.scheduler != TBE_SCHED_GRID && o.scheduler != TBE_SCHED_PERSISTENT) return TBE_ERR_INVALID_ARG;
   if (o.num_events < 0 || (o.num_events > 0 && o.events == nullptr)) return TBE_ERR_INVALID_ARG;
   if (o.classify_mode != TBE_CLASSIFY_ORDERED && o.classify_mode != TBE_CLASSIFY_ATOMIC) return TBE_ERR_INVALID_ARG;
+  if (o.prepared != 0 && o.prepared != 1) return TBE_ERR_INVALID_ARG;
   return TBE_OK;
 }
 }  // namespace
@@ -256,6 +257,22 @@ bool tables_ok(const tbe_tables* tab) {
          tab->row_offsets != nullptr;
 }
 
+// expand, sort, RLE and classify: the transpose half of the backward
+cudaError_t run_transpose(const Problem& P, const tbe_options& o, const BwdLayout& L, const BwdCtx& c,
+                          const DeviceInfo& dev, cudaStream_t s) {
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(c.counters, 0, sizeof(uint32_t) * TBE_NUM_COUNTERS, s)) != cudaSuccess) return e;
+  if ((e = launch_expand(P, c, s)) != cudaSuccess) return e;
+  record(o, TBE_BWD_EV_EXPAND, s);
+  if ((e = launch_sort(P, c, L, s)) != cudaSuccess) return e;
+  record(o, TBE_BWD_EV_SORT, s);
+  if ((e = launch_rle(P, c, L, s)) != cudaSuccess) return e;
+  record(o, TBE_BWD_EV_RLE, s);
+  if ((e = launch_classify(P, c, dev, o.classify_mode, s)) != cudaSuccess) return e;
+  record(o, TBE_BWD_EV_CLASSIFY, s);
+  return cudaSuccess;
+}
+
 }  // namespace
 }  // namespace tbe
 
@@ -292,6 +309,7 @@ void tbe_default_options(tbe_options* opt) {
   opt->num_events = 0;
   opt->launch_counter = nullptr;
   opt->classify_mode = TBE_CLASSIFY_ATOMIC;
+  opt->prepared = 0;
 }
 
 tbe_status tbe_table_layout(const tbe_problem* prob, int64_t* weight_offsets, int32_t* D_offsets,
@@ -413,6 +431,32 @@ size_t tbe_backward_workspace_size(const tbe_problem* prob, const tbe_options* o
   return make_bwd_layout(P, o, dev).total;
 }
 
+tbe_status tbe_backward_prepare(const tbe_problem* prob, const tbe_options* opt, const tbe_tables* tables,
+                                const void* indices, const void* offsets, const float* psw, void* ws,
+                                size_t ws_bytes, int64_t* d_stats, void* stream) {
+  Problem P;
+  tbe_status st = make_problem(prob, &P);
+  if (st != TBE_OK) return st;
+  const tbe_options o = resolve(opt);
+  if ((st = check_options(o)) != TBE_OK) return st;
+  if (!tables_ok(tables) || offsets == nullptr || (P.num_indices > 0 && indices == nullptr))
+    return TBE_ERR_INVALID_ARG;
+  if ((P.weighted && psw == nullptr && P.num_indices > 0) || (!P.weighted && psw != nullptr))
+    return TBE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return TBE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != TBE_OK) return st;
+  const BwdLayout L = make_bwd_layout(P, o, dev);
+  if (ws == nullptr || ws_bytes < L.total) return TBE_ERR_WORKSPACE;
+  const BwdCtx c = make_ctx(P, o, L, tables, nullptr, nullptr, indices, offsets, psw, nullptr, 0.f, 0.f, ws,
+                            d_stats);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LaunchTally tally(o);
+  record(o, TBE_BWD_EV_START, s);
+  const cudaError_t e = run_transpose(P, o, L, c, dev, s);
+  return e == cudaSuccess ? TBE_OK : cuda_status(e);
+}
+
 tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
                                const tbe_tables* tables, void* weights, float* state,
                                const void* indices, const void* offsets, const float* psw,
@@ -442,16 +486,12 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
   cudaError_t e;
   LaunchTally tally(o);
   record(o, TBE_BWD_EV_START, s);
-  if ((e = cudaMemsetAsync(c.counters, 0, sizeof(uint32_t) * TBE_NUM_COUNTERS, s)) != cudaSuccess)
+  if (o.prepared) {
+    // the stage events of the transpose mark the start of the update
+    for (int ev : {TBE_BWD_EV_EXPAND, TBE_BWD_EV_SORT, TBE_BWD_EV_RLE, TBE_BWD_EV_CLASSIFY}) record(o, ev, s);
+  } else if ((e = run_transpose(P, o, L, c, dev, s)) != cudaSuccess) {
     return cuda_status(e);
-  if ((e = launch_expand(P, c, s)) != cudaSuccess) return cuda_status(e);
-  record(o, TBE_BWD_EV_EXPAND, s);
-  if ((e = launch_sort(P, c, L, s)) != cudaSuccess) return cuda_status(e);
-  record(o, TBE_BWD_EV_SORT, s);
-  if ((e = launch_rle(P, c, L, s)) != cudaSuccess) return cuda_status(e);
-  record(o, TBE_BWD_EV_RLE, s);
-  if ((e = launch_classify(P, c, dev, o.classify_mode, s)) != cudaSuccess) return cuda_status(e);
-  record(o, TBE_BWD_EV_CLASSIFY, s);
+  }
   if ((e = launch_short_updates(P, c, L, optimizer, o.scheduler, dev, s)) != cudaSuccess)
     return cuda_status(e);
   record(o, TBE_BWD_EV_SHORT, s);

@@ -56,6 +56,7 @@ tbe_status tbe_backward_update_noalloc(const tbe_problem* prob, const tbe_option
                                        const void* indices, const void* offsets, const float* psw,
                                        const float* grad_out, tbe_optimizer optimizer, float lr,
                                        float eps, int64_t* d_stats, void* stream) {
+  if (opt != nullptr && opt->prepared) return TBE_ERR_INVALID_ARG;  // nothing prepares the built-in array
   const size_t need = tbe_backward_workspace_size(prob, opt);
   if (need == 0) return TBE_ERR_INVALID_ARG;  // the problem or the options were rejected
   if (need > TBE_STATIC_SCRATCH_BYTES) return TBE_ERR_WORKSPACE;

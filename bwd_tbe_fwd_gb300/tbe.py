@@ -38,7 +38,7 @@ EXPORTED = (
     "tbe_default_options", "tbe_table_layout", "tbe_bounds_workspace_size", "tbe_bounds_check",
     "tbe_forward_workspace_size", "tbe_forward", "tbe_backward_workspace_size",
     "tbe_backward_update", "tbe_backward_metadata", "tbe_status_string", "tbe_version",
-    "tbe_last_cuda_error", "tbe_backward_update_noalloc",
+    "tbe_last_cuda_error", "tbe_backward_update_noalloc", "tbe_backward_prepare",
 )
 TBE_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -56,7 +56,8 @@ class Tables(ctypes.Structure):
 class Options(ctypes.Structure):
     _fields_ = [("long_threshold", c_i32), ("chunk", c_i32), ("long_mode", c_i32), ("scheduler", c_i32),
                 ("histogram", c_i32), ("fused_bounds", c_i32), ("events", ctypes.POINTER(vp)),
-                ("num_events", c_i32), ("launch_counter", ctypes.POINTER(c_i64)), ("classify_mode", c_i32)]
+                ("num_events", c_i32), ("launch_counter", ctypes.POINTER(c_i64)), ("classify_mode", c_i32),
+                ("prepared", c_i32)]
 
 
 class RunMetadata(ctypes.Structure):
@@ -100,13 +101,14 @@ def load(path: str | None = None):
         lib.tbe_backward_workspace_size.restype = ctypes.c_size_t
         lib.tbe_backward_update.argtypes = [P, O, T, vp, vp, vp, vp, vp, vp, ctypes.c_int, c_f32, c_f32,
                                             vp, ctypes.c_size_t, vp, vp]
+        lib.tbe_backward_prepare.argtypes = [P, O, T, vp, vp, vp, vp, ctypes.c_size_t, vp, vp]
         lib.tbe_backward_metadata.argtypes = [P, O, vp, ctypes.c_size_t, M]
         lib.tbe_status_string.argtypes = [ctypes.c_int]
         lib.tbe_status_string.restype = ctypes.c_char_p
         lib.tbe_version.restype = ctypes.c_int
         lib.tbe_last_cuda_error.restype = ctypes.c_int
         for name in ("tbe_table_layout", "tbe_bounds_check", "tbe_forward", "tbe_backward_update",
-                     "tbe_backward_metadata"):
+                     "tbe_backward_prepare", "tbe_backward_metadata"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -261,8 +263,24 @@ class TableBatchedEmbedding:
         _check(self.lib, st, "tbe_forward")
         return out
 
+    def backward_prepare(self, indices, offsets, psw=None, stats=None, stream=None,
+                         options: TBEOptions | None = None):
+        """The transpose half of the backward (linearize, sort, RLE, classify) into the backward
+        workspace; a following backward_update with prepared=True only applies the updates."""
+        self._idx(indices, offsets)
+        self._dev(psw, "psw", torch.float32, self.num_indices)
+        self._dev(stats, "stats", torch.int64, TBE_NUM_STATS)
+        o = (options or self.options).c
+        if o.long_threshold != self.options.c.long_threshold or o.chunk != self.options.c.chunk:
+            raise ValueError("threshold/chunk differ from the options the workspace was sized for")
+        st = self.lib.tbe_backward_prepare(
+            ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables), _ptr(indices), _ptr(offsets),
+            _ptr(psw), _ptr(self.ws_backward), self.ws_backward.numel(), _ptr(stats), _stream(stream))
+        _check(self.lib, st, "tbe_backward_prepare")
+
     def backward_update(self, weights, state, indices, offsets, grad_out, psw=None, optimizer="adagrad",
-                        lr=0.01, eps=1e-8, stats=None, stream=None, options: TBEOptions | None = None):
+                        lr=0.01, eps=1e-8, stats=None, stream=None, options: TBEOptions | None = None,
+                        prepared: bool = False):
         self._idx(indices, offsets)
         self._dev(weights, "weights", self.weight_dtype, self.num_weights)
         self._dev(state, "state", torch.float32, self.total_rows)
@@ -273,6 +291,9 @@ class TableBatchedEmbedding:
         o = (options or self.options).c
         if o.long_threshold != self.options.c.long_threshold or o.chunk != self.options.c.chunk:
             raise ValueError("threshold/chunk differ from the options the workspace was sized for")
+        if bool(o.prepared) != prepared:
+            o = Options.from_buffer_copy(o)
+            o.prepared = 1 if prepared else 0
         st = self.lib.tbe_backward_update(
             ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables), _ptr(weights), _ptr(state),
             _ptr(indices), _ptr(offsets), _ptr(psw), _ptr(grad_out), opt, c_f32(lr), c_f32(eps),

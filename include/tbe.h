@@ -134,6 +134,8 @@ typedef struct {
   int32_t num_events;
   int64_t* launch_counter;    /* NULL, or a HOST counter to which each call adds its kernel launches */
   int32_t classify_mode;      /* tbe_classify_mode */
+  int32_t prepared;           /* 1: tbe_backward_update takes the transpose from ws, where
+                                 tbe_backward_prepare left it, instead of computing it */
 } tbe_options;
 
 /* Indices into d_stats (int64).  Counts accumulate over calls. */
@@ -188,6 +190,21 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
                                const float* grad_out, tbe_optimizer optimizer, float lr, float eps,
                                void* ws, size_t ws_bytes, int64_t* d_stats, void* stream);
 
+/* The transpose half of the backward on its own ("Modernizing Table Batched Embeddings with
+ * FBTriton", section 2, "Forward state reuse and preprocessing": the optional path that moves the
+ * index transpose, sort and run-length encoding ahead of the backward): linearize, sort, run-length
+ * encode and classify the batch's lookups into ws.  It reads only the layout, indices, offsets
+ * and psw -- not the weights or the gradient -- so it can run before the gradient exists, e.g. on
+ * a second stream alongside tbe_forward.  A later tbe_backward_update with opt->prepared = 1 and
+ * the same problem, options, ws and inputs then only applies the updates.  One prepare serves one
+ * update (the update consumes the long-run countdowns).  Ids must already be repaired
+ * (tbe_bounds_check, or a tbe_forward with fused bounds that has finished); stats as for
+ * tbe_backward_update.  The workspace size is tbe_backward_workspace_size(). */
+tbe_status tbe_backward_prepare(const tbe_problem* prob, const tbe_options* opt,
+                                const tbe_tables* tables, const void* indices, const void* offsets,
+                                const float* psw, void* ws, size_t ws_bytes, int64_t* d_stats,
+                                void* stream);
+
 /* Device counters kept in the backward workspace (uint32), for the metadata view below. */
 enum {
   TBE_CNT_N = 0,              /* lookups of the batch (offsets[T*B], clamped) */
@@ -238,6 +255,7 @@ tbe_status tbe_backward_metadata(const tbe_problem* prob, const tbe_options* opt
  *   - Sharing: all calls on one device use the same array, which keeps the last call's
  *     contents; each call zeroes what must start at zero.  Calls whose GPU work overlaps (other
  *     streams, other host threads) race on it; the caller must order them.
+ *   - opt->prepared must be 0 (TBE_ERR_INVALID_ARG otherwise): nothing prepares the array.
  * Results equal those of tbe_backward_update on the same inputs. */
 tbe_status tbe_backward_update_noalloc(const tbe_problem* prob, const tbe_options* opt,
                                        const tbe_tables* tables, void* weights, float* state,

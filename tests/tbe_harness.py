@@ -152,7 +152,7 @@ class Case:
         check_forward(out.cpu().numpy(), exact, absterms, self.cfg.wdtype)
         return out
 
-    def backward(self, optimizer=None, steps=1, options=None, check_meta=True):
+    def backward(self, optimizer=None, steps=1, options=None, check_meta=True, prepared=False):
         cfg = self.cfg
         assert steps == 1 or cfg.wdtype == "f32", "multi-step parity needs fp32 tables"
         opt = optimizer or cfg.optimizer
@@ -166,8 +166,17 @@ class Case:
         for step in range(steps):
             w_before = weights_f64(w_d)
             s_before = None if state_d is None else state_d.cpu().numpy().copy()
+            if prepared:
+                # the transpose on a second stream while the forward gather runs on this one
+                main = torch.cuda.current_stream(self.device)
+                side = torch.cuda.Stream(device=self.device)
+                side.wait_stream(main)
+                self.tbe.backward_prepare(self.idx_d, self.off_d, psw=self.psw_d, stats=self.stats, stream=side,
+                                          options=options)
+                self.tbe.forward(w_d, self.idx_d, self.off_d, psw=self.psw_d)
+                main.wait_stream(side)
             self.tbe.backward_update(w_d, state_d, self.idx_d, self.off_d, grad_d, psw=self.psw_d, optimizer=opt,
-                                     lr=cfg.lr, eps=cfg.eps, stats=self.stats, options=options)
+                                     lr=cfg.lr, eps=cfg.eps, stats=self.stats, options=options, prepared=prepared)
             torch.cuda.synchronize()
             res = oracle.backward(self.tables, cfg.B, w_h, state_h, self.idx_h, self.off_h, grad_h, psw=self.psw_h,
                                   optimizer=opt, lr=cfg.lr, eps=cfg.eps, wdtype=cfg.wdtype)

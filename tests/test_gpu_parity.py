@@ -81,6 +81,14 @@ def test_ordered_classifier(name):
     c.backward(options=opts)
 
 
+@pytest.mark.parametrize("name", ["c3", "c5", "c2", "c1"])
+def test_prepared_transpose_beside_the_forward(name):
+    """tbe_backward_prepare on a second stream while the forward gather runs, then the update with
+    prepared=1: the same updates and metadata as the one-call backward."""
+    c = Case(SMALL[name])
+    c.backward(prepared=True)
+
+
 def test_skewed_example_batch_routes_as_printed():
     """The tutorial's skewed batch (T=3, E=50, B=16, D=24, seed 1): the device classifier must
     produce the printed short/long/chunk counts for each threshold and chunk size."""
