@@ -297,6 +297,312 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------------------------------
+// Backward of a counts x table feature: the table's gradient is counts^T x grad_out.
+//
+// "Modernizing Table Batched Embeddings with FBTriton", section 2 ("Forward state reuse and
+// preprocessing"): the backward of the small-table path can reuse the forward's per-bag counts,
+// multiply them into the upstream gradient on the tensor cores with a compensated split of the
+// fp32 gradient into 16-bit parts accumulating in fp32, then apply the optimizer to each row.
+// The pages split into fp16 hi + lo; here each fp32 value is split exactly into three bf16
+// parts (hi + mid + lo carry all 24 significand bits and keep fp32's exponent range, so no
+// gradient overflows or flushes), and counts <= 256 are exact in bf16.  Per CTA and tile of 128
+// bags (K = 128):
+//   1. count the first 256 ids of each bag as in the forward; ids past the 256th (rare) add
+//      their gradient row to the row's fp32 sum with atomics directly;
+//   2. B operand (N = E rounded up to 16, K-major): counts of row e in the tile's bags, bf16;
+//      A operands (M = 128 gradient columns, K-major): the three bf16 parts of grad_out[bag, d]
+//      -- a warp loads 8 bags x 32 columns coalesced and writes one 16-byte core-matrix row per
+//      lane and part;
+//   3. one thread issues 3 x 8 tcgen05.mma (K = 16 each) into one TMEM accumulator (128 lanes =
+//      columns d, N columns = rows e) that lives across the CTA's tiles; the CTA waits on the
+//      commit (bounded) before it rewrites the operands;
+//   4. at the end each thread (column d) adds its accumulator row into the table's fp32 gradient
+//      sum with atomics; the last CTA to finish (fence + counter) applies the optimizer once to
+//      every row whose count is non-zero.
+// ------------------------------------------------------------------------------------------
+constexpr int kBK = 128;                       // bags per tile (the K of the MMA)
+constexpr int kBM = 128;                       // gradient columns (the M of the MMA)
+constexpr uint32_t kBSBO = (kBK / 8) * 128;    // 2048 B between core matrices along M/N
+constexpr int kBATile = kBM * kBK * 2;         // 32 KB per bf16 split of the gradient
+constexpr int kBBTile = kK * kBK * 2;          // 16 KB: counts of up to 64 rows
+constexpr uint32_t kBTmemCols = 64;
+
+struct HistBwdArgs {
+  const void* indices;
+  const void* offsets;
+  const float* grad_out;
+  __half* table;          // E x D, updated in place
+  float* state;           // row-wise Adagrad state of the table's rows (NULL for SGD)
+  float* gsum;            // E x D fp32 gradient sums (zeroed by the caller)
+  uint32_t* rowcnt;       // E lookups per row (zeroed by the caller)
+  uint32_t* done;         // CTAs finished (zeroed by the caller)
+  int64_t B, num_indices, bag0;
+  int E, D, N, col0, total_D;
+  int opt;
+  float lr, eps;
+  unsigned long long* stats;
+};
+
+__device__ __forceinline__ uint64_t smem_desc_bwd(uint32_t addr) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFF) | (static_cast<uint64_t>(kLBO >> 4) << 16) |
+         (static_cast<uint64_t>(kBSBO >> 4) << 32) | (uint64_t(1) << 46);
+}
+
+// kind::f16 instruction descriptor with bf16 A and B (both K-major), fp32 accumulator.
+__device__ __forceinline__ uint32_t instr_desc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t kmajor_offset_bwd(int r, int k) {
+  return static_cast<uint32_t>((r >> 3) * kBSBO + (k >> 3) * kLBO + (r & 7) * 16 + (k & 7) * 2);
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+}
+
+// x == hi + mid + lo exactly (bf16 parts, fp32 arithmetic for the remainders).
+__device__ __forceinline__ void split3(float x, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(h);
+  const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(m);
+  hi = __bfloat16_as_ushort(h);
+  mid = __bfloat16_as_ushort(m);
+  lo = bf16_bits(r2);
+}
+
+template <typename IT>
+__global__ void __launch_bounds__(kThreads, 1) hist_bwd_kernel(HistBwdArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* a_tiles = smem;                                  // 3 x 32 KB: gradient parts
+  uint8_t* b_tile = smem + 3 * kBATile;                     // 16 KB: counts
+  uint32_t* pairs = reinterpret_cast<uint32_t*>(smem + 3 * kBATile + kBBTile);  // [128][32] count pairs
+  __shared__ __align__(8) uint64_t mma_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_failed, s_last;
+  __shared__ int64_t s_off[kBK + 1];
+  __shared__ int s_rel[kBK + 1];
+  __shared__ uint32_t s_rowcnt[kK];
+
+  const int tid = threadIdx.x, lane = lane_id(), warp = tid / kWarp;
+  const int64_t tiles = (a.B + kBK - 1) / kBK;
+
+  if (warp == 0) tmem_alloc(&s_tmem, kBTmemCols);
+  if (tid == 0) {
+    mbar_init(&mma_bar, 1);
+    s_failed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < kK) s_rowcnt[tid] = 0;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t idesc = instr_desc_bf16(kBM, a.N);
+  const uint64_t b_desc0 = smem_desc_bwd(smem_u32(b_tile));
+  uint32_t phase = 0;
+  int mine = 0;  // tiles this CTA accumulated
+
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++mine) {
+    const int64_t b0 = tile * kBK;
+    const int nb = static_cast<int>(min(static_cast<int64_t>(kBK), a.B - b0));
+    // 1. counts of the first 256 ids of each bag
+    for (int i = tid; i < kBK * kK / 2 / 4; i += kThreads) reinterpret_cast<uint4*>(pairs)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i <= kBK; i += kThreads)
+      s_off[i] = clamp64(ld_int<IT>(a.offsets, a.bag0 + b0 + min(i, nb)), 0, a.num_indices);
+    __syncthreads();
+    for (int i = 1; i <= nb; ++i) {
+      if (tid == 0 && s_off[i] < s_off[i - 1]) s_off[i] = s_off[i - 1];
+    }
+    __syncthreads();
+    {
+      const int64_t p0 = s_off[0];
+      const int rel_end = static_cast<int>(s_off[nb] - p0);
+      for (int i = tid; i <= nb; i += kThreads) s_rel[i] = static_cast<int>(s_off[i] - p0);
+      __syncthreads();
+      const IT* ids = static_cast<const IT*>(a.indices) + p0;
+      uint32_t bad = 0;
+      int lo = 0, cur = 0, nxt = nb > 0 ? s_rel[1] : 0x7fffffff;
+      for (int base = 0; base < rel_end; base += kThreads * kIdsPerThread) {
+        IT id[kIdsPerThread];
+#pragma unroll
+        for (int j = 0; j < kIdsPerThread; ++j) {
+          const int r = base + j * kThreads + tid;
+          id[j] = r < rel_end ? __ldg(ids + r) : IT(0);
+        }
+#pragma unroll
+        for (int j = 0; j < kIdsPerThread; ++j) {
+          const int r = base + j * kThreads + tid;
+          if (r >= rel_end) continue;
+          while (r >= nxt) {
+            ++lo;
+            cur = nxt;
+            nxt = lo + 1 <= nb ? s_rel[lo + 1] : 0x7fffffff;
+          }
+          if (static_cast<uint64_t>(static_cast<int64_t>(id[j])) >= static_cast<uint64_t>(a.E)) {
+            ++bad;
+            continue;
+          }
+          const uint32_t k = static_cast<uint32_t>(id[j]);
+          if (r - cur >= kHistIds) {
+            // past the 256th id of its bag: add the bag's gradient row to row k directly
+            const float4* g = reinterpret_cast<const float4*>(a.grad_out + (b0 + lo) * a.total_D + a.col0);
+            float4* dst = reinterpret_cast<float4*>(a.gsum + static_cast<int64_t>(k) * a.D);
+            for (int v = 0; v < a.D / 4; ++v) atomicAdd(dst + v, __ldg(g + v));
+            atomicAdd(&s_rowcnt[k], 1u);
+            continue;
+          }
+          atomicAdd(&pairs[lo * (kK / 2) + (k >> 1)], (k & 1u) << 16 | (~k & 1u));
+        }
+      }
+      if (bad) stat_add(a.stats, TBE_STAT_UNREPAIRED, bad);
+    }
+    __syncthreads();
+    // row totals of the tile
+    if (tid < a.E) {
+      uint32_t tot = 0;
+      for (int k = 0; k < nb; ++k) tot += (pairs[k * (kK / 2) + (tid >> 1)] >> ((tid & 1) * 16)) & 0xFFFFu;
+      s_rowcnt[tid] += tot;
+    }
+    // 2a. B operand: element (row e, bag k) = count, 8 bags per 16-byte core-matrix row
+    for (int q = tid; q < a.N * (kBK / 8); q += kThreads) {
+      const int e = q / (kBK / 8), kb = (q % (kBK / 8)) * 8;
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t c0 = (pairs[(kb + 2 * j) * (kK / 2) + (e >> 1)] >> ((e & 1) * 16)) & 0xFFFFu;
+        const uint32_t c1 = (pairs[(kb + 2 * j + 1) * (kK / 2) + (e >> 1)] >> ((e & 1) * 16)) & 0xFFFFu;
+        w[j] = bf16_bits(static_cast<float>(c0)) | (bf16_bits(static_cast<float>(c1)) << 16);
+      }
+      *reinterpret_cast<uint4*>(b_tile + kmajor_offset_bwd(e, kb)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    // 2b. A operands: element (column d, bag k) of each bf16 part of the gradient
+    for (int task = warp; task < (kBM / kWarp) * (kBK / 8); task += kThreads / kWarp) {
+      const int d = (task % (kBM / kWarp)) * kWarp + lane;
+      const int kb = (task / (kBM / kWarp)) * 8;
+      float g[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int k = kb + j;
+        g[j] = (d < a.D && k < nb) ? __ldg(a.grad_out + (b0 + k) * a.total_D + a.col0 + d) : 0.f;
+      }
+      uint32_t hw[4], mw[4], lw[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t h0, m0, l0, h1, m1, l1;
+        split3(g[2 * j], h0, m0, l0);
+        split3(g[2 * j + 1], h1, m1, l1);
+        hw[j] = h0 | (h1 << 16);
+        mw[j] = m0 | (m1 << 16);
+        lw[j] = l0 | (l1 << 16);
+      }
+      const uint32_t off = kmajor_offset_bwd(d, kb);
+      *reinterpret_cast<uint4*>(a_tiles + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(a_tiles + kBATile + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+      *reinterpret_cast<uint4*>(a_tiles + 2 * kBATile + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // 3. gradient parts x counts into the accumulator
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {
+        const uint64_t a_desc0 = smem_desc_bwd(smem_u32(a_tiles + part * kBATile));
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t adv = static_cast<uint64_t>((kk * 2 * kLBO) >> 4);
+          umma_f16(tmem, a_desc0 + adv, b_desc0 + adv, idesc, (mine > 0 || part > 0 || kk > 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(&mma_bar);
+    }
+    __syncwarp();
+    if (!mbar_wait_bounded(&mma_bar, phase, kWaitLimit)) {
+      if (tid == 0) {
+        s_failed = 1;
+        stat_add(a.stats, TBE_STAT_WAIT_TIMEOUT, 1);
+      }
+    }
+    phase ^= 1u;
+    tc_fence_after();
+    __syncthreads();  // operands free for the next tile; s_failed visible
+    if (s_failed) break;
+  }
+  if (s_failed) mbar_wait_bounded(&mma_bar, phase ^ 1u, kWaitLimit);
+
+  // 4. this CTA's sums into the table's: thread = column d (warps 0-3), accumulator column = row e
+  if (mine > 0 && !s_failed && warp < kBM / kWarp) {
+    const int d = tid;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * kWarp) << 16);
+    for (int c0 = 0; c0 < a.N; c0 += 32) {
+      float v[32];
+      tmem_ld32(lane_addr + c0, v);
+      if (d < a.D) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c0 + i < a.E) atomicAdd(a.gsum + static_cast<int64_t>(c0 + i) * a.D + d, v[i]);
+      }
+    }
+  }
+  if (tid < a.E && s_rowcnt[tid] > 0) atomicAdd(a.rowcnt + tid, s_rowcnt[tid]);
+  __threadfence();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kBTmemCols);
+  if (tid == 0) s_last = atomicAdd(a.done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();  // acquire: every CTA's sums, published before its increment
+  // the optimizer, once per touched row: warp per row, lane over float4 slices
+  for (int e = warp; e < a.E; e += kThreads / kWarp) {
+    if (__ldcg(a.rowcnt + e) == 0) continue;  // untouched rows are not written
+    const int nv = a.D / 4;
+    float g[4][4];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int v = lane + j * kWarp;
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (v < nv) f = __ldcg(reinterpret_cast<const float4*>(a.gsum + static_cast<int64_t>(e) * a.D) + v);
+      g[j][0] = f.x;
+      g[j][1] = f.y;
+      g[j][2] = f.z;
+      g[j][3] = f.w;
+      ss += f.x * f.x + f.y * f.y + f.z * f.z + f.w * f.w;
+    }
+    float scale = a.lr;
+    if (a.opt == TBE_OPT_ROWWISE_ADAGRAD) {
+      for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(FULL, ss, m);
+      const float s_new = a.state[e] + ss / static_cast<float>(a.D);
+      __syncwarp();
+      if (lane == 0) a.state[e] = s_new;
+      scale = a.lr / (sqrtf(s_new) + a.eps);
+    }
+    __half* row = a.table + static_cast<int64_t>(e) * a.D;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int v = lane + j * kWarp;
+      if (v < nv) {
+        uint2 raw = reinterpret_cast<const uint2*>(row)[v];
+        __half2 p0 = *reinterpret_cast<__half2*>(&raw.x), p1 = *reinterpret_cast<__half2*>(&raw.y);
+        const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
+        p0 = __floats2half2_rn(f0.x - scale * g[j][0], f0.y - scale * g[j][1]);
+        p1 = __floats2half2_rn(f1.x - scale * g[j][2], f1.y - scale * g[j][3]);
+        raw.x = *reinterpret_cast<uint32_t*>(&p0);
+        raw.y = *reinterpret_cast<uint32_t*>(&p1);
+        reinterpret_cast<uint2*>(row)[v] = raw;
+      }
+    }
+  }
+}
+
 }  // namespace
 
 bool histogram_supported() { return true; }
@@ -342,6 +648,60 @@ cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, co
   const int64_t tiles = (P.B + kM - 1) / kM;
   // at most 4 CTAs per SM: 4 x 128 TMEM columns fit in the SM's 512 without waiting
   int64_t grid = static_cast<int64_t>(dev.sms) * 4;
+  if (tiles < grid) grid = tiles;
+  k<<<static_cast<int>(grid), kThreads, smem, s>>>(a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+size_t hist_backward_ws_bytes() { return kHistWsBytes; }
+
+cudaError_t launch_backward_histogram(const Problem& P, const BwdCtx& c, int table, void* hist_ws,
+                                      tbe_optimizer opt, const DeviceInfo& dev, cudaStream_t s) {
+  int64_t woff = 0, roff = 0, col0 = 0;
+  for (int t = 0; t < table; ++t) {
+    woff += P.E[t] * P.D[t];
+    roff += P.E[t];
+    col0 += P.D[t];
+  }
+  HistBwdArgs a;
+  a.indices = c.indices;
+  a.offsets = c.offsets;
+  a.grad_out = c.grad_out;
+  a.table = static_cast<__half*>(c.weights) + woff;
+  a.state = c.state == nullptr ? nullptr : c.state + roff;
+  char* ws = static_cast<char*>(hist_ws);
+  a.gsum = reinterpret_cast<float*>(ws);
+  a.rowcnt = reinterpret_cast<uint32_t*>(ws + kHistGsumBytes);
+  a.done = a.rowcnt + kK;
+  a.B = P.B;
+  a.num_indices = P.num_indices;
+  a.bag0 = static_cast<int64_t>(table) * P.B;
+  a.E = static_cast<int>(P.E[table]);
+  a.D = P.D[table];
+  a.N = (a.E + 15) / 16 * 16;
+  a.col0 = static_cast<int>(col0);
+  a.total_D = P.total_D;
+  a.opt = opt;
+  a.lr = c.lr;
+  a.eps = c.eps;
+  a.stats = c.stats;
+  if (P.B == 0) return cudaSuccess;
+  const size_t smem = 3 * kBATile + kBBTile + kBK * kK * 2 + 1024;
+  auto k = P.itype == TBE_I32 ? hist_bwd_kernel<int32_t> : hist_bwd_kernel<int64_t>;
+  static std::atomic<uint64_t> attr_set[2] = {{0}, {0}};
+  int dev_id = 0;
+  cudaError_t e = cudaGetDevice(&dev_id);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = uint64_t(1) << (dev_id & 63);
+  std::atomic<uint64_t>& flag = attr_set[P.itype == TBE_I32 ? 0 : 1];
+  if ((flag.load() & bit) == 0) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    flag.fetch_or(bit);
+  }
+  const int64_t tiles = (P.B + kBK - 1) / kBK;
+  int64_t grid = dev.sms;  // one CTA per SM (129 KB of shared memory each)
   if (tiles < grid) grid = tiles;
   k<<<static_cast<int>(grid), kThreads, smem, s>>>(a);
   note_launch();

@@ -49,21 +49,31 @@ struct ExpandArgs {
   float* psw_out;
   uint32_t* counters;
   unsigned long long* stats;
+  int nhist;                   // tables whose lookups stay out of the sort
+  int hist_t[kMaxHistTables];  // ascending
 };
 
 template <typename IT, bool PSW>
 __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
   __shared__ int64_t s_off[kExpandBags + 1];
   __shared__ unsigned long long s_bad;
+  __shared__ int64_t s_hlen[kMaxHistTables];
   const int64_t N = clamp64(ld_int<IT>(a.offsets, a.TB), 0, a.num_indices);
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * a.bags_per_cta;
   const int nb = static_cast<int>(min(static_cast<int64_t>(a.bags_per_cta), a.TB - i0));
-  if (threadIdx.x == 0) {
-    s_bad = 0;
-    if (blockIdx.x == 0) a.counters[TBE_CNT_N] = static_cast<uint32_t>(N);
+  // Lookups of the counts-path tables are left out: a lookup of table t lands at its position
+  // minus the lookups of the counts-path tables before t, and N shrinks by all of them.
+  if (threadIdx.x < a.nhist) {
+    const int64_t h0 = a.hist_t[threadIdx.x] * a.B;
+    const int64_t hs = clamp64(ld_int<IT>(a.offsets, h0), 0, N);
+    s_hlen[threadIdx.x] = clamp64(ld_int<IT>(a.offsets, h0 + a.B), hs, N) - hs;
   }
   for (int k = threadIdx.x; k <= nb; k += blockDim.x) s_off[k] = clamp64(ld_int<IT>(a.offsets, i0 + k), 0, N);
+  if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
+  int64_t n_kept = N;
+  for (int h = 0; h < a.nhist; ++h) n_kept -= s_hlen[h];
+  if (threadIdx.x == 0 && blockIdx.x == 0) a.counters[TBE_CNT_N] = static_cast<uint32_t>(n_kept < 0 ? 0 : n_kept);
   unsigned long long bad = 0;
   if (threadIdx.x < nb && s_off[threadIdx.x + 1] < s_off[threadIdx.x]) ++bad;  // decreasing offsets
   for (int k = threadIdx.x + kThreads; k < nb; k += blockDim.x)
@@ -71,7 +81,12 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
   const int64_t t0 = a.B > 0 ? i0 / a.B : 0;
   const int64_t r0 = i0 - t0 * a.B;
   const uint32_t B32 = static_cast<uint32_t>(a.B);
-  const int64_t p0 = s_off[0], p1 = max(s_off[0], s_off[nb]);
+  int64_t p0 = s_off[0], p1 = max(s_off[0], s_off[nb]);
+  if (a.nhist > 0 && nb > 0 && a.B > 0 && t0 == (i0 + nb - 1) / a.B) {
+    bool all = false;  // every bag of this CTA is in one counts-path table
+    for (int h = 0; h < a.nhist; ++h) all |= a.hist_t[h] == t0;
+    if (all) p1 = p0;
+  }
   constexpr int U = 4;  // lookups per thread in flight
   for (int64_t pb = p0; pb < p1; pb += U * blockDim.x) {
     int64_t id[U];
@@ -95,6 +110,15 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
       const uint32_t rel = static_cast<uint32_t>(r0 + lo);
       const int t = static_cast<int>(t0 + rel / B32);
       const uint32_t b = rel % B32;
+      int64_t q = p;  // where the lookup lands among the kept ones
+      if (a.nhist > 0) {
+        bool skip = false;
+        for (int h = 0; h < a.nhist; ++h) {
+          if (a.hist_t[h] < t) q -= s_hlen[h];
+          skip |= a.hist_t[h] == t;
+        }
+        if (skip || q < 0 || q >= n_kept) continue;  // (out of range only for unrepaired offsets)
+      }
       const int64_t rb = __ldg(a.roff + t);
       const int64_t E = __ldg(a.roff + t + 1) - rb;
       uint32_t key;
@@ -104,9 +128,9 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
         key = a.sentinel;
         ++bad;
       }
-      a.keys[p] = key;
-      a.vals[p] = b;
-      if (PSW) a.psw_out[p] = w[u];
+      a.keys[q] = key;
+      a.vals[q] = b;
+      if (PSW) a.psw_out[q] = w[u];
     }
   }
   if (bad) atomicAdd(&s_bad, bad);
@@ -471,6 +495,8 @@ cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s) {
   a.psw_out = c.pswbuf[0];
   a.counters = c.counters;
   a.stats = c.stats;
+  a.nhist = c.nhist;
+  for (int h = 0; h < kMaxHistTables; ++h) a.hist_t[h] = h < c.nhist ? c.hist_t[h] : 0;
   // about 16K lookups per CTA: bags per CTA from the mean bag length the host can see
   const int64_t mean_len = c.TB > 0 ? (c.num_indices + c.TB - 1) / c.TB : 1;
   int bpc = kExpandBags;

@@ -127,8 +127,15 @@ tbe_status device_info(DeviceInfo* out) {
   return TBE_OK;
 }
 
+bool hist_forward_eligible(const Problem& P, const tbe_options& o, int t) {
+  return o.histogram && histogram_supported() && P.wdtype == TBE_F16 && !P.weighted && P.E[t] <= 64 &&
+         P.D[t] >= 64 && P.D[t] <= 128 && P.long_bags[t] != 0;
+}
+
 BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const DeviceInfo& dev) {
   BwdLayout L;
+  for (int t = 0; t < P.T && L.nhist < kMaxHistTables; ++t)
+    if (hist_forward_eligible(P, opt, t)) L.hist_t[L.nhist++] = t;
   const uint32_t n_cap = static_cast<uint32_t>(P.num_indices);
   L.n_cap = n_cap;
   // key range [0, total_rows]: total_rows is the sentinel of an out-of-range id
@@ -188,6 +195,7 @@ BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const Device
   L.countdown = take(sizeof(uint32_t) * L.long_cap);
   L.ws_rows = take(static_cast<size_t>(L.long_cap) * P.max_D * L.acc_bytes);
   L.cls_counts = take(sizeof(uint32_t) * (kNumBuckets + 2) * L.cls_grid);
+  L.hist_ws = take(kHistWsBytes * L.nhist);
   L.total = off;
   return L;
 }
@@ -249,6 +257,9 @@ BwdCtx make_ctx(const Problem& P, const tbe_options& o, const BwdLayout& L, cons
   c.cls_counts = reinterpret_cast<uint32_t*>(base + L.cls_counts);
   c.rle_grid = L.rle_grid;
   c.stats = reinterpret_cast<unsigned long long*>(d_stats);
+  c.nhist = L.nhist;
+  for (int h = 0; h < kMaxHistTables; ++h) c.hist_t[h] = L.hist_t[h];
+  c.hist_ws = base + L.hist_ws;
   return c;
 }
 
@@ -390,13 +401,8 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
   // Tables on the counts x table path are skipped by the gather, which walks the remaining
   // contiguous table ranges.
   std::vector<int> hist;
-  if (o.histogram) {
-    for (int t = 0; t < P.T; ++t) {
-      const bool eligible = P.wdtype == TBE_F16 && !P.weighted && P.E[t] <= 64 && P.D[t] >= 64 &&
-                            P.D[t] <= 128 && P.long_bags[t] != 0 && !o.fused_bounds;
-      if (eligible && histogram_supported()) hist.push_back(t);
-    }
-  }
+  for (int t = 0; t < P.T; ++t)
+    if (!o.fused_bounds && hist_forward_eligible(P, o, t)) hist.push_back(t);
   int t0 = 0;
   size_t h = 0;
   while (t0 < P.T) {
@@ -500,6 +506,14 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
   record(o, TBE_BWD_EV_LONG, s);
   if (!fused && (e = launch_long_apply(P, c, L, optimizer, dev, s)) != cudaSuccess) return cuda_status(e);
   record(o, TBE_BWD_EV_APPLY, s);
+  if (c.nhist > 0) {
+    if ((e = cudaMemsetAsync(c.hist_ws, 0, kHistWsBytes * c.nhist, s)) != cudaSuccess) return cuda_status(e);
+    for (int h = 0; h < c.nhist; ++h) {
+      e = launch_backward_histogram(P, c, c.hist_t[h], c.hist_ws + kHistWsBytes * h, optimizer, dev, s);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+  }
+  record(o, TBE_BWD_EV_HISTOGRAM, s);
   return TBE_OK;
 }
 

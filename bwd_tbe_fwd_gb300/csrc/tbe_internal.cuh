@@ -48,6 +48,15 @@ struct DeviceInfo {
   int sms = 0;
 };
 
+// Tables whose backward goes through counts^T x grad_out on the tensor cores (the forward's
+// counts x table tables): at most kMaxHistTables per call, each with kHistWsBytes of workspace
+// zeroed per call (fp32 gradient sums of up to 64 x 128, row counts, a CTA counter).  Their
+// lookups stay out of the sort.
+constexpr int kMaxHistTables = 8;
+constexpr size_t kHistGsumBytes = 64 * 128 * 4;
+constexpr size_t kHistWsBytes = kHistGsumBytes + 512;
+bool hist_forward_eligible(const Problem& P, const tbe_options& o, int t);
+
 tbe_status make_problem(const tbe_problem* p, Problem* out);
 
 // Counts kernel launches of the current call on this host thread (reported through
@@ -66,6 +75,9 @@ struct BwdLayout {
   uint32_t long_cap = 0, chunk_cap = 0, u_cap = 0, n_cap = 0;
   int sort_grid = 1, rle_grid = 1, cls_grid = 1, key_bits = 1, passes = 1, radix_bits = 8, final_buf = 0;
   int acc_bytes = 4;  // fp32 workspace rows (fp64 for fp32 tables)
+  size_t hist_ws = 0;  // nhist x kHistWsBytes
+  int nhist = 0;
+  int hist_t[kMaxHistTables] = {0};
 };
 
 BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const DeviceInfo& dev);
@@ -124,6 +136,9 @@ struct BwdCtx {
   int sort_grid, rle_grid, cls_grid;
   uint32_t* cls_counts;             // [lists][cls_grid] per-block counts, then their prefixes
   unsigned long long* stats;
+  int nhist;                        // tables on the counts path (their lookups skip the sort)
+  int hist_t[kMaxHistTables];
+  char* hist_ws;
 };
 
 // ------------------------------------------------------------------------------------------
@@ -139,6 +154,8 @@ cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const
                                   unsigned long long* stats, const DeviceInfo& dev, cudaStream_t s);
 
 bool histogram_supported();
+cudaError_t launch_backward_histogram(const Problem& P, const BwdCtx& c, int table, void* hist_ws,
+                                      tbe_optimizer opt, const DeviceInfo& dev, cudaStream_t s);
 cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, const void* weights,
                                      const void* indices, const void* offsets, float* out, int table,
                                      unsigned long long* stats, const DeviceInfo& dev, cudaStream_t s);

@@ -25,9 +25,9 @@ TBE_LONG_AUTO, TBE_LONG_TWO_KERNEL, TBE_LONG_FUSED = 0, 1, 2
 TBE_SCHED_GRID, TBE_SCHED_PERSISTENT = 0, 1
 TBE_CLASSIFY_ATOMIC, TBE_CLASSIFY_ORDERED = 0, 1
 TBE_FWD_NUM_EVENTS = 3
-TBE_BWD_NUM_EVENTS = 8
+TBE_BWD_NUM_EVENTS = 9
 FWD_STAGES = ("gather", "histogram")
-BWD_STAGES = ("expand", "sort", "rle", "classify", "short", "long", "apply")
+BWD_STAGES = ("expand", "sort", "rle", "classify", "short", "long", "apply", "bwd_histogram")
 TBE_NUM_STATS = 8
 STAT_NAMES = ("bad_indices", "bad_offsets", "unrepaired", "wait_timeout")
 TBE_CNT_N, TBE_CNT_RUNS, TBE_CNT_LONG, TBE_CNT_CHUNKS, TBE_CNT_SHORT0 = 0, 1, 2, 3, 4

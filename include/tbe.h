@@ -120,7 +120,7 @@ enum {
 enum {
   TBE_BWD_EV_START = 0, TBE_BWD_EV_EXPAND = 1, TBE_BWD_EV_SORT = 2, TBE_BWD_EV_RLE = 3,
   TBE_BWD_EV_CLASSIFY = 4, TBE_BWD_EV_SHORT = 5, TBE_BWD_EV_LONG = 6, TBE_BWD_EV_APPLY = 7,
-  TBE_BWD_NUM_EVENTS = 8
+  TBE_BWD_EV_HISTOGRAM = 8, TBE_BWD_NUM_EVENTS = 9
 };
 
 typedef struct {

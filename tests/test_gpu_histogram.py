@@ -1,5 +1,5 @@
-"""The small-table counts x table forward (tcgen05 tensor cores) against the oracle and against
-the gather path on the same inputs."""
+"""The small-table counts x table forward and its counts^T x grad_out backward (tcgen05 tensor
+cores) against the oracle and against the gather / sort paths on the same inputs."""
 import dataclasses
 
 import numpy as np
@@ -53,3 +53,60 @@ def test_histogram_skips_out_of_range_ids():
     # after repair, the histogram path equals the oracle
     c.run_bounds()
     c.forward()
+
+
+@pytest.mark.parametrize("optimizer", ["adagrad", "sgd"])
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_histogram_backward_matches_oracle(name, optimizer):
+    """Table 0's update comes from counts^T x grad_out (three bf16 parts of the gradient); every
+    touched row is updated once, within tolerance of the oracle; the companion table goes through
+    the sort and its metadata is bit-exact."""
+    c = Case(CASES[name])
+    assert c.counts_path_tables() == [0]
+    c.backward(optimizer=optimizer)
+
+
+def test_histogram_backward_equals_sort_path():
+    cfg = CASES["tail_past_256_D64"]
+    c = Case(cfg)
+    w_sort = c.w0.cuda()
+    w_hist = c.w0.cuda()
+    s_sort = torch.zeros(cfg.total_rows, device="cuda")
+    s_hist = torch.zeros(cfg.total_rows, device="cuda")
+    g = c.grad.cuda()
+    off = TBEOptions(histogram=0)
+    c.tbe.backward_update(w_sort, s_sort, c.idx_d, c.off_d, g, lr=cfg.lr, eps=cfg.eps, options=off)
+    c.tbe.backward_update(w_hist, s_hist, c.idx_d, c.off_d, g, lr=cfg.lr, eps=cfg.eps)
+    torch.cuda.synchronize()
+    assert torch.allclose(w_hist.float(), w_sort.float(), rtol=2e-3, atol=1e-6)
+    assert torch.allclose(s_hist, s_sort, rtol=1e-5, atol=0)
+    # rows no lookup touched keep their bits on both paths
+    touched = np.zeros(cfg.total_rows, dtype=bool)
+    woff, roff = 0, 0
+    w_mask = np.zeros(c.w0.numel(), dtype=bool)
+    for t, spec in enumerate(cfg.tables):
+        ids = c.idx_h[c.off_h[t * cfg.B]:c.off_h[(t + 1) * cfg.B]]
+        rows = np.zeros(spec.E, dtype=bool)
+        rows[ids] = True
+        touched[roff:roff + spec.E] = rows
+        w_mask[woff:woff + spec.E * spec.D] = ~np.repeat(rows, spec.D)
+        woff += spec.E * spec.D
+        roff += spec.E
+    m = torch.from_numpy(w_mask).cuda()
+    assert torch.equal(w_hist[m], c.w0.cuda()[m]) and torch.equal(w_sort[m], c.w0.cuda()[m])
+    assert not bool(s_hist[torch.from_numpy(~touched).cuda()].any())
+
+
+def test_histogram_backward_counts_out_of_range_ids():
+    cfg = hist_config(64, 128, LengthSpec("fixed", 256), 512, bad=0.002, name="hist_bad_bwd")
+    c = Case(cfg, bounds_check=False)
+    n_bad = len(c.batch.bad_positions)
+    assert n_bad > 0
+    w = c.w0.cuda()
+    state = torch.zeros(cfg.total_rows, device="cuda")
+    c.tbe.backward_update(w, state, c.idx_d, c.off_d, c.grad.cuda(), stats=c.stats)
+    torch.cuda.synchronize()
+    assert c.stats[2].item() == n_bad
+    # after repair the update equals the oracle's
+    c.run_bounds()
+    c.backward()

@@ -42,6 +42,10 @@ def test_paths_exercised(case):
     m = case.tbe.metadata()
     if case.cfg.name.startswith("c1"):
         return  # uniform ids over 1000 rows: runs of length 1-2 only
+    if case.counts_path_tables():
+        # the skewed rows are the counts-path table's: the companion table's runs are short
+        assert m["short_per_bucket"].sum() > 0 and m["N"] < case.batch.N, m["N"]
+        return
     assert m["num_long"] > 0 and m["short_per_bucket"].sum() > 0, m["short_per_bucket"]
 
 
