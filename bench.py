@@ -134,7 +134,15 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None):
     hist_bytes = int(np.sum(st["per_table"][hist] * ib) + int(hist.sum()) * cfg.B * ib
                      + cfg.B * int(D[hist].sum()) * 4 + int(np.sum(cfg.E[hist] * D[hist] * wb)))
     hist_flops = int(np.sum(2 * cfg.B * cfg.E[hist] * D[hist]))
+    # backward of those tables: counts^T x grad_out (ids and offsets again, the gradient slice,
+    # the table and its state read and written once)
+    bwd_hist = int(np.sum(st["per_table"][hist] * ib) + int(hist.sum()) * cfg.B * ib
+                   + cfg.B * int(D[hist].sum()) * 4 + int(np.sum(cfg.E[hist] * (2 * D[hist] * wb + 8))))
+    bwd_hist_flops = hist_flops
     bounds = (TB + 1) * ib + N * ib
+    # the sort only sees the other tables' lookups and runs
+    N = N - int(np.sum(st["per_table"][hist]))
+    run_keep = ~hist[st["run_table"]]
     if passes is None:  # the library's choice: digits of 8-10 bits, ceil(bits / 10) passes
         bits = 1
         while (1 << bits) <= cfg.total_rows:
@@ -142,10 +150,11 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None):
         passes = (bits + 9) // 10
     expand = N * (ib + 8 + 2 * pw) + TB * ib
     sort = passes * N * (20 + 2 * pw)
-    rle = N * 8 + st["U"] * 8
-    classify = st["U"] * 20
-    Dr = D[st["run_table"]]
-    L = st["run_len"]
+    U = int(run_keep.sum())
+    rle = N * 8 + U * 8
+    classify = U * 20
+    Dr = D[st["run_table"][run_keep]]
+    L = st["run_len"][run_keep]
     short = L < threshold
     upd_short = int(np.sum(L[short] * (4 + pw + Dr[short] * 4) + 2 * Dr[short] * wb + 8 + 16))
     nch = -(-L[~short] // chunk)
@@ -153,6 +162,7 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None):
                           + 2 * Dr[~short] * wb + 8 + Dr[~short] * 4))
     return dict(bounds=bounds, gather=fwd, histogram=hist_bytes, histogram_flops=hist_flops, expand=expand,
                 sort=sort, rle=rle, classify=classify, short=upd_short, long=upd_long, apply=0,
+                bwd_histogram=bwd_hist, bwd_histogram_flops=bwd_hist_flops, lookups_sorted=N,
                 lookups_short=int(L[short].sum()), lookups_long=int(L[~short].sum()),
                 runs_short=int(short.sum()), runs_long=int((~short).sum()), passes=passes)
 
@@ -432,9 +442,10 @@ def run_ours(args):
         stages[name] = {"ms": round(float(ms), 4), "algorithmic_GB": round(gb, 4),
                         "GBps": round(gb / (ms / 1e3), 1) if ms > 0 and gb > 0 else None,
                         "frac": round(gb / (ms / 1e3) / peak, 4) if ms > 0 and gb > 0 else None}
-    if model["histogram_flops"] > 0 and stage_ms["histogram"] > 0:
-        stages["histogram"]["tensor_TFLOPs"] = round(model["histogram_flops"] / (stage_ms["histogram"] / 1e3) / 1e12, 3)
-    kernel_stages = ("gather", "histogram", "short", "long")
+    for name in ("histogram", "bwd_histogram"):
+        if model[name + "_flops"] > 0 and stage_ms[name] > 0:
+            stages[name]["tensor_TFLOPs"] = round(model[name + "_flops"] / (stage_ms[name] / 1e3) / 1e12, 3)
+    kernel_stages = ("gather", "histogram", "short", "long", "bwd_histogram")
     dom = max(kernel_stages, key=lambda n: stage_ms[n])
     achieved = model[dom] / 1e9 / (stage_ms[dom] / 1e3)
     traffic = profiled_traffic(dom, cfg.name)

@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
 // ------------------------------------------------------------------------------------------
 // Backward of a counts x table feature: the table's gradient is counts^T x grad_out.
 //
-// "Modernizing Table Batched Embeddings with FBTriton", section 2 ("Forward state reuse and
+// "Modernizing Table Batched Embeddings with FBTriton", section 2 ("Forward-state reuse and
 // preprocessing"): the backward of the small-table path can reuse the forward's per-bag counts,
 // multiply them into the upstream gradient on the tensor cores with a compensated split of the
 // fp32 gradient into 16-bit parts accumulating in fp32, then apply the optimizer to each row.

@@ -191,7 +191,7 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
                                void* ws, size_t ws_bytes, int64_t* d_stats, void* stream);
 
 /* The transpose half of the backward on its own ("Modernizing Table Batched Embeddings with
- * FBTriton", section 2, "Forward state reuse and preprocessing": the optional path that moves the
+ * FBTriton", section 2, "Forward-state reuse and preprocessing": the optional path that moves the
  * index transpose, sort and run-length encoding ahead of the backward): linearize, sort, run-length
  * encode and classify the batch's lookups into ws.  It reads only the layout, indices, offsets
  * and psw -- not the weights or the gradient -- so it can run before the gradient exists, e.g. on
