@@ -43,8 +43,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c3", help="workload: c1..c5 (default c3, the large skew batch)")
     ap.add_argument("--long-mode", choices=["auto", "two_kernel", "fused"], default="auto")
-    ap.add_argument("--scheduler", choices=["grid", "persistent"], default="grid")
-    ap.add_argument("--classify", choices=["atomic", "ordered"], default="atomic")
+    ap.add_argument("--scheduler", choices=["grid", "persistent", "clc"], default="persistent")
+    ap.add_argument("--merge", choices=["atomic", "bulk"], default="atomic")
+    ap.add_argument("--classify", choices=["atomic", "ordered"], default="ordered")
     ap.add_argument("--hoist", choices=["on", "off"], default="off",
                     help="run the backward's transpose (tbe_backward_prepare) on a second stream beside "
                          "the forward gather")
@@ -302,11 +303,14 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
+_CSRC = "bwd_tbe_fwd_gb300/csrc/"
 KERNEL_SOURCES = {
-    "gather": ["bwd_tbe_fwd_gb300/csrc/k_forward.cu", "bwd_tbe_fwd_gb300/csrc/tbe_internal.cuh"],
-    "short": ["bwd_tbe_fwd_gb300/csrc/k_update.cu", "bwd_tbe_fwd_gb300/csrc/tbe_internal.cuh"],
-    "long": ["bwd_tbe_fwd_gb300/csrc/k_update.cu", "bwd_tbe_fwd_gb300/csrc/tbe_internal.cuh"],
-    "sort": ["bwd_tbe_fwd_gb300/csrc/k_sort.cu", "bwd_tbe_fwd_gb300/csrc/tbe_internal.cuh"],
+    "gather": [_CSRC + "k_forward.cu", _CSRC + "tbe_internal.cuh"],
+    "short": [_CSRC + "k_short.cu", _CSRC + "k_update_common.cuh", _CSRC + "tbe_internal.cuh"],
+    "long": [_CSRC + "k_long.cu", _CSRC + "k_update_common.cuh", _CSRC + "tbe_internal.cuh"],
+    "sort": [_CSRC + "k_sort.cu", _CSRC + "tbe_internal.cuh"],
+    "histogram": [_CSRC + "k_hist.cu", _CSRC + "tbe_internal.cuh"],
+    "bwd_histogram": [_CSRC + "k_hist.cu", _CSRC + "tbe_internal.cuh"],
 }
 
 
@@ -352,7 +356,8 @@ def run_ours(args):
     batch = make_batch(cfg)
     st = batch_stats(cfg, batch)
     opts = TBEOptions(long_mode={"auto": 0, "two_kernel": 1, "fused": 2}[args.long_mode],
-                      scheduler={"grid": 0, "persistent": 1}[args.scheduler],
+                      scheduler={"grid": 0, "persistent": 1, "clc": 2}[args.scheduler],
+                      merge={"atomic": 0, "bulk": 1}[args.merge],
                       classify_mode={"atomic": 0, "ordered": 1}[args.classify])
     itype = torch.int32 if cfg.itype == "i32" else torch.int64
     tbe = TableBatchedEmbedding(cfg.D, cfg.E, cfg.B, batch.N, torch_dtype(cfg.wdtype), itype,
@@ -502,7 +507,7 @@ def run_ours(args):
                 "long_runs": model["runs_long"], "lookups_in_long_runs": model["lookups_long"],
                 "weights_storage": cfg.wdtype, "step": ("tbe_bounds_check + (tbe_forward || tbe_backward_prepare) + tbe_backward_update(prepared)"
                          if args.hoist == "on" else "tbe_bounds_check + tbe_forward + tbe_backward_update"),
-                "long_mode": args.long_mode, "scheduler": args.scheduler, "classify": args.classify,
+                "long_mode": args.long_mode, "scheduler": args.scheduler, "merge": args.merge, "classify": args.classify,
                 "transpose": "hoisted beside the forward (second stream)" if args.hoist == "on" else "in the backward",
                 "parallelism": f"replicas x{world}",
                 "l2": "inputs larger than L2 (weights alone exceed 129 MB); no flush between steps",

@@ -67,32 +67,19 @@ __device__ __forceinline__ void apply_from_workspace(const BwdCtx& c, uint32_t k
   apply_row_group<WT, OPT, Acc, MAXV>(wrow, c.state + key, g, lane, kWarp, nv, D, c.lr, c.eps, FULL);
 }
 
-template <typename WT, bool PSW, int OPT, int MAXV, bool FUSED, bool PERSIST>
-__global__ void __launch_bounds__(kThreads, 4) long_chunk_kernel(BwdCtx c,
-                                                                const uint32_t* __restrict__ sorted_vals,
-                                                                const float* __restrict__ sorted_psw) {
+// Sum of one chunk of a long run merged into the run's workspace row; with FUSED, the chunk
+// that takes the run's countdown to zero applies the optimizer.
+template <typename WT, bool PSW, int OPT, int MAXV, bool FUSED>
+__device__ __forceinline__ void long_chunk_body(const BwdCtx& c, int64_t ci, const uint32_t* __restrict__ sorted_vals,
+                                                const float* __restrict__ sorted_psw, bool merge_bulk,
+                                                void* srow) {
   using Acc = typename WTraits<WT>::Acc;
-  constexpr int UNROLL = MAXV == 1 ? 8 : 4;  // rows in flight per lane
+  constexpr int UNROLL = 8 / MAXV > 0 ? 8 / MAXV : 1;  // rows in flight per lane: 8 float4 loads
   const int lane = lane_id();
-  const uint32_t nchunks = min(c.counters[TBE_CNT_CHUNKS], c.chunk_cap);
-  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / kWarp;
-  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) / kWarp;
   const size_t row_bytes = static_cast<size_t>(c.max_D) * sizeof(Acc);
-  int64_t it = 0;
-  while (true) {
-    int64_t ci;
-    if (PERSIST) {
-      uint32_t x = 0;
-      if (lane == 0) x = atomicAdd(c.counters + kWorkLong, 1u);
-      ci = __shfl_sync(FULL, x, 0);
-    } else {
-      ci = gw + it * nw;
-      ++it;
-    }
-    if (ci >= nchunks) break;
     const uint4 rec = __ldg(c.chunks + ci);  // {first lookup, end, key, slot}
     const uint32_t s = rec.x, e = rec.y, key = rec.z, slot = rec.w;
-    if (slot >= c.long_cap) continue;
+    if (slot >= c.long_cap) return;
     const int t = table_of_row(c.roff, c.T, key);
     const int col0 = __ldg(c.doff + t);
     const int D = __ldg(c.doff + t + 1) - col0;
@@ -191,7 +178,28 @@ __global__ void __launch_bounds__(kThreads, 4) long_chunk_kernel(BwdCtx c,
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[k][i] += __shfl_xor_sync(FULL, acc[k][i], m);
     void* ws_row = static_cast<char*>(c.ws_rows) + static_cast<size_t>(slot) * row_bytes;
-    if (rs == 0) {
+    if (merge_bulk) {
+      // the chunk sum into this warp's shared-memory row, then one bulk reduction (an
+      // asynchronous add of the whole row into the workspace, performed in L2) by lane 0
+      if (rs == 0) {
+#pragma unroll
+        for (int k = 0; k < MAXV; ++k) {
+          const int vec = vi + k * kWarp;
+          if (vec < nv) {
+            if constexpr (sizeof(Acc) == 8) {
+              reinterpret_cast<double2*>(srow)[2 * vec] = make_double2(acc[k][0], acc[k][1]);
+              reinterpret_cast<double2*>(srow)[2 * vec + 1] = make_double2(acc[k][2], acc[k][3]);
+            } else {
+              reinterpret_cast<float4*>(srow)[vec] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the bulk copy reads the row through the async proxy
+      __syncwarp();
+      if (lane == 0) bulk_reduce_add<Acc>(ws_row, srow, static_cast<uint32_t>(D * sizeof(Acc)));
+      __syncwarp();
+    } else if (rs == 0) {
 #pragma unroll
       for (int k = 0; k < MAXV; ++k) {
         const int vec = vi + k * kWarp;
@@ -210,6 +218,55 @@ __global__ void __launch_bounds__(kThreads, 4) long_chunk_kernel(BwdCtx c,
         apply_from_workspace<WT, OPT, Acc, MAXV>(c, key, ws_row);
       }
     }
+}
+
+// Work distribution (tbe_scheduler): GRID = the warps of one resident wave take a fixed stride
+// of the chunk list; PERSISTENT = resident warps claim chunks from an atomic counter; CLC = one
+// CTA per 8 chunks, whose CTAs, when done, cancel a CTA that has not started yet (cluster launch
+// control) and take its chunks instead, so an SM keeps its CTA rather than launching a new one
+// ([FBT] section 4, Problem 1, Solution 1.2).
+template <typename WT, bool PSW, int OPT, int MAXV, bool FUSED>
+__global__ void __launch_bounds__(kThreads, 4) long_chunk_kernel(BwdCtx c,
+                                                                const uint32_t* __restrict__ sorted_vals,
+                                                                const float* __restrict__ sorted_psw,
+                                                                int sched, int merge) {
+  extern __shared__ __align__(16) uint8_t long_smem[];  // bulk merge: one workspace row per warp
+  __shared__ __align__(16) uint4 clc_resp;
+  __shared__ __align__(8) uint64_t clc_bar;
+  __shared__ int64_t clc_vb;
+  using Acc = typename WTraits<WT>::Acc;
+  const int lane = lane_id();
+  const int wib = threadIdx.x / kWarp, wpb = blockDim.x / kWarp;
+  const uint32_t nchunks = min(c.counters[TBE_CNT_CHUNKS], c.chunk_cap);
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / kWarp;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) / kWarp;
+  const bool merge_bulk = merge == TBE_MERGE_BULK;
+  void* srow = long_smem + static_cast<size_t>(wib) * c.max_D * sizeof(Acc);
+  if (sched == TBE_SCHED_CLC) {
+    if (threadIdx.x == 0) clc_init(&clc_bar);
+    __syncthreads();
+  }
+  int64_t vb = blockIdx.x;
+  uint32_t clc_phase = 0;
+  for (int64_t it = 0;; ++it) {
+    int64_t ci;
+    if (sched == TBE_SCHED_PERSISTENT) {
+      uint32_t x = 0;
+      if (lane == 0) x = atomicAdd(c.counters + kWorkLong, 1u);
+      ci = __shfl_sync(FULL, x, 0);
+      if (ci >= nchunks) break;
+    } else if (sched == TBE_SCHED_CLC) {
+      if (it > 0) {
+        if ((vb + 1) * wpb >= nchunks) break;  // later CTAs hold no chunks either (CTA-uniform)
+        vb = clc_steal(&clc_resp, &clc_bar, &clc_vb, clc_phase, c.stats);
+        if (vb < 0) break;
+      }
+      ci = vb * wpb + wib;
+    } else {
+      ci = gw + it * nw;
+      if (ci >= nchunks) break;
+    }
+    if (ci < nchunks) long_chunk_body<WT, PSW, OPT, MAXV, FUSED>(c, ci, sorted_vals, sorted_psw, merge_bulk, srow);
   }
 }
 
@@ -229,33 +286,35 @@ __global__ void __launch_bounds__(kThreads) long_apply_kernel(BwdCtx c) {
 }
 
 template <typename WT, bool PSW, int OPT, int MAXV>
-cudaError_t launch_long_t(const BwdCtx& c, const uint32_t* vals, const float* psw, bool fused,
-                          bool persist, const DeviceInfo& dev, cudaStream_t s) {
+cudaError_t launch_long_t(const BwdCtx& c, const uint32_t* vals, const float* psw, bool fused, int sched,
+                          int merge, const DeviceInfo& dev, cudaStream_t s) {
+  using Acc = typename WTraits<WT>::Acc;
   const int64_t want = (static_cast<int64_t>(c.chunk_cap) + (kThreads / kWarp) - 1) / (kThreads / kWarp);
-#define TBE_LONG_LAUNCH(F, P)                                            \
-  {                                                                      \
-    auto k = long_chunk_kernel<WT, PSW, OPT, MAXV, F, P>;                \
-    const int grid = persistent_grid(k, kThreads, 0, dev, want);         \
-    k<<<grid, kThreads, 0, s>>>(c, vals, psw);                           \
-    note_launch();                                                   \
-  }
-  if (fused) {
-    if (persist) TBE_LONG_LAUNCH(true, true) else TBE_LONG_LAUNCH(true, false)
-  } else {
-    if (persist) TBE_LONG_LAUNCH(false, true) else TBE_LONG_LAUNCH(false, false)
-  }
-#undef TBE_LONG_LAUNCH
+  // bulk merge: one workspace row per warp in shared memory (up to the default 48 KB)
+  size_t smem = static_cast<size_t>(kThreads / kWarp) * c.max_D * sizeof(Acc);
+  if (merge == TBE_MERGE_BULK && smem > 48 * 1024) merge = TBE_MERGE_ATOMIC;
+  if (merge != TBE_MERGE_BULK) smem = 0;
+  auto k = fused ? long_chunk_kernel<WT, PSW, OPT, MAXV, true> : long_chunk_kernel<WT, PSW, OPT, MAXV, false>;
+  const int64_t resident = persistent_grid(k, kThreads, smem, dev, INT64_MAX);
+  int64_t grid;
+  if (sched == TBE_SCHED_PERSISTENT) grid = resident;                      // claims from a counter
+  else if (sched == TBE_SCHED_CLC) grid = want;                            // one CTA per 8 chunks, stolen when idle
+  else grid = resident;                                                    // one resident wave, grid stride
+  if (grid > want) grid = want;
+  if (grid > 0x7fffffff) grid = 0x7fffffff;
+  k<<<static_cast<int>(grid < 1 ? 1 : grid), kThreads, smem, s>>>(c, vals, psw, sched, merge);
+  note_launch();
   return cudaGetLastError();
 }
 
 template <typename WT, bool PSW, int OPT>
-cudaError_t launch_long_maxv(const BwdCtx& c, const uint32_t* vals, const float* psw, bool fused,
-                             bool persist, int maxv, const DeviceInfo& dev, cudaStream_t s) {
+cudaError_t launch_long_maxv(const BwdCtx& c, const uint32_t* vals, const float* psw, bool fused, int sched,
+                             int merge, int maxv, const DeviceInfo& dev, cudaStream_t s) {
   switch (maxv) {
-    case 1: return launch_long_t<WT, PSW, OPT, 1>(c, vals, psw, fused, persist, dev, s);
-    case 2: return launch_long_t<WT, PSW, OPT, 2>(c, vals, psw, fused, persist, dev, s);
-    case 4: return launch_long_t<WT, PSW, OPT, 4>(c, vals, psw, fused, persist, dev, s);
-    default: return launch_long_t<WT, PSW, OPT, 8>(c, vals, psw, fused, persist, dev, s);
+    case 1: return launch_long_t<WT, PSW, OPT, 1>(c, vals, psw, fused, sched, merge, dev, s);
+    case 2: return launch_long_t<WT, PSW, OPT, 2>(c, vals, psw, fused, sched, merge, dev, s);
+    case 4: return launch_long_t<WT, PSW, OPT, 4>(c, vals, psw, fused, sched, merge, dev, s);
+    default: return launch_long_t<WT, PSW, OPT, 8>(c, vals, psw, fused, sched, merge, dev, s);
   }
 }
 
@@ -282,21 +341,24 @@ cudaError_t launch_apply_maxv(const BwdCtx& c, int maxv, const DeviceInfo& dev, 
 }  // namespace
 
 cudaError_t launch_long_updates(const Problem& P, const BwdCtx& c, const BwdLayout& L,
-                                tbe_optimizer opt, bool fused, int scheduler, const DeviceInfo& dev,
-                                cudaStream_t s) {
+                                tbe_optimizer opt, bool fused, int scheduler, int merge,
+                                const DeviceInfo& dev, cudaStream_t s) {
   if (c.long_cap == 0) return cudaSuccess;
   const uint32_t* vals = c.vals[L.final_buf];
   const float* psw = P.weighted ? c.pswbuf[L.final_buf] : nullptr;
-  const bool persist = scheduler == TBE_SCHED_PERSISTENT;
   const int maxv = maxv_for(P.max_D);
   return by_weight_type(P.wdtype, [&](auto w) -> cudaError_t {
     using WT = decltype(w);
     if (P.weighted) {
-      return opt == TBE_OPT_SGD ? launch_long_maxv<WT, true, TBE_OPT_SGD>(c, vals, psw, fused, persist, maxv, dev, s)
-                                : launch_long_maxv<WT, true, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, persist, maxv, dev, s);
+      return opt == TBE_OPT_SGD
+                 ? launch_long_maxv<WT, true, TBE_OPT_SGD>(c, vals, psw, fused, scheduler, merge, maxv, dev, s)
+                 : launch_long_maxv<WT, true, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, scheduler, merge, maxv,
+                                                                       dev, s);
     }
-    return opt == TBE_OPT_SGD ? launch_long_maxv<WT, false, TBE_OPT_SGD>(c, vals, psw, fused, persist, maxv, dev, s)
-                              : launch_long_maxv<WT, false, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, persist, maxv, dev, s);
+    return opt == TBE_OPT_SGD
+               ? launch_long_maxv<WT, false, TBE_OPT_SGD>(c, vals, psw, fused, scheduler, merge, maxv, dev, s)
+               : launch_long_maxv<WT, false, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, scheduler, merge, maxv,
+                                                                      dev, s);
   });
 }
 

@@ -54,7 +54,9 @@ tbe_options resolve(const tbe_options* opt) {
 tbe_status check_options(const tbe_options& o) {
   if (o.long_threshold < 1 || o.chunk < 1) return TBE_ERR_INVALID_ARG;
   if (o.long_mode < TBE_LONG_AUTO || o.long_mode > TBE_LONG_FUSED) return TBE_ERR_INVALID_ARG;
-  if (o.scheduler != TBE_SCHED_GRID && o.scheduler != TBE_SCHED_PERSISTENT) return TBE_ERR_INVALID_ARG;
+  if (o.scheduler != TBE_SCHED_GRID && o.scheduler != TBE_SCHED_PERSISTENT && o.scheduler != TBE_SCHED_CLC)
+    return TBE_ERR_INVALID_ARG;
+  if (o.merge != TBE_MERGE_ATOMIC && o.merge != TBE_MERGE_BULK) return TBE_ERR_INVALID_ARG;
   if (o.num_events < 0 || (o.num_events > 0 && o.events == nullptr)) return TBE_ERR_INVALID_ARG;
   if (o.classify_mode != TBE_CLASSIFY_ORDERED && o.classify_mode != TBE_CLASSIFY_ATOMIC) return TBE_ERR_INVALID_ARG;
   if (o.prepared != 0 && o.prepared != 1) return TBE_ERR_INVALID_ARG;
@@ -313,14 +315,15 @@ void tbe_default_options(tbe_options* opt) {
   opt->long_threshold = 256;
   opt->chunk = 256;
   opt->long_mode = TBE_LONG_AUTO;
-  opt->scheduler = TBE_SCHED_GRID;
+  opt->scheduler = TBE_SCHED_PERSISTENT;
   opt->histogram = 1;
   opt->fused_bounds = 0;
   opt->events = nullptr;
   opt->num_events = 0;
   opt->launch_counter = nullptr;
-  opt->classify_mode = TBE_CLASSIFY_ATOMIC;
+  opt->classify_mode = TBE_CLASSIFY_ORDERED;
   opt->prepared = 0;
+  opt->merge = TBE_MERGE_ATOMIC;
 }
 
 tbe_status tbe_table_layout(const tbe_problem* prob, int64_t* weight_offsets, int32_t* D_offsets,
@@ -501,7 +504,7 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
   if ((e = launch_short_updates(P, c, L, optimizer, o.scheduler, dev, s)) != cudaSuccess)
     return cuda_status(e);
   record(o, TBE_BWD_EV_SHORT, s);
-  if ((e = launch_long_updates(P, c, L, optimizer, fused, o.scheduler, dev, s)) != cudaSuccess)
+  if ((e = launch_long_updates(P, c, L, optimizer, fused, o.scheduler, o.merge, dev, s)) != cudaSuccess)
     return cuda_status(e);
   record(o, TBE_BWD_EV_LONG, s);
   if (!fused && (e = launch_long_apply(P, c, L, optimizer, dev, s)) != cudaSuccess) return cuda_status(e);

@@ -168,8 +168,8 @@ cudaError_t launch_short_updates(const Problem& P, const BwdCtx& c, const BwdLay
                                  tbe_optimizer opt, int scheduler, const DeviceInfo& dev,
                                  cudaStream_t s);
 cudaError_t launch_long_updates(const Problem& P, const BwdCtx& c, const BwdLayout& L,
-                                tbe_optimizer opt, bool fused, int scheduler, const DeviceInfo& dev,
-                                cudaStream_t s);
+                                tbe_optimizer opt, bool fused, int scheduler, int merge,
+                                const DeviceInfo& dev, cudaStream_t s);
 cudaError_t launch_long_apply(const Problem& P, const BwdCtx& c, const BwdLayout& L,
                               tbe_optimizer opt, const DeviceInfo& dev, cudaStream_t s);
 
@@ -324,19 +324,73 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) global -> shared.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // Orders this thread's earlier shared-memory accesses before later bulk-copy (async proxy)
 // accesses of the same memory, and makes barrier initialisation visible to it.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk reduction (sm_90+): global[dst .. dst+bytes) += shared[src ..), element type Acc (f32 or
+// f64), performed by the async proxy in L2.  bytes is a multiple of 16, both addresses 16-byte
+// aligned.  Waits until the additions have been performed, then orders them before this
+// thread's later generic-proxy accesses of global memory.
+template <typename Acc>
+__device__ __forceinline__ void bulk_reduce_add(void* dst, const void* src, uint32_t bytes) {
+  if constexpr (sizeof(Acc) == 8) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f64 [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+  } else {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+  }
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Cluster launch control (sm_100+).  clc_init by one thread before a __syncthreads; clc_steal
+// by every thread of the CTA: it asks the hardware to cancel a CTA of this grid that has not
+// started, and returns that CTA's x index (whose work the caller then does) or -1 when none is
+// left.  The response wait is bounded; on time-out the CTA counts TBE_STAT_WAIT_TIMEOUT, waits
+// once more for the response (bounded) and stops stealing.
+constexpr uint32_t kClcWaitLimit = 1u << 22;
+
+__device__ __forceinline__ void clc_init(uint64_t* bar) {
+  mbar_init(bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ int64_t clc_steal(uint4* resp, uint64_t* bar, int64_t* next, uint32_t& phase,
+                                             unsigned long long* stats) {
+  __syncthreads();  // every warp is done with the current block (and has read *next)
+  if (threadIdx.x == 0) {
+    int64_t nb = -1;
+    mbar_arrive_expect_tx(bar, 16);
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                     smem_u32(resp)),
+                 "r"(smem_u32(bar))
+                 : "memory");
+    if (mbar_wait_bounded(bar, phase, kClcWaitLimit)) {
+      uint32_t cancelled = 0, x = 0;
+      asm volatile(
+          "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\tld.shared.b128 r, [%2];\n\t"
+          "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\tselp.u32 %0, 1, 0, p;\n\t"
+          "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+          : "=r"(cancelled), "=r"(x)
+          : "r"(smem_u32(resp))
+          : "memory");
+      if (cancelled) nb = x;
+    } else {
+      stat_add(stats, TBE_STAT_WAIT_TIMEOUT, 1);
+      mbar_wait_bounded(bar, phase, kClcWaitLimit);
+    }
+    *next = nb;
+  }
+  phase ^= 1u;
+  __syncthreads();
+  return *next;
 }
 
 template <typename Raw>

@@ -77,17 +77,31 @@ typedef enum { TBE_OPT_SGD = 0, TBE_OPT_ROWWISE_ADAGRAD = 1 } tbe_optimizer;
 typedef enum { TBE_LONG_AUTO = 0, TBE_LONG_TWO_KERNEL = 1, TBE_LONG_FUSED = 2 } tbe_long_mode;
 
 /* Work distribution of the backward update kernels ([FBT] section 4, Problem 1, Solution 1.2):
- * GRID = each warp takes a fixed stride of the device-side run/chunk lists; PERSISTENT = a
- * persistent grid whose warps claim the next run or chunk from an atomic counter until none
- * is left. */
-typedef enum { TBE_SCHED_GRID = 0, TBE_SCHED_PERSISTENT = 1 } tbe_scheduler;
+ * GRID = each warp of one resident wave takes a fixed stride of the device-side run/chunk
+ * lists (short runs: sixteen waves); PERSISTENT = a persistent
+ * grid whose warps claim the next run or chunk from an atomic counter until none is left;
+ * CLC = (long-run chunks; short runs as GRID) one CTA per 8 chunks (sized by the chunk
+ * capacity), whose CTAs, when done, cancel a CTA that has not started (cluster launch control,
+ * sm_100+) and process its chunks instead. */
+typedef enum { TBE_SCHED_GRID = 0, TBE_SCHED_PERSISTENT = 1, TBE_SCHED_CLC = 2 } tbe_scheduler;
+/* (PERSISTENT is the default: on the 83.9M-lookup stress batch it takes the short runs from 2.0
+ * to 1.45 ms and the long chunks from 3.5 to 3.1 ms; CLC gives 3.3 ms for the chunks.) */
 
-/* How the run classifier compacts runs into its lists ([FBT] section 4: one reservation per
- * block per list, offsets inside the block from prefix sums, counts kept on the device):
- * ATOMIC reserves with one atomicAdd per block per list, so the lists come out in arbitrary
- * block order; ORDERED reserves with a scan over the blocks' counts (no atomics), so the lists
- * are in key order (three launches instead of one).  Both give the same updates and counts;
- * ATOMIC, the pages' scheme, is the default. */
+/* How a long-run chunk merges its partial sum into the run's workspace row ([FBT] section 4,
+ * Problem 6): ATOMIC = vector atomic adds from registers (red.global.add.v4.f32); BULK = the
+ * warp stages the row in shared memory and one lane issues a bulk reduction
+ * (cp.reduce.async.bulk .add) of the whole row, performed in L2 (falls back to ATOMIC when a
+ * CTA's rows would exceed 48 KB of shared memory). */
+typedef enum { TBE_MERGE_ATOMIC = 0, TBE_MERGE_BULK = 1 } tbe_merge_mode;
+
+/* How the run classifier compacts runs into its lists ([FBT] section 4, Problem 4: one reservation
+ * per block per list, offsets inside the block from prefix sums, counts kept on the device):
+ * ATOMIC reserves with one atomicAdd per block per list, so the lists come out in block
+ * completion order; ORDERED reserves with a scan over the blocks' counts (no atomics, three
+ * launches), so the lists are in key order.  Both give the same updates and counts.  ORDERED is
+ * the default: with the PERSISTENT scheduler the warps then work through one table's rows at a
+ * time, whose gradient slice stays in L2 (stress batch: long chunks 3.1 -> 1.9 ms, short runs
+ * 1.43 -> 1.22 ms). */
 typedef enum { TBE_CLASSIFY_ATOMIC = 0, TBE_CLASSIFY_ORDERED = 1 } tbe_classify_mode;
 
 /* Host description of the problem.  Nothing here is read from the device. */
@@ -136,6 +150,7 @@ typedef struct {
   int32_t classify_mode;      /* tbe_classify_mode */
   int32_t prepared;           /* 1: tbe_backward_update takes the transpose from ws, where
                                  tbe_backward_prepare left it, instead of computing it */
+  int32_t merge;              /* tbe_merge_mode */
 } tbe_options;
 
 /* Indices into d_stats (int64).  Counts accumulate over calls. */

@@ -46,7 +46,8 @@ def test_version_status_and_defaults(lib):
     o = tbe.Options()
     lib.tbe_default_options(ctypes.byref(o))
     assert (o.long_threshold, o.chunk, o.long_mode, o.scheduler, o.histogram, o.fused_bounds) == \
-        (256, 256, tbe.TBE_LONG_AUTO, tbe.TBE_SCHED_GRID, 1, 0)
+        (256, 256, tbe.TBE_LONG_AUTO, tbe.TBE_SCHED_PERSISTENT, 1, 0)
+    assert (o.classify_mode, o.prepared, o.merge) == (tbe.TBE_CLASSIFY_ORDERED, 0, 0)
 
 
 def test_table_layout(lib):

@@ -66,21 +66,36 @@ def test_threshold_sweep_same_answer(threshold, chunk):
     c.backward()
 
 
+@pytest.mark.parametrize("merge", ["atomic", "bulk"])
 @pytest.mark.parametrize("long_mode", ["two_kernel", "fused"])
-@pytest.mark.parametrize("scheduler", ["grid", "persistent"])
-def test_long_modes_and_schedulers(long_mode, scheduler):
+@pytest.mark.parametrize("scheduler", ["grid", "persistent", "clc"])
+def test_long_modes_and_schedulers(long_mode, scheduler, merge):
+    """Every way of distributing the long-run chunks (fixed stride, atomic claims, cluster launch
+    control) and of merging their partial sums (vector atomics, bulk reductions) gives the
+    oracle's updates."""
     opts = TBEOptions(long_mode={"two_kernel": 1, "fused": 2}[long_mode],
-                      scheduler={"grid": 0, "persistent": 1}[scheduler])
+                      scheduler={"grid": 0, "persistent": 1, "clc": 2}[scheduler],
+                      merge={"atomic": 0, "bulk": 1}[merge])
     for name in ("c3", "c5"):
         c = Case(SMALL[name], options=opts)
         c.backward(options=opts)
 
 
+@pytest.mark.parametrize("merge", ["atomic", "bulk"])
+def test_fp64_long_runs(merge):
+    """fp32 tables accumulate the long runs in fp64 (an f64 bulk reduction with merge=bulk):
+    every run of the tiny workload forced onto the long path in chunks of 2."""
+    opts = TBEOptions(merge={"atomic": 0, "bulk": 1}[merge], scheduler=2)
+    c = Case(SMALL["c1"], threshold=2, chunk=2, options=opts)
+    assert c.backward(options=opts)["num_lookups"] > 0
+    assert c.tbe.metadata()["num_long"] > 0
+
+
 @pytest.mark.parametrize("name", ["c3", "c5", "c2"])
-def test_ordered_classifier(name):
-    """The order-preserving compaction (a scan over the blocks' counts, lists in key order) gives
-    the same updates and the same route counts as the default atomic one."""
-    opts = TBEOptions(classify_mode=1)
+def test_atomic_classifier(name):
+    """The pages' compaction (one atomicAdd per block per list, lists in block order) gives the
+    same updates and the same route counts as the default order-preserving one."""
+    opts = TBEOptions(classify_mode=0)
     c = Case(SMALL[name], options=opts)
     c.backward(options=opts)
 
