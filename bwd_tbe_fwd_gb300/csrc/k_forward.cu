@@ -160,9 +160,12 @@ fwd_gather_kernel(FwdArgs a) {
     const int rps = kWarp / lpr;                                    // rows per load step
     const int slot = lane / lpr;
     const int vi = lane & (lpr - 1);
-    // this lane's first vector of row 0 of the table, and of the item's first output row
-    const Raw* table =
-        reinterpret_cast<const Raw*>(static_cast<const WT*>(a.weights) + __ldg(a.woff + t)) + vi;
+    // row 0 of the table; this lane's vectors of a row (lanes past the row width re-read its last
+    // vector in full batches: their sums are never stored); the item's first output row
+    const Raw* table = reinterpret_cast<const Raw*>(static_cast<const WT*>(a.weights) + __ldg(a.woff + t));
+    int vk[MAXV];
+#pragma unroll
+    for (int m = 0; m < MAXV; ++m) vk[m] = min(vi + m * kWarp, nvec - 1);
     float* orow = a.out + b0 * a.total_D + col0 + vi * NE;
     const int qmax = min(UNROLL, kWarp / rps);  // a batch covers at most 32 positions
 
@@ -223,21 +226,34 @@ fwd_gather_kernel(FwdArgs a) {
           const float pb = __shfl_sync(FULL, wb.w, rel & (kWarp - 1));
           my_w = rel < kWarp ? pa : pb;
         }
+        const bool chunk_ok = __all_sync(FULL, lane >= n || my_id >= 0);  // no skipped id
         for (int j = 0; j < n; j += rps * qmax) {
           Raw v[UNROLL][MAXV];
           float w[UNROLL];
+          if (chunk_ok && qmax == UNROLL && j + rps * UNROLL <= n) {
+            // every row of the batch is valid: unpredicated loads
 #pragma unroll
-          for (int q = 0; q < UNROLL; ++q) {
-            const int r = j + q * rps + slot;  // < 64; lanes past n hold -1
-            const int32_t id = __shfl_sync(FULL, my_id, r & (kWarp - 1));
-            w[q] = PSW ? __shfl_sync(FULL, my_w, r & (kWarp - 1)) : 1.0f;
-            const bool ok = q < qmax && r < n && id >= 0;
-            const Raw* row = table + static_cast<int64_t>(ok ? id : 0) * nvec;
+            for (int q = 0; q < UNROLL; ++q) {
+              const int r = j + q * rps + slot;
+              const int32_t id = __shfl_sync(FULL, my_id, r);
+              w[q] = PSW ? __shfl_sync(FULL, my_w, r) : 1.0f;
+              const Raw* row = table + static_cast<int64_t>(id) * nvec;
 #pragma unroll
-            for (int m = 0; m < MAXV; ++m) {
-              const int vv = vi + m * kWarp;
-              if (ok && vv < nvec) v[q][m] = ldg_raw(row + m * kWarp);
-              else v[q][m] = Raw{};
+              for (int m = 0; m < MAXV; ++m) v[q][m] = ldg_raw(row + vk[m]);
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < UNROLL; ++q) {
+              const int r = j + q * rps + slot;  // < 64; lanes past n hold -1
+              const int32_t id = __shfl_sync(FULL, my_id, r & (kWarp - 1));
+              w[q] = PSW ? __shfl_sync(FULL, my_w, r & (kWarp - 1)) : 1.0f;
+              const bool ok = q < qmax && r < n && id >= 0;
+              const Raw* row = table + static_cast<int64_t>(ok ? id : 0) * nvec;
+#pragma unroll
+              for (int m = 0; m < MAXV; ++m) {
+                if (ok && vi + m * kWarp < nvec) v[q][m] = ldg_raw(row + vk[m]);
+                else v[q][m] = Raw{};
+              }
             }
           }
 #pragma unroll
