@@ -60,10 +60,12 @@ def _bind(lib):
     lib.oracle_version.restype = ctypes.c_int
     lib.oracle_bounds_repair.argtypes = [c_i32, c_i64, c_i64, vp, c_i32, vp, vp, vp, vp]
     lib.oracle_bounds_repair.restype = ctypes.c_int
-    lib.oracle_forward.argtypes = [c_i32, c_i64, vp, vp, c_i32, vp, c_i32, vp, vp, vp, vp, vp, vp]
+    lib.oracle_forward.argtypes = [c_i32, c_i64, vp, vp, c_i32, vp, c_i32, vp, vp, vp, c_i32, vp, vp, vp]
     lib.oracle_forward.restype = ctypes.c_int
     lib.oracle_backward.argtypes = [c_i32, c_i64, vp, vp, c_i32, vp, vp, c_i32, vp, vp, vp, vp,
-                                    c_i32, c_f32, c_f32, vp]
+                                    c_i32, c_i32, c_f32, c_f32, vp]
+    lib.oracle_psw_gradient.argtypes = [c_i32, c_i64, vp, vp, c_i32, vp, c_i32, vp, vp, vp, c_i32, vp]
+    lib.oracle_psw_gradient.restype = ctypes.c_int
     lib.oracle_backward.restype = vp
     for name in ("oracle_result_num_lookups", "oracle_result_num_runs", "oracle_result_num_elems"):
         getattr(lib, name).argtypes = [vp]
@@ -104,6 +106,9 @@ def _itype(indices, offsets):
     if indices.dtype != offsets.dtype or indices.dtype not in (np.int32, np.int64):
         raise TypeError("indices and offsets must share one dtype, int32 or int64")
     return 0 if indices.dtype == np.int32 else 1
+
+
+_POOL = {"sum": 0, "mean": 1}
 
 
 def _wdtype(weights, wdtype):
@@ -156,7 +161,7 @@ class Oracle:
         return per_table, int(n_off[0])
 
     def forward(self, tables: Tables, B: int, weights: np.ndarray, indices: np.ndarray, offsets: np.ndarray,
-                psw: np.ndarray | None = None, wdtype: str | None = None):
+                psw: np.ndarray | None = None, wdtype: str | None = None, pooling: str = "sum"):
         """Returns (out fp32, out_exact fp64, out_absterms fp64), each [B, sum(D)]."""
         lib = self.lib
         wd = _wdtype(weights, wdtype)
@@ -168,15 +173,30 @@ class Oracle:
         psw_c = None if psw is None else _c(psw, np.float32)
         rc = lib.oracle_forward(tables.T, B, _ptr(tables.D), _ptr(tables.E), wd, _ptr(_c(weights, weights.dtype)),
                                 it, _ptr(_c(indices, indices.dtype)), _ptr(_c(offsets, offsets.dtype)),
-                                _ptr(psw_c), _ptr(out), _ptr(exact), _ptr(absterms))
+                                _ptr(psw_c), _POOL[pooling], _ptr(out), _ptr(exact), _ptr(absterms))
         if rc != 0:
             raise RuntimeError(f"oracle_forward failed: {rc}")
         return out, exact, absterms
 
+    def psw_gradient(self, tables: Tables, B: int, weights: np.ndarray, indices: np.ndarray, offsets: np.ndarray,
+                     grad_out: np.ndarray, wdtype: str | None = None, pooling: str = "sum") -> np.ndarray:
+        """fp64 gradient with respect to the per-sample weights, one value per index position
+        (positions outside every bag stay NaN)."""
+        lib = self.lib
+        wd = _wdtype(weights, wdtype)
+        it = _itype(indices, offsets)
+        g = np.full(len(indices), np.nan, dtype=np.float64)
+        rc = lib.oracle_psw_gradient(tables.T, B, _ptr(tables.D), _ptr(tables.E), wd, _ptr(_c(weights, weights.dtype)),
+                                     it, _ptr(_c(indices, indices.dtype)), _ptr(_c(offsets, offsets.dtype)),
+                                     _ptr(_c(grad_out, np.float32)), _POOL[pooling], _ptr(g))
+        if rc != 0:
+            raise RuntimeError(f"oracle_psw_gradient failed: {rc}")
+        return g
+
     def backward(self, tables: Tables, B: int, weights: np.ndarray, state: np.ndarray | None,
                  indices: np.ndarray, offsets: np.ndarray, grad_out: np.ndarray,
                  psw: np.ndarray | None = None, optimizer: str = "adagrad", lr: float = 0.01,
-                 eps: float = 1e-8, wdtype: str | None = None) -> dict:
+                 eps: float = 1e-8, wdtype: str | None = None, pooling: str = "sum") -> dict:
         """Updates weights (and state, for Adagrad) in place; returns the run metadata and
         the exact per-run values as a dict of numpy arrays."""
         lib = self.lib
@@ -191,7 +211,7 @@ class Oracle:
         status = ctypes.c_int32(0)
         h = lib.oracle_backward(tables.T, B, _ptr(tables.D), _ptr(tables.E), wd, _ptr(weights),
                                 _ptr(state), it, _ptr(_c(indices, indices.dtype)),
-                                _ptr(_c(offsets, offsets.dtype)), _ptr(psw_c), _ptr(grad_c), opt,
+                                _ptr(_c(offsets, offsets.dtype)), _ptr(psw_c), _ptr(grad_c), _POOL[pooling], opt,
                                 ctypes.c_float(lr), ctypes.c_float(eps), ctypes.byref(status))
         if not h:
             raise RuntimeError(f"oracle_backward failed: {status.value}")
@@ -264,6 +284,10 @@ def bounds_repair(*a, **k):
 
 def forward(*a, **k):
     return default().forward(*a, **k)
+
+
+def psw_gradient(*a, **k):
+    return default().psw_gradient(*a, **k)
 
 
 def backward(*a, **k):

@@ -231,13 +231,15 @@ int oracle_bounds_repair(int32_t T, int64_t B, int64_t num_indices, const int64_
 
 /* Forward, [FBT] section 2: for each table and bag, gather the indexed rows, optionally
  * multiply by the per-sample weight, sum, and write one D-wide pooled output; the output row
- * of sample b is [pool_t0(b) | pool_t1(b) | ...] ([TUT] section 1).  An empty bag sums to 0. */
+ * of sample b is [pool_t0(b) | pool_t1(b) | ...] ([TUT] section 1).  An empty bag sums to 0.
+ * Mean pooling ([TUT], "Try this": divide by the bag length): the sum divided by the bag's
+ * number of lookups; an empty bag gives 0, as embedding_bag(mode="mean") does. */
 int oracle_forward(int32_t T, int64_t B, const int32_t* D, const int64_t* E, int32_t wdtype,
                    const void* weights, int32_t itype, const void* indices, const void* offsets,
-                   const float* psw, float* out, double* out_exact, double* out_absterms) {
+                   const float* psw, int32_t pooling, float* out, double* out_exact, double* out_absterms) {
   Layout L;
   if (!make_layout(T, D, E, &L) || B < 0 || offsets == nullptr || weights == nullptr) return -1;
-  if (wdtype < 0 || wdtype > 2 || (itype != 0 && itype != 1)) return -2;
+  if (wdtype < 0 || wdtype > 2 || (itype != 0 && itype != 1) || pooling < 0 || pooling > 1) return -2;
   if (!inputs_valid(T, B, E, itype, indices, offsets)) return -3;
   const int64_t width = L.col_begin[T];
   for (int64_t b = 0; b < B; ++b) {
@@ -253,6 +255,12 @@ int oracle_forward(int32_t T, int64_t B, const int32_t* D, const int64_t* E, int
           const double term = scale * load_weight(weights, wdtype, base + d);
           acc[d] += term;
           absacc[d] += std::fabs(term);
+        }
+      }
+      if (pooling == 1 && e > s) {
+        for (int32_t d = 0; d < D[t]; ++d) {
+          acc[d] /= static_cast<double>(e - s);
+          absacc[d] /= static_cast<double>(e - s);
         }
       }
       for (int32_t d = 0; d < D[t]; ++d) {
@@ -277,7 +285,7 @@ int oracle_forward(int32_t T, int64_t B, const int32_t* D, const int64_t* E, int
  * squared gradient over the row, then w -= lr * g / (sqrt(state) + eps). */
 void* oracle_backward(int32_t T, int64_t B, const int32_t* D, const int64_t* E, int32_t wdtype,
                       void* weights, float* state, int32_t itype, const void* indices,
-                      const void* offsets, const float* psw, const float* grad_out,
+                      const void* offsets, const float* psw, const float* grad_out, int32_t pooling,
                       int32_t optimizer, float lr, float eps, int32_t* status) {
   int32_t dummy;
   if (!status) status = &dummy;
@@ -287,7 +295,8 @@ void* oracle_backward(int32_t T, int64_t B, const int32_t* D, const int64_t* E, 
     *status = -1;
     return nullptr;
   }
-  if (wdtype < 0 || wdtype > 2 || (itype != 0 && itype != 1) || optimizer < 0 || optimizer > 1) {
+  if (wdtype < 0 || wdtype > 2 || (itype != 0 && itype != 1) || optimizer < 0 || optimizer > 1 ||
+      pooling < 0 || pooling > 1) {
     *status = -2;
     return nullptr;
   }
@@ -308,11 +317,14 @@ void* oracle_backward(int32_t T, int64_t B, const int32_t* D, const int64_t* E, 
         const int64_t key = L.row_begin[t] + load_int(indices, itype, p);
         RowEntry& r = rows[key];
         if (r.g.empty()) r.g.assign(D[t], 0.0);
-        const float w = psw ? psw[p] : 1.0f;
+        // the lookup's factor: its per-sample weight, divided by the bag length when pooling by
+        // mean (the derivative of the mean is the derivative of the sum over L)
+        double factor = psw ? static_cast<double>(psw[p]) : 1.0;
+        if (pooling == 1) factor /= static_cast<double>(e - s);
         for (int32_t d = 0; d < D[t]; ++d)
-          r.g[d] += static_cast<double>(w) * static_cast<double>(grad_out[b * width + L.col_begin[t] + d]);
+          r.g[d] += factor * static_cast<double>(grad_out[b * width + L.col_begin[t] + d]);
         r.bags.push_back(b);
-        r.psw.push_back(w);
+        r.psw.push_back(static_cast<float>(factor));
         ++N;
       }
     }
@@ -401,6 +413,37 @@ void oracle_result_copy(const void* h, int64_t* sorted_keys, int64_t* sorted_bag
 }
 
 void oracle_result_free(void* h) { delete static_cast<Result*>(h); }
+
+/* Gradient of the pooled output with respect to the per-sample weights: for lookup p of bag
+ * (t, b), d out[b, cols of t] / d psw[p] = W_t[idx[p]] (divided by the bag length when pooling
+ * by mean), so grad_psw[p] = sum_d grad_out[b, col_t + d] * W_t[idx[p], d] (/ L).  Computed in
+ * fp64 from the weights as they are (before any update).  Positions outside every bag are
+ * left untouched. */
+int oracle_psw_gradient(int32_t T, int64_t B, const int32_t* D, const int64_t* E, int32_t wdtype,
+                        const void* weights, int32_t itype, const void* indices, const void* offsets,
+                        const float* grad_out, int32_t pooling, double* grad_psw) {
+  Layout L;
+  if (!make_layout(T, D, E, &L) || B < 0 || offsets == nullptr || weights == nullptr ||
+      grad_out == nullptr || grad_psw == nullptr)
+    return -1;
+  if (wdtype < 0 || wdtype > 2 || (itype != 0 && itype != 1) || pooling < 0 || pooling > 1) return -2;
+  if (!inputs_valid(T, B, E, itype, indices, offsets)) return -3;
+  const int64_t width = L.col_begin[T];
+  for (int32_t t = 0; t < T; ++t) {
+    for (int64_t b = 0; b < B; ++b) {
+      const int64_t s = load_int(offsets, itype, t * B + b);
+      const int64_t e = load_int(offsets, itype, t * B + b + 1);
+      for (int64_t p = s; p < e; ++p) {
+        const int64_t base = L.elem_begin[t] + load_int(indices, itype, p) * D[t];
+        double dot = 0.0;
+        for (int32_t d = 0; d < D[t]; ++d)
+          dot += static_cast<double>(grad_out[b * width + L.col_begin[t] + d]) * load_weight(weights, wdtype, base + d);
+        grad_psw[p] = pooling == 1 ? dot / static_cast<double>(e - s) : dot;
+      }
+    }
+  }
+  return 0;
+}
 
 int oracle_classify(int32_t T, const int32_t* D, const int64_t* E, int64_t U,
                     const int64_t* unique_keys, const int64_t* run_lengths, int64_t threshold,

@@ -47,15 +47,18 @@ int oracle_bounds_repair(int32_t T, int64_t B, int64_t num_indices, const int64_
                          void* indices, void* offsets, int64_t* repaired_per_table,
                          int64_t* repaired_offsets);
 
-/* Pooled forward.  out (nullable) receives the fp32 result (round-to-nearest-even of the
- * exact value), out_exact (nullable) the fp64 accumulation, out_absterms (nullable) the sum
- * of |psw * w| over the bag for each element (its condition scale).  All are B x sum(D). */
+/* Pooled forward.  pooling: 0 = sum, 1 = mean (the sum over the bag length; an empty bag
+ * gives 0).  out (nullable) receives the fp32 result (round-to-nearest-even of the exact
+ * value), out_exact (nullable) the fp64 value, out_absterms (nullable) the sum of |psw * w|
+ * over the bag for each element (its condition scale; divided by L for mean).  All are
+ * B x sum(D). */
 int oracle_forward(int32_t T, int64_t B, const int32_t* D, const int64_t* E, int32_t wdtype,
                    const void* weights, int32_t itype, const void* indices, const void* offsets,
-                   const float* psw, float* out, double* out_exact, double* out_absterms);
+                   const float* psw, int32_t pooling, float* out, double* out_exact, double* out_absterms);
 
 /* Backward + optimizer.  Groups the lookups by key with a std::map, sums the upstream
- * gradient rows of each key in fp64, and applies exactly one optimizer update per key:
+ * gradient rows of each key in fp64 (each scaled by its lookup's factor: psw, or 1, divided
+ * by the bag length when pooling = 1 (mean)), and applies exactly one optimizer update per key:
  *   optimizer 0 (SGD):                w -= lr * g
  *   optimizer 1 (row-wise Adagrad):   s += mean_d(g_d^2);  w -= lr * g / (sqrt(s) + eps)
  * weights (wdtype) and state (fp32, one per linear row; may be NULL for SGD) are updated in
@@ -63,7 +66,7 @@ int oracle_forward(int32_t T, int64_t B, const int32_t* D, const int64_t* E, int
  * *status set) from which run metadata and exact values are read. */
 void* oracle_backward(int32_t T, int64_t B, const int32_t* D, const int64_t* E, int32_t wdtype,
                       void* weights, float* state, int32_t itype, const void* indices,
-                      const void* offsets, const float* psw, const float* grad_out,
+                      const void* offsets, const float* psw, const float* grad_out, int32_t pooling,
                       int32_t optimizer, float lr, float eps, int32_t* status);
 
 int64_t oracle_result_num_lookups(const void* h);  /* N = offsets[T*B] */
@@ -73,7 +76,8 @@ int64_t oracle_result_num_elems(const void* h);    /* sum over runs of D of the 
 /* Copies the result out; any pointer may be NULL.
  *   sorted_keys[N]     keys in ascending order, each repeated run-length times
  *   sorted_bags[N]     bag b of each sorted lookup; inside a run, ascending lookup position
- *   sorted_psw[N]      per-sample weight of each sorted lookup (1 when unweighted)
+ *   sorted_psw[N]      factor of each sorted lookup: its per-sample weight (1 when unweighted),
+ *                      divided by the bag length for mean pooling, rounded to fp32
  *   unique_keys[U], run_lengths[U], run_offsets[U+1] (exclusive prefix sum, last = N)
  *   run_elem_offsets[U+1]  where run r's D values start in the three arrays below
  *   grad_sum[E]        fp64 gradient sum of each run's row
@@ -85,6 +89,13 @@ void oracle_result_copy(const void* h, int64_t* sorted_keys, int64_t* sorted_bag
                         double* w_exact, double* state_exact);
 
 void oracle_result_free(void* h);
+
+/* Gradient with respect to the per-sample weights (fp64): grad_psw[p] = sum_d
+ * grad_out[b, col_t + d] * W_t[idx[p], d], divided by the bag length when pooling = 1.
+ * Positions outside every bag are not written. */
+int oracle_psw_gradient(int32_t T, int64_t B, const int32_t* D, const int64_t* E, int32_t wdtype,
+                        const void* weights, int32_t itype, const void* indices, const void* offsets,
+                        const float* grad_out, int32_t pooling, double* grad_psw);
 
 /* Run routing ("Modernizing Table Batched Embeddings with FBTriton", section 3 and
  * section 4, Problems 1 and 3): a run is long when its length is at or above `threshold`

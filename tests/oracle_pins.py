@@ -94,8 +94,9 @@ def _table_weight_view(P, t, w64):
     return w64[eb[t]:eb[t + 1]].reshape(int(P["E"][t]), int(P["D"][t]))
 
 
-def embedding_bag_reference(P, w64: np.ndarray) -> np.ndarray:
-    """Per-table torch embedding_bag (sum) in fp64, concatenated along columns."""
+def embedding_bag_reference(P, w64: np.ndarray, mode: str = "sum") -> np.ndarray:
+    """Per-table torch embedding_bag (sum, or mean for unweighted problems) in fp64,
+    concatenated along columns."""
     B, T = P["B"], P["tables"].T
     offs = P["offsets"].astype(np.int64)
     idx = torch.from_numpy(P["indices"].astype(np.int64))
@@ -105,8 +106,51 @@ def embedding_bag_reference(P, w64: np.ndarray) -> np.ndarray:
         tab = torch.from_numpy(_table_weight_view(P, t, w64))
         psw = None if P["psw"] is None else torch.from_numpy(P["psw"][o[0]:o[-1]].astype(np.float64))
         outs.append(torch.nn.functional.embedding_bag(
-            idx[o[0]:o[-1]], tab, torch.from_numpy(o[:-1] - o[0]), mode="sum", per_sample_weights=psw))
+            idx[o[0]:o[-1]], tab, torch.from_numpy(o[:-1] - o[0]), mode=mode, per_sample_weights=psw))
     return torch.cat(outs, dim=1).numpy()
+
+
+def bag_lengths_per_output(P) -> np.ndarray:
+    """[B, sum D]: the length of the bag each output element pools."""
+    B, D = P["B"], P["D"]
+    L = np.diff(P["offsets"].astype(np.int64)).reshape(len(D), B)
+    return np.concatenate([np.repeat(L[t][:, None], D[t], axis=1) for t in range(len(D))], axis=1)
+
+
+def autograd_psw_grad(P, w64: np.ndarray) -> np.ndarray:
+    """d(sum(out * grad_out))/d psw through torch autograd of embedding_bag(mode="sum") in fp64."""
+    B, T = P["B"], P["tables"].T
+    offs = P["offsets"].astype(np.int64)
+    idx = torch.from_numpy(P["indices"].astype(np.int64))
+    cb = _col_begin(P["D"])
+    out_g = np.full(len(P["indices"]), np.nan)
+    for t in range(T):
+        o = offs[t * B:(t + 1) * B + 1]
+        tab = torch.from_numpy(_table_weight_view(P, t, w64).copy())
+        psw = torch.from_numpy(P["psw"][o[0]:o[-1]].astype(np.float64)).requires_grad_(True)
+        out = torch.nn.functional.embedding_bag(
+            idx[o[0]:o[-1]], tab, torch.from_numpy(o[:-1] - o[0]), mode="sum", per_sample_weights=psw)
+        out.backward(torch.from_numpy(P["grad"][:, cb[t]:cb[t + 1]].astype(np.float64)))
+        out_g[o[0]:o[-1]] = psw.grad.numpy()
+    return out_g
+
+
+def autograd_weight_grad_mean(P, w64: np.ndarray) -> np.ndarray:
+    """As autograd_weight_grad, through embedding_bag(mode="mean") (unweighted)."""
+    B, T = P["B"], P["tables"].T
+    offs = P["offsets"].astype(np.int64)
+    idx = torch.from_numpy(P["indices"].astype(np.int64))
+    eb = _elem_begin(P["D"], P["E"])
+    grads = np.zeros_like(w64)
+    cb = _col_begin(P["D"])
+    for t in range(T):
+        o = offs[t * B:(t + 1) * B + 1]
+        tab = torch.from_numpy(_table_weight_view(P, t, w64).copy()).requires_grad_(True)
+        out = torch.nn.functional.embedding_bag(
+            idx[o[0]:o[-1]], tab, torch.from_numpy(o[:-1] - o[0]), mode="mean")
+        out.backward(torch.from_numpy(P["grad"][:, cb[t]:cb[t + 1]].astype(np.float64)))
+        grads[eb[t]:eb[t + 1]] = tab.grad.numpy().reshape(-1)
+    return grads
 
 
 def autograd_weight_grad(P, w64: np.ndarray) -> np.ndarray:
@@ -218,6 +262,72 @@ def check_forward_embedding_bag(orc):
                     Q = dict(P)
                     ref_abs = embedding_bag_reference(Q, np.abs(w64))
                     assert np.allclose(absterms, ref_abs, rtol=1e-12, atol=0)
+
+
+def check_forward_mean(orc):
+    """Mean pooling ([TUT], "Try this"): embedding_bag(mode="mean") for unweighted bags (an
+    empty bag gives 0 there too); for weighted bags the closed form sum(psw * w) / L, with the
+    sum from embedding_bag(mode="sum", per_sample_weights)."""
+    rng = np.random.default_rng(21)
+    for wdtype in ("f32", "f16", "bf16"):
+        for weighted in (False, True):
+            P = random_problem(rng, wdtype, weighted=weighted)
+            w64 = weights_as_f64(P["weights"], wdtype)
+            _, exact, absterms = orc.forward(P["tables"], P["B"], P["weights"], P["indices"], P["offsets"],
+                                             psw=P["psw"], wdtype=wdtype, pooling="mean")
+            if weighted:
+                L = bag_lengths_per_output(P)
+                ref = embedding_bag_reference(P, w64) / np.maximum(L, 1)
+            else:
+                ref = embedding_bag_reference(P, w64, mode="mean")
+            assert np.all(np.abs(exact - ref) <= 1e-12 * np.maximum(absterms, 1e-300)), \
+                f"mean forward ({wdtype}, weighted={weighted})"
+
+
+def check_backward_mean_sgd_autograd(orc):
+    """SGD with mean pooling equals W - lr * autograd of embedding_bag(mode="mean"); the
+    recorded per-lookup factor is 1 / L."""
+    rng = np.random.default_rng(22)
+    for wdtype in ("f32", "bf16"):
+        P = random_problem(rng, wdtype)
+        w64 = weights_as_f64(P["weights"], wdtype)
+        w = P["weights"].copy()
+        lr = 0.125
+        res = orc.backward(P["tables"], P["B"], w, None, P["indices"], P["offsets"], P["grad"],
+                           optimizer="sgd", lr=lr, wdtype=wdtype, pooling="mean")
+        gW = autograd_weight_grad_mean(P, w64)
+        expected = w64 - lr * gW
+        eb = _elem_begin(P["D"], P["E"])
+        rb = np.concatenate([[0], np.cumsum(P["E"])])
+        for r, key in enumerate(res["unique_keys"]):
+            t = int(np.searchsorted(rb, key, side="right") - 1)
+            base = eb[t] + (key - rb[t]) * P["D"][t]
+            got = res["w_exact"][res["run_elem_offsets"][r]:res["run_elem_offsets"][r + 1]]
+            want = expected[base:base + P["D"][t]]
+            assert np.all(np.abs(got - want) <= 1e-12 * (np.abs(want) + lr * np.abs(gW[base:base + P["D"][t]]) + 1e-300)), \
+                f"mean SGD vs autograd ({wdtype})"
+        # factor of each sorted lookup = 1 / (length of its bag)
+        L = np.diff(P["offsets"].astype(np.int64))
+        tab_of = np.searchsorted(rb, res["sorted_keys"], side="right") - 1
+        want_f = (1.0 / L[tab_of * P["B"] + res["sorted_bags"]]).astype(np.float32)
+        assert np.array_equal(res["sorted_psw"], want_f), "mean factor 1/L"
+
+
+def check_psw_gradient_autograd(orc):
+    """Gradient with respect to the per-sample weights: torch autograd of
+    embedding_bag(mode="sum", per_sample_weights) in fp64; for mean pooling the same over L."""
+    rng = np.random.default_rng(23)
+    for wdtype in ("f32", "f16", "bf16"):
+        P = random_problem(rng, wdtype, weighted=True)
+        w64 = weights_as_f64(P["weights"], wdtype)
+        g = orc.psw_gradient(P["tables"], P["B"], P["weights"], P["indices"], P["offsets"], P["grad"],
+                             wdtype=wdtype)
+        ref = autograd_psw_grad(P, w64)
+        assert np.all(np.abs(g - ref) <= 1e-12 * (np.abs(ref) + 1e-9)), f"psw gradient ({wdtype})"
+        gm = orc.psw_gradient(P["tables"], P["B"], P["weights"], P["indices"], P["offsets"], P["grad"],
+                              wdtype=wdtype, pooling="mean")
+        Ls = np.concatenate([np.full(int(n), float(n)) for n in np.diff(P["offsets"].astype(np.int64))])
+        assert np.all(np.abs(gm - ref / Ls) <= 1e-12 * (np.abs(ref) + 1e-9)), f"mean psw gradient ({wdtype})"
 
 
 def check_forward_special_cases(orc):
@@ -460,6 +570,9 @@ ALL_CHECKS = [
     check_bf16_conversions,
     check_forward_embedding_bag,
     check_forward_special_cases,
+    check_forward_mean,
+    check_backward_mean_sgd_autograd,
+    check_psw_gradient_autograd,
     check_backward_sgd_autograd,
     check_backward_metadata_library,
     check_grad_sum_scatter,

@@ -26,9 +26,10 @@ MUTANTS = [
     ("sgd_sign", "w_new = w_old - static_cast<double>(lr) * r.g[d];", "w_new = w_old + static_cast<double>(lr) * r.g[d];"),
     # per-sample weights dropped in forward / backward
     ("forward_drops_psw", "const double scale = psw ? static_cast<double>(psw[p]) : 1.0;", "const double scale = 1.0;"),
-    ("backward_drops_psw", "const float w = psw ? psw[p] : 1.0f;", "const float w = 1.0f;"),
+    ("backward_drops_psw", "double factor = psw ? static_cast<double>(psw[p]) : 1.0;", "double factor = 1.0;"),
     # wrong gradient column (table block offset dropped) / wrong weight row base
-    ("backward_grad_column", "grad_out[b * width + L.col_begin[t] + d]", "grad_out[b * width + d]"),
+    ("backward_grad_column", "factor * static_cast<double>(grad_out[b * width + L.col_begin[t] + d])",
+     "factor * static_cast<double>(grad_out[b * width + d])"),
     ("forward_row_base", "const int64_t base = L.elem_begin[t] + row * D[t];\n        for (int32_t d = 0; d < D[t]; ++d) {\n          const double term",
      "const int64_t base = row * D[t];\n        for (int32_t d = 0; d < D[t]; ++d) {\n          const double term"),
     ("forward_output_column", "const int64_t o = b * width + L.col_begin[t] + d;", "const int64_t o = b * width + d;"),
@@ -49,6 +50,13 @@ MUTANTS = [
      "double q = std::floor(std::ldexp(a, frac_bits - e));"),
     ("bf16_decoder_bits", "double bf16_to_double(uint16_t h) { return decode_small_float(h, 8, 7); }",
      "double bf16_to_double(uint16_t h) { return decode_small_float(h, 7, 8); }"),
+    # mean pooling: divided by L + 1; backward factor without 1/L; psw gradient column / mean
+    ("mean_forward_len_plus_one", "          acc[d] /= static_cast<double>(e - s);\n          absacc",
+     "          acc[d] /= static_cast<double>(e - s + 1);\n          absacc"),
+    ("mean_backward_unscaled", "if (pooling == 1) factor /= static_cast<double>(e - s);", "if (pooling == 1) factor /= 1.0;"),
+    ("psw_grad_column", "static_cast<double>(grad_out[b * width + L.col_begin[t] + d]) * load_weight",
+     "static_cast<double>(grad_out[b * width + d]) * load_weight"),
+    ("psw_grad_mean_unscaled", "grad_psw[p] = pooling == 1 ? dot / static_cast<double>(e - s) : dot;", "grad_psw[p] = dot;"),
     # the forward's empty-bag/loop bound: last lookup of each bag dropped
     ("forward_drops_last_lookup",
      "for (int64_t p = s; p < e; ++p) {\n        const int64_t row = load_int(indices, itype, p);",
