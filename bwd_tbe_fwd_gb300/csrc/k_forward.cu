@@ -41,6 +41,7 @@ struct FwdArgs {
   int64_t num_indices;
   int64_t unit_begin, unit_end;
   int bags_per_item;  // 1..32
+  int mean;           // mean pooling: the sum over the bag length (an empty bag stays 0)
   int total_D;
   int fused_bounds;
   unsigned long long* stats;
@@ -269,6 +270,12 @@ fwd_gather_kernel(FwdArgs a) {
 #pragma unroll
           for (int i = 0; i < NE; ++i) acc[x][i] += __shfl_xor_sync(FULL, acc[x][i], m);
       }
+      if (a.mean && e > s) {
+#pragma unroll
+        for (int x = 0; x < MAXV; ++x)
+#pragma unroll
+          for (int i = 0; i < NE; ++i) acc[x][i] /= static_cast<Acc>(e - s);
+      }
       if (slot == 0) {
 #pragma unroll
         for (int x = 0; x < MAXV; ++x) {
@@ -360,6 +367,7 @@ cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const
   a.unit_end = unit_end;
   a.total_D = P.total_D;
   a.fused_bounds = fused_bounds ? 1 : 0;
+  a.mean = P.pooling == TBE_POOL_MEAN;
   a.stats = stats;
   const int vb = P.vec_bytes;
   const int ne = vb / P.wbytes;

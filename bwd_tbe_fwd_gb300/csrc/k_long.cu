@@ -345,11 +345,11 @@ cudaError_t launch_long_updates(const Problem& P, const BwdCtx& c, const BwdLayo
                                 const DeviceInfo& dev, cudaStream_t s) {
   if (c.long_cap == 0) return cudaSuccess;
   const uint32_t* vals = c.vals[L.final_buf];
-  const float* psw = P.weighted ? c.pswbuf[L.final_buf] : nullptr;
+  const float* psw = P.scaled ? c.pswbuf[L.final_buf] : nullptr;
   const int maxv = maxv_for(P.max_D);
   return by_weight_type(P.wdtype, [&](auto w) -> cudaError_t {
     using WT = decltype(w);
-    if (P.weighted) {
+    if (P.scaled) {
       return opt == TBE_OPT_SGD
                  ? launch_long_maxv<WT, true, TBE_OPT_SGD>(c, vals, psw, fused, scheduler, merge, maxv, dev, s)
                  : launch_long_maxv<WT, true, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, scheduler, merge, maxv,

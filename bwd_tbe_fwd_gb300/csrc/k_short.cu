@@ -173,13 +173,13 @@ cudaError_t launch_short_updates(const Problem& P, const BwdCtx& c, const BwdLay
                                  tbe_optimizer opt, int scheduler, const DeviceInfo& dev,
                                  cudaStream_t s) {
   const uint32_t* vals = c.vals[L.final_buf];
-  const float* psw = P.weighted ? c.pswbuf[L.final_buf] : nullptr;
+  const float* psw = P.scaled ? c.pswbuf[L.final_buf] : nullptr;
   const bool persist = scheduler == TBE_SCHED_PERSISTENT;
   for (int k = 2; k < kNumBuckets; ++k) {
     if (c.short_cap[k] == 0) continue;
     cudaError_t e = by_weight_type(P.wdtype, [&](auto w) -> cudaError_t {
       using WT = decltype(w);
-      if (P.weighted) {
+      if (P.scaled) {
         return opt == TBE_OPT_SGD ? launch_short_bucket<WT, true, TBE_OPT_SGD>(c, k, vals, psw, persist, dev, s)
                                   : launch_short_bucket<WT, true, TBE_OPT_ROWWISE_ADAGRAD>(c, k, vals, psw, persist, dev, s);
       }

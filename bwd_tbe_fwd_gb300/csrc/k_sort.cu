@@ -49,6 +49,7 @@ struct ExpandArgs {
   float* psw_out;
   uint32_t* counters;
   unsigned long long* stats;
+  int mean;                    // mean pooling: the factor is psw / L (1 / L unweighted)
   int nhist;                   // tables whose lookups stay out of the sort
   int hist_t[kMaxHistTables];  // ascending
 };
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
     for (int u = 0; u < U; ++u) {
       const int64_t p = pb + u * blockDim.x + threadIdx.x;
       id[u] = p < p1 ? ld_int<IT>(a.indices, p) : 0;
-      if (PSW) w[u] = p < p1 ? __ldg(a.psw + p) : 0.f;
+      if (PSW) w[u] = p < p1 ? (a.psw != nullptr ? __ldg(a.psw + p) : 1.f) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -130,7 +131,8 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
       }
       a.keys[q] = key;
       a.vals[q] = b;
-      if (PSW) a.psw_out[q] = w[u];
+      // the lookup's factor: psw, over the bag length for mean pooling (correctly rounded)
+      if (PSW) a.psw_out[q] = a.mean ? __fdiv_rn(w[u], static_cast<float>(s_off[lo + 1] - s_off[lo])) : w[u];
     }
   }
   if (bad) atomicAdd(&s_bad, bad);
@@ -495,6 +497,7 @@ cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s) {
   a.psw_out = c.pswbuf[0];
   a.counters = c.counters;
   a.stats = c.stats;
+  a.mean = P.pooling == TBE_POOL_MEAN;
   a.nhist = c.nhist;
   for (int h = 0; h < kMaxHistTables; ++h) a.hist_t[h] = h < c.nhist ? c.hist_t[h] : 0;
   // about 16K lookups per CTA: bags per CTA from the mean bag length the host can see
@@ -504,7 +507,7 @@ cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s) {
   a.bags_per_cta = bpc;
   const int64_t grid64 = (c.TB + bpc - 1) / bpc;
   const int grid = static_cast<int>(grid64 < 1 ? 1 : grid64);
-  const bool psw = P.weighted;
+  const bool psw = P.scaled;
   if (P.itype == TBE_I32) {
     if (psw) expand_kernel<int32_t, true><<<grid, kThreads, 0, s>>>(a);
     else expand_kernel<int32_t, false><<<grid, kThreads, 0, s>>>(a);
@@ -518,7 +521,7 @@ cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s) {
 
 template <int RB>
 cudaError_t launch_sort_rb(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s) {
-  const bool psw = P.weighted;
+  const bool psw = P.scaled;
   const size_t smem = downsweep_smem_bytes(RB, psw);
   // the opt-in shared memory size is a per-device function attribute: set it once per device
   static std::atomic<uint64_t> attr_set[2] = {{0}, {0}};

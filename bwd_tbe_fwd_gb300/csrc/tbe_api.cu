@@ -73,6 +73,7 @@ tbe_status make_problem(const tbe_problem* p, Problem* out) {
   if (p->T > kMaxTables) return TBE_ERR_UNSUPPORTED;
   if (p->wdtype != TBE_F32 && p->wdtype != TBE_F16 && p->wdtype != TBE_BF16) return TBE_ERR_UNSUPPORTED;
   if (p->itype != TBE_I32 && p->itype != TBE_I64) return TBE_ERR_UNSUPPORTED;
+  if (p->pooling != TBE_POOL_SUM && p->pooling != TBE_POOL_MEAN) return TBE_ERR_INVALID_ARG;
   Problem& P = *out;
   P = Problem();
   P.T = p->T;
@@ -82,6 +83,8 @@ tbe_status make_problem(const tbe_problem* p, Problem* out) {
   P.wdtype = p->wdtype;
   P.itype = p->itype;
   P.weighted = p->weighted != 0;
+  P.pooling = p->pooling;
+  P.scaled = P.weighted || P.pooling == TBE_POOL_MEAN;
   P.wbytes = p->wdtype == TBE_F32 ? 4 : 2;
   P.D.assign(p->D, p->D + p->T);
   P.E.assign(p->E, p->E + p->T);
@@ -130,7 +133,8 @@ tbe_status device_info(DeviceInfo* out) {
 }
 
 bool hist_forward_eligible(const Problem& P, const tbe_options& o, int t) {
-  return o.histogram && histogram_supported() && P.wdtype == TBE_F16 && !P.weighted && P.E[t] <= 64 &&
+  return o.histogram && histogram_supported() && P.wdtype == TBE_F16 && !P.weighted &&
+         P.pooling == TBE_POOL_SUM && P.E[t] <= 64 &&
          P.D[t] >= 64 && P.D[t] <= 128 && P.long_bags[t] != 0;
 }
 
@@ -183,7 +187,7 @@ BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const Device
   for (int b = 0; b < 2; ++b) {
     L.keys[b] = take(sizeof(uint32_t) * n_cap);
     L.vals[b] = take(sizeof(uint32_t) * n_cap);
-    L.psw[b] = P.weighted ? take(sizeof(float) * n_cap) : 0;
+    L.psw[b] = P.scaled ? take(sizeof(float) * n_cap) : 0;
   }
   L.sort_counts = take(sizeof(uint32_t) * (size_t(1) << L.radix_bits) * L.sort_grid);
   L.sort_totals = take(sizeof(uint32_t) * (size_t(1) << L.radix_bits));
@@ -235,7 +239,7 @@ BwdCtx make_ctx(const Problem& P, const tbe_options& o, const BwdLayout& L, cons
   for (int b = 0; b < 2; ++b) {
     c.keys[b] = reinterpret_cast<uint32_t*>(base + L.keys[b]);
     c.vals[b] = reinterpret_cast<uint32_t*>(base + L.vals[b]);
-    c.pswbuf[b] = P.weighted ? reinterpret_cast<float*>(base + L.psw[b]) : nullptr;
+    c.pswbuf[b] = P.scaled ? reinterpret_cast<float*>(base + L.psw[b]) : nullptr;
   }
   c.sort_counts = reinterpret_cast<uint32_t*>(base + L.sort_counts);
   c.sort_totals = reinterpret_cast<uint32_t*>(base + L.sort_totals);
@@ -440,6 +444,26 @@ size_t tbe_backward_workspace_size(const tbe_problem* prob, const tbe_options* o
   return make_bwd_layout(P, o, dev).total;
 }
 
+tbe_status tbe_psw_gradient(const tbe_problem* prob, const tbe_options* opt, const tbe_tables* tables,
+                            const void* weights, const void* indices, const void* offsets,
+                            const float* grad_out, float* grad_psw, void* stream) {
+  Problem P;
+  tbe_status st = make_problem(prob, &P);
+  if (st != TBE_OK) return st;
+  const tbe_options o = resolve(opt);
+  if ((st = check_options(o)) != TBE_OK) return st;
+  if (!P.weighted || !tables_ok(tables) || weights == nullptr || offsets == nullptr || grad_out == nullptr ||
+      (P.num_indices > 0 && (indices == nullptr || grad_psw == nullptr)))
+    return TBE_ERR_INVALID_ARG;
+  if (!aligned(weights, 16) || !aligned(grad_out, 16)) return TBE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != TBE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LaunchTally tally(o);
+  const cudaError_t e = launch_psw_gradient(P, *tables, weights, indices, offsets, grad_out, grad_psw, dev, s);
+  return e == cudaSuccess ? TBE_OK : cuda_status(e);
+}
+
 tbe_status tbe_backward_prepare(const tbe_problem* prob, const tbe_options* opt, const tbe_tables* tables,
                                 const void* indices, const void* offsets, const float* psw, void* ws,
                                 size_t ws_bytes, int64_t* d_stats, void* stream) {
@@ -536,7 +560,7 @@ tbe_status tbe_backward_metadata(const tbe_problem* prob, const tbe_options* opt
   meta->counters = reinterpret_cast<const uint32_t*>(base + L.counters);
   meta->sorted_keys = reinterpret_cast<const uint32_t*>(base + L.keys[L.final_buf]);
   meta->sorted_bags = reinterpret_cast<const uint32_t*>(base + L.vals[L.final_buf]);
-  meta->sorted_psw = P.weighted ? reinterpret_cast<const float*>(base + L.psw[L.final_buf]) : nullptr;
+  meta->sorted_psw = P.scaled ? reinterpret_cast<const float*>(base + L.psw[L.final_buf]) : nullptr;
   meta->unique_keys = reinterpret_cast<const uint32_t*>(base + L.unique);
   meta->run_offsets = reinterpret_cast<const uint32_t*>(base + L.run_off);
   meta->run_lengths = reinterpret_cast<const uint32_t*>(base + L.run_len);

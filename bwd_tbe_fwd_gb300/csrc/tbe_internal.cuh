@@ -34,6 +34,8 @@ struct Problem {
   int64_t B = 0, TB = 0, num_indices = 0;
   int wdtype = 0, itype = 0;
   bool weighted = false;
+  int pooling = 0;          // tbe_pooling
+  bool scaled = false;      // the backward carries a per-lookup factor: weighted or mean pooling
   std::vector<int> D;
   std::vector<int64_t> E;
   std::vector<uint8_t> long_bags;
@@ -159,6 +161,10 @@ cudaError_t launch_backward_histogram(const Problem& P, const BwdCtx& c, int tab
 cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, const void* weights,
                                      const void* indices, const void* offsets, float* out, int table,
                                      unsigned long long* stats, const DeviceInfo& dev, cudaStream_t s);
+
+cudaError_t launch_psw_gradient(const Problem& P, const tbe_tables& tab, const void* weights,
+                                const void* indices, const void* offsets, const float* grad_out,
+                                float* grad_psw, const DeviceInfo& dev, cudaStream_t s);
 
 cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s);
 cudaError_t launch_sort(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s);

@@ -20,6 +20,7 @@ c_i32, c_i64, c_u8, c_f32, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint8, 
 TBE_OK, TBE_ERR_INVALID_ARG, TBE_ERR_UNSUPPORTED, TBE_ERR_WORKSPACE, TBE_ERR_CUDA, TBE_ERR_RANGE = range(6)
 TBE_F32, TBE_F16, TBE_BF16 = 0, 1, 2
 TBE_I32, TBE_I64 = 0, 1
+TBE_POOL_SUM, TBE_POOL_MEAN = 0, 1
 TBE_OPT_SGD, TBE_OPT_ROWWISE_ADAGRAD = 0, 1
 TBE_LONG_AUTO, TBE_LONG_TWO_KERNEL, TBE_LONG_FUSED = 0, 1, 2
 TBE_SCHED_GRID, TBE_SCHED_PERSISTENT, TBE_SCHED_CLC = 0, 1, 2
@@ -39,7 +40,7 @@ EXPORTED = (
     "tbe_default_options", "tbe_table_layout", "tbe_bounds_workspace_size", "tbe_bounds_check",
     "tbe_forward_workspace_size", "tbe_forward", "tbe_backward_workspace_size",
     "tbe_backward_update", "tbe_backward_metadata", "tbe_status_string", "tbe_version",
-    "tbe_last_cuda_error", "tbe_backward_update_noalloc", "tbe_backward_prepare",
+    "tbe_last_cuda_error", "tbe_backward_update_noalloc", "tbe_backward_prepare", "tbe_psw_gradient",
 )
 TBE_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -47,7 +48,7 @@ TBE_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
 class Problem(ctypes.Structure):
     _fields_ = [("T", c_i32), ("B", c_i64), ("num_indices", c_i64), ("D", ctypes.POINTER(c_i32)),
                 ("E", ctypes.POINTER(c_i64)), ("wdtype", ctypes.c_int), ("itype", ctypes.c_int),
-                ("weighted", c_i32), ("long_bags", ctypes.POINTER(c_u8))]
+                ("weighted", c_i32), ("long_bags", ctypes.POINTER(c_u8)), ("pooling", c_i32)]
 
 
 class Tables(ctypes.Structure):
@@ -103,13 +104,14 @@ def load(path: str | None = None):
         lib.tbe_backward_update.argtypes = [P, O, T, vp, vp, vp, vp, vp, vp, ctypes.c_int, c_f32, c_f32,
                                             vp, ctypes.c_size_t, vp, vp]
         lib.tbe_backward_prepare.argtypes = [P, O, T, vp, vp, vp, vp, ctypes.c_size_t, vp, vp]
+        lib.tbe_psw_gradient.argtypes = [P, O, T, vp, vp, vp, vp, vp, vp]
         lib.tbe_backward_metadata.argtypes = [P, O, vp, ctypes.c_size_t, M]
         lib.tbe_status_string.argtypes = [ctypes.c_int]
         lib.tbe_status_string.restype = ctypes.c_char_p
         lib.tbe_version.restype = ctypes.c_int
         lib.tbe_last_cuda_error.restype = ctypes.c_int
         for name in ("tbe_table_layout", "tbe_bounds_check", "tbe_forward", "tbe_backward_update",
-                     "tbe_backward_prepare", "tbe_backward_metadata"):
+                     "tbe_backward_prepare", "tbe_psw_gradient", "tbe_backward_metadata"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -178,7 +180,7 @@ class TableBatchedEmbedding:
 
     def __init__(self, D, E, B: int, num_indices: int, weight_dtype: torch.dtype,
                  index_dtype: torch.dtype = torch.int64, weighted: bool = False, long_bags=None,
-                 device="cuda", options: TBEOptions | None = None):
+                 device="cuda", options: TBEOptions | None = None, pooling: str = "sum"):
         self.lib = load()
         dev = torch.device(device)
         if dev.type == "cuda" and dev.index is None:
@@ -195,8 +197,10 @@ class TableBatchedEmbedding:
         self._D = (c_i32 * self.T)(*self.D)
         self._E = (c_i64 * self.T)(*self.E)
         self._long = (c_u8 * self.T)(*([1 if x else 0 for x in long_bags] if long_bags is not None else [0] * self.T))
+        self.pooling = pooling
         self.prob = Problem(self.T, self.B, self.num_indices, self._D, self._E, _WDTYPE[weight_dtype],
-                            _ITYPE[index_dtype], 1 if self.weighted else 0, self._long)
+                            _ITYPE[index_dtype], 1 if self.weighted else 0, self._long,
+                            {"sum": TBE_POOL_SUM, "mean": TBE_POOL_MEAN}[pooling])
         self.options = options or TBEOptions()
         woff = (c_i64 * (self.T + 1))()
         doff = (c_i32 * (self.T + 1))()
@@ -263,6 +267,23 @@ class TableBatchedEmbedding:
                                   _ptr(self.ws_forward), self.ws_forward.numel(), _ptr(stats), _stream(stream))
         _check(self.lib, st, "tbe_forward")
         return out
+
+    def psw_gradient(self, weights, indices, offsets, grad_out, grad_psw=None, stream=None,
+                     options: TBEOptions | None = None):
+        """Gradient with respect to the per-sample weights (weighted problems); call it before
+        backward_update changes the weights.  Returns grad_psw [num_indices] fp32."""
+        self._idx(indices, offsets)
+        self._dev(weights, "weights", self.weight_dtype, self.num_weights)
+        self._dev(grad_out, "grad_out", torch.float32, self.B * self.total_D)
+        if grad_psw is None:
+            grad_psw = torch.zeros(self.num_indices, dtype=torch.float32, device=self.device)
+        self._dev(grad_psw, "grad_psw", torch.float32, self.num_indices)
+        o = (options or self.options).c
+        st = self.lib.tbe_psw_gradient(ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables),
+                                       _ptr(weights), _ptr(indices), _ptr(offsets), _ptr(grad_out), _ptr(grad_psw),
+                                       _stream(stream))
+        _check(self.lib, st, "tbe_psw_gradient")
+        return grad_psw
 
     def backward_prepare(self, indices, offsets, psw=None, stats=None, stream=None,
                          options: TBEOptions | None = None):

@@ -67,6 +67,7 @@ typedef enum {
 
 typedef enum { TBE_F32 = 0, TBE_F16 = 1, TBE_BF16 = 2 } tbe_dtype;
 typedef enum { TBE_I32 = 0, TBE_I64 = 1 } tbe_itype;
+typedef enum { TBE_POOL_SUM = 0, TBE_POOL_MEAN = 1 } tbe_pooling;
 typedef enum { TBE_OPT_SGD = 0, TBE_OPT_ROWWISE_ADAGRAD = 1 } tbe_optimizer;
 
 /* Long-run update ([FBT] section 3 and section 4, Problem 5): runs of at least
@@ -118,6 +119,10 @@ typedef struct {
    * It only steers the choice of the counts x table path ([FBT] section 2, "The small-table
    * histogram and tensor-core path"); results do not depend on it. */
   const uint8_t* long_bags;
+  /* tbe_pooling: SUM, or MEAN ("Table-Batched Embeddings in Triton", "Try this": the sum
+   * divided by the bag length; an empty bag gives 0).  The backward of MEAN scales each
+   * lookup's gradient row by psw / L (1 / L when unweighted). */
+  int32_t pooling;
 } tbe_problem;
 
 /* Device arrays describing the packed layout (see tbe_table_layout). */
@@ -219,6 +224,16 @@ tbe_status tbe_backward_prepare(const tbe_problem* prob, const tbe_options* opt,
                                 const tbe_tables* tables, const void* indices, const void* offsets,
                                 const float* psw, void* ws, size_t ws_bytes, int64_t* d_stats,
                                 void* stream);
+
+/* Gradient with respect to the per-sample weights of a weighted problem: for lookup p of bag
+ * (t, b), grad_psw[p] = sum_d grad_out[b, col_t + d] * W_t[idx[p], d] (divided by the bag length
+ * for MEAN pooling), accumulated in fp32 (fp64 for fp32 tables).  It reads the weights as they
+ * are, so call it before tbe_backward_update changes them.  grad_psw: device fp32
+ * [num_indices]; positions outside every bag are not written, lookups with an out-of-range id
+ * get 0.  TBE_ERR_INVALID_ARG for an unweighted problem.  No workspace. */
+tbe_status tbe_psw_gradient(const tbe_problem* prob, const tbe_options* opt, const tbe_tables* tables,
+                            const void* weights, const void* indices, const void* offsets,
+                            const float* grad_out, float* grad_psw, void* stream);
 
 /* Device counters kept in the backward workspace (uint32), for the metadata view below. */
 enum {

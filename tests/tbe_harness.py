@@ -102,8 +102,9 @@ class Case:
     """One workload instance on both sides."""
 
     def __init__(self, cfg, device="cuda", options: TBEOptions | None = None, threshold=None, chunk=None,
-                 bounds_check=True):
+                 bounds_check=True, pooling="sum"):
         self.cfg = cfg
+        self.pooling = pooling
         self.batch = make_batch(cfg)
         self.tables = oracle.Tables(cfg.D, cfg.E)
         opts = options or TBEOptions()
@@ -115,7 +116,7 @@ class Case:
         itype = torch.int32 if cfg.itype == "i32" else torch.int64
         self.tbe = TableBatchedEmbedding(
             cfg.D, cfg.E, cfg.B, self.batch.N, TORCH_W[cfg.wdtype], itype, weighted=cfg.weighted,
-            long_bags=[t.histogram for t in cfg.tables], device=device, options=opts)
+            long_bags=[t.histogram for t in cfg.tables], device=device, options=opts, pooling=pooling)
         self.device = device
         self.w0 = weights_tensor(cfg)                     # CPU, exact generator values
         self.grad = grad_out_tensor(cfg)                  # CPU [B, sum D]
@@ -148,9 +149,47 @@ class Case:
         out = self.tbe.forward(w_d, self.idx_d, self.off_d, psw=self.psw_d, stats=self.stats, options=options)
         torch.cuda.synchronize()
         o_out, exact, absterms = oracle.forward(self.tables, self.cfg.B, weights_to_oracle(self.w0, self.cfg.wdtype),
-                                                self.idx_h, self.off_h, psw=self.psw_h, wdtype=self.cfg.wdtype)
+                                                self.idx_h, self.off_h, psw=self.psw_h, wdtype=self.cfg.wdtype,
+                                                pooling=self.pooling)
         check_forward(out.cpu().numpy(), exact, absterms, self.cfg.wdtype)
         return out
+
+    def psw_gradient(self):
+        """The library's gradient with respect to the per-sample weights against the oracle's,
+        per lookup, within rtol of the sum of |grad * w| over the row (its condition scale)."""
+        cfg = self.cfg
+        w_d = self.w0.to(self.device)
+        g = self.tbe.psw_gradient(w_d, self.idx_d, self.off_d, self.grad.to(self.device))
+        torch.cuda.synchronize()
+        w_h = weights_to_oracle(self.w0, cfg.wdtype)
+        ref = oracle.psw_gradient(self.tables, cfg.B, w_h, self.idx_h, self.off_h, self.grad.numpy(),
+                                  wdtype=cfg.wdtype, pooling=self.pooling)
+        # condition scale: sum_d |grad * w| of each lookup (over L for mean pooling)
+        w64 = weights_f64(self.w0)
+        D = np.asarray(cfg.D, dtype=np.int64)
+        E = np.asarray(cfg.E, dtype=np.int64)
+        eb = np.concatenate([[0], np.cumsum(E * D)])
+        cb = np.concatenate([[0], np.cumsum(D)])
+        off = self.off_h.astype(np.int64)
+        scale = np.zeros(len(ref))
+        for t in range(cfg.T):
+            for_b = np.repeat(np.arange(cfg.B), np.diff(off[t * cfg.B:(t + 1) * cfg.B + 1]))
+            s, e = off[t * cfg.B], off[(t + 1) * cfg.B]
+            rows = w64[eb[t]:eb[t + 1]].reshape(E[t], D[t])[self.idx_h[s:e].astype(np.int64)]
+            gr = self.grad.numpy()[for_b, cb[t]:cb[t + 1]].astype(np.float64)
+            sc = np.abs(rows * gr).sum(axis=1)
+            if self.pooling == "mean":
+                sc /= np.diff(off[t * cfg.B:(t + 1) * cfg.B + 1])[for_b]
+            scale[s:e] = sc
+        n = int(off[-1])
+        x = g.cpu().numpy()[:n].astype(np.float64)
+        err = np.abs(x - ref[:n])
+        bad = err > RTOL[cfg.wdtype] * np.maximum(np.abs(ref[:n]), scale[:n]) + 1e-30
+        if bad.any():
+            i = int(np.argwhere(bad)[0][0])
+            raise AssertionError(f"psw gradient mismatch at {i}: gpu {x[i]!r} oracle {ref[i]!r} "
+                                 f"({int(bad.sum())} of {n} out of tolerance)")
+        return g
 
     def backward(self, optimizer=None, steps=1, options=None, check_meta=True, prepared=False):
         cfg = self.cfg
@@ -179,7 +218,7 @@ class Case:
                                      lr=cfg.lr, eps=cfg.eps, stats=self.stats, options=options, prepared=prepared)
             torch.cuda.synchronize()
             res = oracle.backward(self.tables, cfg.B, w_h, state_h, self.idx_h, self.off_h, grad_h, psw=self.psw_h,
-                                  optimizer=opt, lr=cfg.lr, eps=cfg.eps, wdtype=cfg.wdtype)
+                                  optimizer=opt, lr=cfg.lr, eps=cfg.eps, wdtype=cfg.wdtype, pooling=self.pooling)
             if check_meta:
                 self.check_metadata(res, options)
             # each side continues from its own results (the oracle never takes GPU values);
@@ -193,7 +232,8 @@ class Case:
         """Tables whose backward the library runs as counts^T x grad_out (their lookups are not in
         the sorted metadata): the forward's counts x table tables, at most 8."""
         cfg = self.cfg
-        if not (options or self.options).c.histogram or cfg.wdtype != "f16" or cfg.weighted:
+        if (not (options or self.options).c.histogram or cfg.wdtype != "f16" or cfg.weighted
+                or self.pooling != "sum"):
             return []
         hist = [t for t, spec in enumerate(cfg.tables)
                 if spec.E <= 64 and 64 <= spec.D <= 128 and spec.histogram]

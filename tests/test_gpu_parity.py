@@ -108,6 +108,34 @@ def test_prepared_transpose_beside_the_forward(name):
     c.backward(prepared=True)
 
 
+@pytest.mark.parametrize("name", ["c5", "c2", "c1", "c3"])
+def test_mean_pooling(name):
+    """Mean pooling ("Table-Batched Embeddings in Triton", "Try this"): the forward divides each
+    bag's sum by its length (empty bags stay 0), the backward scales each lookup by psw / L; the
+    per-lookup factors in the metadata are the oracle's, bit for bit."""
+    c = Case(SMALL[name], pooling="mean")
+    c.forward()
+    c.backward()
+
+
+@pytest.mark.parametrize("pooling", ["sum", "mean"])
+@pytest.mark.parametrize("name", ["c5", "c1_weighted"])
+def test_psw_gradient(name, pooling):
+    """Gradient with respect to the per-sample weights, against the oracle per lookup."""
+    import dataclasses
+    cfg = SMALL["c5"] if name == "c5" else dataclasses.replace(get_config("c1"), weighted=True, name="c1_weighted")
+    c = Case(cfg, pooling=pooling)
+    g = c.psw_gradient()
+    assert torch.isfinite(g).all()
+
+
+def test_psw_gradient_rejects_unweighted():
+    from bwd_tbe_fwd_gb300.tbe import TBEError
+    c = Case(SMALL["c2"])
+    with pytest.raises(TBEError):
+        c.tbe.psw_gradient(c.w0.cuda(), c.idx_d, c.off_d, c.grad.cuda())
+
+
 def test_skewed_example_batch_routes_as_printed():
     """The tutorial's skewed batch (T=3, E=50, B=16, D=24, seed 1): the device classifier must
     produce the printed short/long/chunk counts for each threshold and chunk size."""
