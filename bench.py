@@ -45,6 +45,10 @@ def parse_args():
     ap.add_argument("--long-mode", choices=["auto", "two_kernel", "fused"], default="auto")
     ap.add_argument("--scheduler", choices=["grid", "persistent", "clc"], default="persistent")
     ap.add_argument("--merge", choices=["atomic", "bulk"], default="atomic")
+    ap.add_argument("--pooling", choices=["sum", "mean"], default="sum")
+    ap.add_argument("--psw-grad", action="store_true",
+                    help="weighted workloads: also compute the gradient with respect to the per-sample "
+                         "weights (tbe_psw_gradient) in each step, before the update")
     ap.add_argument("--classify", choices=["atomic", "ordered"], default="ordered")
     ap.add_argument("--hoist", choices=["on", "off"], default="off",
                     help="run the backward's transpose (tbe_backward_prepare) on a second stream beside "
@@ -140,6 +144,9 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None):
     bwd_hist = int(np.sum(st["per_table"][hist] * ib) + int(hist.sum()) * cfg.B * ib
                    + cfg.B * int(D[hist].sum()) * 4 + int(np.sum(cfg.E[hist] * (2 * D[hist] * wb + 8))))
     bwd_hist_flops = hist_flops
+    # gradient with respect to psw (weighted workloads): the rows again, the ids, one fp32 out per
+    # lookup, each bag's gradient row once
+    psw_grad = int(np.sum(st["per_table"] * (D * wb + ib + 4)) + TB * ib + cfg.B * int(D.sum()) * 4)
     bounds = (TB + 1) * ib + N * ib
     # the sort only sees the other tables' lookups and runs
     N = N - int(np.sum(st["per_table"][hist]))
@@ -163,7 +170,7 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None):
                           + 2 * Dr[~short] * wb + 8 + Dr[~short] * 4))
     return dict(bounds=bounds, gather=fwd, histogram=hist_bytes, histogram_flops=hist_flops, expand=expand,
                 sort=sort, rle=rle, classify=classify, short=upd_short, long=upd_long, apply=0,
-                bwd_histogram=bwd_hist, bwd_histogram_flops=bwd_hist_flops, lookups_sorted=N,
+                bwd_histogram=bwd_hist, bwd_histogram_flops=bwd_hist_flops, lookups_sorted=N, psw_grad=psw_grad,
                 lookups_short=int(L[short].sum()), lookups_long=int(L[~short].sum()),
                 runs_short=int(short.sum()), runs_long=int((~short).sum()), passes=passes)
 
@@ -362,7 +369,9 @@ def run_ours(args):
     itype = torch.int32 if cfg.itype == "i32" else torch.int64
     tbe = TableBatchedEmbedding(cfg.D, cfg.E, cfg.B, batch.N, torch_dtype(cfg.wdtype), itype,
                                 weighted=cfg.weighted, long_bags=[t.histogram for t in cfg.tables],
-                                device=dev, options=opts)
+                                device=dev, options=opts, pooling=args.pooling)
+    psw_grad = args.psw_grad and cfg.weighted
+    grad_psw = torch.empty(batch.N, dtype=torch.float32, device=dev) if psw_grad else None
     weights = weights_tensor(cfg, device=dev)
     state = torch.zeros(cfg.total_rows, dtype=torch.float32, device=dev) if cfg.optimizer == "adagrad" else None
     grad = grad_out_tensor(cfg, device=dev)
@@ -380,7 +389,7 @@ def run_ours(args):
     main = torch.cuda.current_stream(dev)
     side = torch.cuda.Stream(device=dev, priority=-1)  # its CTAs go first when SMs free up
 
-    def step(fev=None, bev=None, bounds_ev=None, pev=None):
+    def step(fev=None, bev=None, bounds_ev=None, pev=None, gev=None):
         if bounds_ev is not None:
             bounds_ev[0].record()
         tbe.bounds_check(idx, off, stats=stats)
@@ -395,6 +404,12 @@ def run_ours(args):
         tbe.forward(weights, idx, off, psw=psw, out=out, stats=stats)
         if args.hoist == "on":
             main.wait_stream(side)
+        if psw_grad:
+            if gev is not None:
+                gev[0].record()
+            tbe.psw_gradient(weights, idx, off, grad, grad_psw=grad_psw)
+            if gev is not None:
+                gev[1].record()
         opts.with_events(bev)
         tbe.backward_update(weights, state, idx, off, grad, psw=psw, optimizer=cfg.optimizer, lr=cfg.lr,
                             eps=cfg.eps, stats=stats, prepared=args.hoist == "on")
@@ -410,6 +425,7 @@ def run_ours(args):
     bevs = [[mk() for _ in range(TBE_BWD_NUM_EVENTS)] for _ in range(K)]
     bnds = [[mk(), mk()] for _ in range(K)]
     pevs = [[mk() for _ in range(TBE_BWD_NUM_EVENTS)] for _ in range(K)]
+    gevs = [[mk(), mk()] for _ in range(K)]
     e0, e1 = mk(), mk()
     clocks = ClockSampler(local)
     launches.value = 0
@@ -419,7 +435,7 @@ def run_ours(args):
     time.sleep(0.4)  # let the sampler take a first sample
     e0.record()
     for k in range(K):
-        step(fevs[k], bevs[k], bnds[k], pevs[k] if args.hoist == "on" else None)
+        step(fevs[k], bevs[k], bnds[k], pevs[k] if args.hoist == "on" else None, gevs[k])
     e1.record()
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -431,6 +447,7 @@ def run_ours(args):
 
     # per-stage device times (ms per step)
     stage_ms = {"bounds": np.mean([b[0].elapsed_time(b[1]) for b in bnds]),
+                "psw_grad": np.mean([g[0].elapsed_time(g[1]) for g in gevs]) if psw_grad else 0.0,
                 "gather": np.mean([f[0].elapsed_time(f[1]) for f in fevs]),
                 "histogram": np.mean([f[1].elapsed_time(f[2]) for f in fevs])}
     for i, name in enumerate(BWD_STAGES):
@@ -509,6 +526,7 @@ def run_ours(args):
                          if args.hoist == "on" else "tbe_bounds_check + tbe_forward + tbe_backward_update"),
                 "long_mode": args.long_mode, "scheduler": args.scheduler, "merge": args.merge, "classify": args.classify,
                 "transpose": "hoisted beside the forward (second stream)" if args.hoist == "on" else "in the backward",
+                "pooling": args.pooling, "psw_grad": bool(psw_grad),
                 "parallelism": f"replicas x{world}",
                 "l2": "inputs larger than L2 (weights alone exceed 129 MB); no flush between steps",
                 "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
