@@ -117,39 +117,56 @@ __global__ void __launch_bounds__(kThreads) offsets_fix_kernel(IT* offsets, int6
 }
 
 // Every lookup p in [0, N): its table is the t with offsets[t*B] <= p < offsets[(t+1)*B].
+// A thread checks 8 consecutive ids per step (two or four 16-byte loads), finds the table of
+// the first by binary search over the table starts in shared memory and walks forward for the
+// rest; the row counts of the tables sit in shared memory too.
 template <typename IT>
 __global__ void __launch_bounds__(kThreads) indices_fix_kernel(IT* indices, const IT* offsets,
                                                               int T, int64_t B,
                                                               const int64_t* roff,
                                                               const int64_t* ws,
-                                                              unsigned long long* stats) {
-  extern __shared__ int64_t tstart[];  // [T+1]
+                                                              unsigned long long* stats, int vec_ok) {
+  extern __shared__ int32_t tshared[];  // [T+1] table starts, then [T] row counts (both < 2^31)
+  int32_t* tstart = tshared;
+  int32_t* trows = tshared + T + 1;
   __shared__ unsigned long long shc[kThreads / kWarp];
-  for (int t = threadIdx.x; t <= T; t += blockDim.x) tstart[t] = static_cast<int64_t>(offsets[t * B]);
-  __syncthreads();
   const int64_t N = ws[0];
+  for (int t = threadIdx.x; t <= T; t += blockDim.x)
+    tstart[t] = static_cast<int32_t>(clamp64(static_cast<int64_t>(offsets[t * B]), 0, N));
+  for (int t = threadIdx.x; t < T; t += blockDim.x) trows[t] = static_cast<int32_t>(__ldg(roff + t + 1) - __ldg(roff + t));
+  __syncthreads();
   unsigned long long bad = 0;
-  constexpr int U = 4;  // ids per thread in flight
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * U;
-  for (int64_t pb = static_cast<int64_t>(blockIdx.x) * blockDim.x * U; pb < N; pb += stride) {
-    int64_t id[U];
+  constexpr int V = 8;                                  // ids per thread per step
+  constexpr int W = V * static_cast<int>(sizeof(IT)) / 16;  // 16-byte loads per step
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * V;
+  for (int64_t p0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * V; p0 < N; p0 += stride) {
+    IT id[V];
+    if (vec_ok && p0 + V <= N) {
+      const uint4* src = reinterpret_cast<const uint4*>(indices + p0);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t p = pb + u * blockDim.x + threadIdx.x;
-      id[u] = p < N ? static_cast<int64_t>(indices[p]) : 0;
+      for (int w = 0; w < W; ++w) {
+        const uint4 r = src[w];
+        const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) reinterpret_cast<uint32_t*>(id)[w * 4 + q] = words[q];
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < V; ++u) id[u] = p0 + u < N ? indices[p0 + u] : IT(0);
+    }
+    int lo = 0, hi = T;  // tstart[lo] <= p0 < tstart[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tstart[mid] <= p0) lo = mid;
+      else hi = mid;
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t p = pb + u * blockDim.x + threadIdx.x;
-      if (p >= N) continue;
-      int lo = 0, hi = T;  // tstart[lo] <= p < tstart[hi]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (tstart[mid] <= p) lo = mid;
-        else hi = mid;
-      }
-      const int64_t E = __ldg(roff + lo + 1) - __ldg(roff + lo);
-      if (id[u] < 0 || id[u] >= E) {
+    for (int u = 0; u < V; ++u) {
+      const int64_t p = p0 + u;
+      if (p >= N) break;
+      while (lo + 1 < T && tstart[lo + 1] <= p) ++lo;  // next table (tables can be empty)
+      const int64_t v = static_cast<int64_t>(id[u]);
+      if (v < 0 || v >= trows[lo]) {
         indices[p] = IT(0);
         ++bad;
       }
@@ -168,11 +185,13 @@ cudaError_t launch_typed(const Problem& P, const tbe_tables& tab, void* indices,
   offsets_fix_kernel<IT><<<grid, kThreads, 0, s>>>(off, P.TB, ws, stats);
   note_launch();
   if (P.num_indices > 0) {
-    const size_t smem = sizeof(int64_t) * (P.T + 1);
-    int64_t want = (P.num_indices + 4 * kThreads - 1) / (4 * kThreads);
-    const int g = static_cast<int>(want < grid ? (want < 1 ? 1 : want) : grid);
+    const size_t smem = sizeof(int32_t) * (2 * P.T + 1);
+    const int64_t want = (P.num_indices + 8 * kThreads - 1) / (8 * kThreads);
+    const int64_t cap = static_cast<int64_t>(grid) * 2;  // two waves of the bounds grid
+    const int g = static_cast<int>(want < cap ? (want < 1 ? 1 : want) : cap);
     indices_fix_kernel<IT><<<g, kThreads, smem, s>>>(static_cast<IT*>(indices), off, P.T, P.B,
-                                                     tab.row_offsets, ws, stats);
+                                                     tab.row_offsets, ws, stats,
+                                                     reinterpret_cast<uintptr_t>(indices) % 16 == 0 ? 1 : 0);
     note_launch();
   }
   return cudaGetLastError();

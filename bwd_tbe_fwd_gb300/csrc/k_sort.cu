@@ -57,6 +57,7 @@ struct ExpandArgs {
 template <typename IT, bool PSW>
 __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
   __shared__ int64_t s_off[kExpandBags + 1];
+  __shared__ uint32_t s_b[kExpandBags], s_rb[kExpandBags], s_E[kExpandBags], s_shift[kExpandBags];
   __shared__ unsigned long long s_bad;
   __shared__ int64_t s_hlen[kMaxHistTables];
   const int64_t N = clamp64(ld_int<IT>(a.offsets, a.TB), 0, a.num_indices);
@@ -80,57 +81,65 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
   for (int k = threadIdx.x + kThreads; k < nb; k += blockDim.x)
     if (s_off[k + 1] < s_off[k]) ++bad;
   const int64_t t0 = a.B > 0 ? i0 / a.B : 0;
-  const int64_t r0 = i0 - t0 * a.B;
-  const uint32_t B32 = static_cast<uint32_t>(a.B);
   int64_t p0 = s_off[0], p1 = max(s_off[0], s_off[nb]);
   if (a.nhist > 0 && nb > 0 && a.B > 0 && t0 == (i0 + nb - 1) / a.B) {
     bool all = false;  // every bag of this CTA is in one counts-path table
     for (int h = 0; h < a.nhist; ++h) all |= a.hist_t[h] == t0;
     if (all) p1 = p0;
   }
-  constexpr int U = 4;  // lookups per thread in flight
-  for (int64_t pb = p0; pb < p1; pb += U * blockDim.x) {
+  // per bag of the CTA: its bag index b, its table's first key and row count, and how far its
+  // lookups move down (the counts-path lookups before its table); row count 0 marks a bag of a
+  // counts-path table, whose lookups are left out
+  for (int k = threadIdx.x; k < nb; k += blockDim.x) {
+    const int64_t u = i0 + k;
+    const int t = static_cast<int>(u / a.B);
+    const int64_t rb = __ldg(a.roff + t);
+    s_b[k] = static_cast<uint32_t>(u - static_cast<int64_t>(t) * a.B);
+    s_rb[k] = static_cast<uint32_t>(rb);
+    uint32_t E = static_cast<uint32_t>(__ldg(a.roff + t + 1) - rb);
+    int64_t shift = 0;
+    for (int h = 0; h < a.nhist; ++h) {
+      if (a.hist_t[h] < t) shift += s_hlen[h];
+      if (a.hist_t[h] == t) E = 0;
+    }
+    s_E[k] = E;
+    s_shift[k] = static_cast<uint32_t>(shift);
+  }
+  __syncthreads();
+  constexpr int U = 4;  // consecutive lookups per thread
+  for (int64_t pb = p0 + static_cast<int64_t>(threadIdx.x) * U; pb < p1; pb += static_cast<int64_t>(U) * blockDim.x) {
     int64_t id[U];
     float w[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t p = pb + u * blockDim.x + threadIdx.x;
+      const int64_t p = pb + u;
       id[u] = p < p1 ? ld_int<IT>(a.indices, p) : 0;
       if (PSW) w[u] = p < p1 ? (a.psw != nullptr ? __ldg(a.psw + p) : 1.f) : 0.f;
     }
+    int lo = 0, hi = nb;  // s_off[lo] <= pb < s_off[hi] (for non-decreasing offsets)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_off[mid] <= pb) lo = mid;
+      else hi = mid;
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t p = pb + u * blockDim.x + threadIdx.x;
-      if (p >= p1) continue;
-      int lo = 0, hi = nb;  // s_off[lo] <= p < s_off[hi] (for non-decreasing offsets)
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_off[mid] <= p) lo = mid;
-        else hi = mid;
-      }
-      const uint32_t rel = static_cast<uint32_t>(r0 + lo);
-      const int t = static_cast<int>(t0 + rel / B32);
-      const uint32_t b = rel % B32;
-      int64_t q = p;  // where the lookup lands among the kept ones
-      if (a.nhist > 0) {
-        bool skip = false;
-        for (int h = 0; h < a.nhist; ++h) {
-          if (a.hist_t[h] < t) q -= s_hlen[h];
-          skip |= a.hist_t[h] == t;
-        }
-        if (skip || q < 0 || q >= n_kept) continue;  // (out of range only for unrepaired offsets)
-      }
-      const int64_t rb = __ldg(a.roff + t);
-      const int64_t E = __ldg(a.roff + t + 1) - rb;
+      const int64_t p = pb + u;
+      if (p >= p1) break;
+      while (lo + 1 < nb && s_off[lo + 1] <= p) ++lo;  // the next bags (possibly empty ones)
+      const uint32_t E = s_E[lo];
+      const bool hist_bag = a.nhist > 0 && E == 0;
+      const int64_t q = p - s_shift[lo];  // where the lookup lands among the kept ones
+      if (hist_bag || q < 0 || q >= n_kept) continue;  // (out of range only for unrepaired offsets)
       uint32_t key;
-      if (id[u] >= 0 && id[u] < E) {
-        key = static_cast<uint32_t>(rb + id[u]);
+      if (id[u] >= 0 && id[u] < static_cast<int64_t>(E)) {
+        key = s_rb[lo] + static_cast<uint32_t>(id[u]);
       } else {
         key = a.sentinel;
         ++bad;
       }
       a.keys[q] = key;
-      a.vals[q] = b;
+      a.vals[q] = s_b[lo];
       // the lookup's factor: psw, over the bag length for mean pooling (correctly rounded)
       if (PSW) a.psw_out[q] = a.mean ? __fdiv_rn(w[u], static_cast<float>(s_off[lo + 1] - s_off[lo])) : w[u];
     }
