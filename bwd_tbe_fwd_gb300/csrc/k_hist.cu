@@ -306,22 +306,22 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
 // fp32 gradient into 16-bit parts accumulating in fp32, then apply the optimizer to each row.
 // The pages split into fp16 hi + lo; here each fp32 value is split exactly into three bf16
 // parts (hi + mid + lo carry all 24 significand bits and keep fp32's exponent range, so no
-// gradient overflows or flushes), and counts <= 256 are exact in bf16.  Per CTA and tile of 128
-// bags (K = 128):
+// gradient overflows or flushes), and counts <= 256 are exact in bf16.  Per CTA and tile of 64
+// bags (K = 64; two CTAs per SM):
 //   1. count the first 256 ids of each bag as in the forward; ids past the 256th (rare) add
 //      their gradient row to the row's fp32 sum with atomics directly;
 //   2. B operand (N = E rounded up to 16, K-major): counts of row e in the tile's bags, bf16;
 //      A operands (M = 128 gradient columns, K-major): the three bf16 parts of grad_out[bag, d]
 //      -- a warp loads 8 bags x 32 columns coalesced and writes one 16-byte core-matrix row per
 //      lane and part;
-//   3. one thread issues 3 x 8 tcgen05.mma (K = 16 each) into one TMEM accumulator (128 lanes =
+//   3. one thread issues 3 x 4 tcgen05.mma (K = 16 each) into one TMEM accumulator (128 lanes =
 //      columns d, N columns = rows e) that lives across the CTA's tiles; the CTA waits on the
 //      commit (bounded) before it rewrites the operands;
 //   4. at the end each thread (column d) adds its accumulator row into the table's fp32 gradient
 //      sum with atomics; the last CTA to finish (fence + counter) applies the optimizer once to
 //      every row whose count is non-zero.
 // ------------------------------------------------------------------------------------------
-constexpr int kBK = 128;                       // bags per tile (the K of the MMA)
+constexpr int kBK = 64;                        // bags per tile (the K of the MMA)
 constexpr int kBM = 128;                       // gradient columns (the M of the MMA)
 constexpr uint32_t kBSBO = (kBK / 8) * 128;    // 2048 B between core matrices along M/N
 constexpr int kBATile = kBM * kBK * 2;         // 32 KB per bf16 split of the gradient
@@ -375,7 +375,7 @@ __device__ __forceinline__ void split3(float x, uint32_t& hi, uint32_t& mid, uin
 }
 
 template <typename IT>
-__global__ void __launch_bounds__(kThreads, 1) hist_bwd_kernel(HistBwdArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) hist_bwd_kernel(HistBwdArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* a_tiles = smem;                                  // 3 x 32 KB: gradient parts
@@ -701,7 +701,7 @@ cudaError_t launch_backward_histogram(const Problem& P, const BwdCtx& c, int tab
     flag.fetch_or(bit);
   }
   const int64_t tiles = (P.B + kBK - 1) / kBK;
-  int64_t grid = dev.sms;  // one CTA per SM (129 KB of shared memory each)
+  int64_t grid = 2 * static_cast<int64_t>(dev.sms);  // two CTAs per SM (65 KB of shared memory each)
   if (tiles < grid) grid = tiles;
   k<<<static_cast<int>(grid), kThreads, smem, s>>>(a);
   note_launch();
