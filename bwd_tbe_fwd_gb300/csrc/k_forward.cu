@@ -23,6 +23,10 @@
 //     83.9M-lookup stress batch).
 // Out-of-range ids are repaired to row 0 in flight when fused bounds checking is on (writing
 // the repaired id back), else skipped and counted; no id outside its table is dereferenced.
+// The same kernel in dot mode computes the gradient with respect to the per-sample weights: the
+// derivative of bag (t, b)'s pooled row with respect to psw[p] is W_t[idx[p]] (over L for mean
+// pooling), so grad_psw[p] = <grad_out[b, table's columns], W_t[idx[p]]>; each lane holds its
+// slice of the bag's gradient row and the row's dot product replaces its sum.
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -42,6 +46,10 @@ struct FwdArgs {
   int64_t unit_begin, unit_end;
   int bags_per_item;  // 1..32
   int mean;           // mean pooling: the sum over the bag length (an empty bag stays 0)
+  // dot mode (the gradient with respect to the per-sample weights): grad_out rows in, one fp32
+  // per lookup out: grad_psw[p] = <grad_out[b, table's columns], W[idx[p]]> (/ L for mean)
+  const float* grad;
+  float* grad_psw;
   int total_D;
   int fused_bounds;
   unsigned long long* stats;
@@ -131,7 +139,10 @@ __device__ __forceinline__ IdWindow<PSW> load_window(const FwdArgs& a, int pos, 
 // only loads on the critical path of a bag are its row loads: offsets and ids are fetched once
 // per item and up to 64 positions ahead.  Offsets that are not monotone (not repaired) cost a
 // reload of the windows where the stream jumps back or far ahead.
-template <typename WT, typename IT, bool PSW, int VB, int MAXV, int UNROLL>
+// DOT = the gradient with respect to the per-sample weights: the same walk over bags, windows and
+// rows, but each lane keeps its slice of the bag's gradient row and every row is dotted into it
+// (reduced within its row group) instead of being summed.
+template <typename WT, typename IT, bool PSW, int VB, int MAXV, int UNROLL, bool DOT>
 __global__ void __launch_bounds__(256, MAXV == 1 ? (sizeof(WT) == 4 ? 3 : 4) : (MAXV == 2 ? 2 : 1))
 fwd_gather_kernel(FwdArgs a) {
   using IO = VecIO<WT, VB>;
@@ -191,11 +202,21 @@ fwd_gather_kernel(FwdArgs a) {
     for (int k = 0; k < nb; ++k) {
       const int s = __shfl_sync(FULL, off_s, k);
       const int e = __shfl_sync(FULL, off_e, k);
-      Acc acc[MAXV][NE];
+      Acc acc[MAXV][NE];  // the pooled sums; in DOT mode the bag's gradient row slice
+      if constexpr (DOT) {
+        const float* grow = a.grad + (b0 + k) * a.total_D + col0;
 #pragma unroll
-      for (int m = 0; m < MAXV; ++m)
+        for (int m = 0; m < MAXV; ++m)
 #pragma unroll
-        for (int i = 0; i < NE; ++i) acc[m][i] = Acc(0);
+          for (int i = 0; i < NE; ++i)
+            acc[m][i] = vi + m * kWarp < nvec ? static_cast<Acc>(__ldg(grow + (vi + m * kWarp) * NE + i)) : Acc(0);
+      } else {
+#pragma unroll
+        for (int m = 0; m < MAXV; ++m)
+#pragma unroll
+          for (int i = 0; i < NE; ++i) acc[m][i] = Acc(0);
+      }
+      const Acc inv_len = (DOT && a.mean && e > s) ? Acc(1) / static_cast<Acc>(e - s) : Acc(1);
 
       for (int c0 = s; c0 < e; c0 += kWarp) {  // 32 positions of the bag at a time
         // slide the windows so that c0 - w0 is in [0, 32) (warp-uniform)
@@ -257,12 +278,54 @@ fwd_gather_kernel(FwdArgs a) {
               }
             }
           }
+          if constexpr (DOT) {
+            Acc dot[UNROLL];
 #pragma unroll
-          for (int q = 0; q < UNROLL; ++q)
+            for (int q = 0; q < UNROLL; ++q) {
+              dot[q] = 0;
 #pragma unroll
-            for (int m = 0; m < MAXV; ++m) accumulate<WT, VB, PSW>(acc[m], v[q][m], w[q]);
+              for (int m = 0; m < MAXV; ++m) {
+                if (vi + m * kWarp < nvec) {  // lanes past the row width re-read its last vector
+                  float f[NE];
+                  IO::unpack(v[q][m], f);
+#pragma unroll
+                  for (int i = 0; i < NE; ++i) dot[q] += acc[m][i] * static_cast<Acc>(f[i]);
+                }
+              }
+            }
+            if (UNROLL == 4 && lpr >= 4) {
+              // the four rows' partial dots reduced together: two halving rounds leave each lane
+              // one row (the bits lpr/2 and lpr/4 of its lane pick which), then a plain xor
+              // reduction over the remaining lanes of the row group
+              const int o1 = lpr >> 1, o2 = lpr >> 2;
+              const bool up1 = (lane & o1) != 0, up2 = (lane & o2) != 0;
+              Acc k0 = up1 ? dot[2] : dot[0], k1 = up1 ? dot[3] : dot[1];
+              k0 += __shfl_xor_sync(FULL, up1 ? dot[0] : dot[2], o1);
+              k1 += __shfl_xor_sync(FULL, up1 ? dot[1] : dot[3], o1);
+              Acc d = up2 ? k1 : k0;
+              d += __shfl_xor_sync(FULL, up2 ? k0 : k1, o2);
+              for (int off = o2 >> 1; off > 0; off >>= 1) d += __shfl_xor_sync(FULL, d, off);
+              const int q = (up1 ? 2 : 0) + (up2 ? 1 : 0);
+              const int r = j + q * rps + slot;
+              if ((vi & (o2 - 1)) == 0 && q < qmax && r < n) a.grad_psw[c0 + r] = static_cast<float>(d * inv_len);
+            } else {
+#pragma unroll
+              for (int q = 0; q < UNROLL; ++q) {
+                Acc d = dot[q];
+                for (int off = lpr >> 1; off > 0; off >>= 1) d += __shfl_xor_sync(FULL, d, off);
+                const int r = j + q * rps + slot;
+                if (vi == 0 && q < qmax && r < n) a.grad_psw[c0 + r] = static_cast<float>(d * inv_len);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < UNROLL; ++q)
+#pragma unroll
+              for (int m = 0; m < MAXV; ++m) accumulate<WT, VB, PSW>(acc[m], v[q][m], w[q]);
+          }
         }
       }
+      if constexpr (DOT) continue;  // no pooled row
       // reduce the row groups of the warp (lanes that share vi)
       for (int m = lpr; m < kWarp; m <<= 1) {
 #pragma unroll
@@ -295,7 +358,9 @@ fwd_gather_kernel(FwdArgs a) {
 template <typename WT, typename IT, bool PSW, int VB, int MAXV>
 cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   constexpr int UNROLL = MAXV >= 4 ? 1 : (MAXV == 2 ? 2 : 4);  // 4 to 8 loads in flight per lane
-  auto k = fwd_gather_kernel<WT, IT, PSW, VB, MAXV, UNROLL>;
+  // the gradient with respect to psw does not read psw: it runs the unweighted walk in DOT mode
+  auto k = a.grad_psw != nullptr ? fwd_gather_kernel<WT, IT, false, VB, MAXV, UNROLL, true>
+                                 : fwd_gather_kernel<WT, IT, PSW, VB, MAXV, UNROLL, false>;
   const int threads = 256;
   const int64_t tables = (a.unit_end - a.unit_begin) / a.B;
   const int64_t warps = static_cast<int64_t>(persistent_grid(k, threads, 0, dev, INT64_MAX)) * (threads / kWarp);
@@ -368,6 +433,8 @@ cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const
   a.total_D = P.total_D;
   a.fused_bounds = fused_bounds ? 1 : 0;
   a.mean = P.pooling == TBE_POOL_MEAN;
+  a.grad = nullptr;
+  a.grad_psw = nullptr;
   a.stats = stats;
   const int vb = P.vec_bytes;
   const int ne = vb / P.wbytes;
@@ -379,6 +446,43 @@ cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const
     case TBE_F32: return dispatch_it<float>(a, P.itype, has_psw, vb, maxv, dev, s);
     case TBE_F16: return dispatch_it<__half>(a, P.itype, has_psw, vb, maxv, dev, s);
     default: return dispatch_it<__nv_bfloat16>(a, P.itype, has_psw, vb, maxv, dev, s);
+  }
+}
+
+// The gradient with respect to the per-sample weights: the gather's walk in dot mode over every
+// table (it neither repairs nor counts ids: the forward did).
+cudaError_t launch_psw_gradient(const Problem& P, const tbe_tables& tab, const void* weights,
+                                const void* indices, const void* offsets, const float* grad_out,
+                                float* grad_psw, const DeviceInfo& dev, cudaStream_t s) {
+  if (P.TB == 0 || P.num_indices == 0) return cudaSuccess;
+  FwdArgs a;
+  a.weights = weights;
+  a.woff = tab.weight_offsets;
+  a.doff = tab.D_offsets;
+  a.roff = tab.row_offsets;
+  a.indices = const_cast<void*>(indices);  // read only: fused_bounds is off
+  a.offsets = offsets;
+  a.psw = nullptr;
+  a.out = nullptr;
+  a.B = P.B;
+  a.num_indices = P.num_indices;
+  a.unit_begin = 0;
+  a.unit_end = P.TB;
+  a.total_D = P.total_D;
+  a.fused_bounds = 0;
+  a.mean = P.pooling == TBE_POOL_MEAN;
+  a.grad = grad_out;
+  a.grad_psw = grad_psw;
+  a.stats = nullptr;
+  const int vb = P.vec_bytes;
+  const int ne = vb / P.wbytes;
+  const int max_nvec = P.max_D / ne;
+  int maxv = (max_nvec + kWarp - 1) / kWarp;
+  maxv = maxv <= 1 ? 1 : (maxv <= 2 ? 2 : (maxv <= 4 ? 4 : 8));
+  switch (P.wdtype) {
+    case TBE_F32: return dispatch_it<float>(a, P.itype, false, vb, maxv, dev, s);
+    case TBE_F16: return dispatch_it<__half>(a, P.itype, false, vb, maxv, dev, s);
+    default: return dispatch_it<__nv_bfloat16>(a, P.itype, false, vb, maxv, dev, s);
   }
 }
 
