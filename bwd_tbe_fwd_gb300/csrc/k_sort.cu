@@ -250,27 +250,34 @@ __global__ void __launch_bounds__(kThreads) digit_scan_kernel(uint32_t* counts, 
 
 size_t downsweep_smem_bytes(int rb, bool psw) {
   const size_t R = size_t(1) << rb;
-  return sizeof(uint32_t) * kSortTile * (psw ? 3 : 2) + sizeof(uint16_t) * kWarpsPerBlock * R +
+  return 2 * sizeof(uint32_t) * kSortTile * (psw ? 3 : 2) + sizeof(uint16_t) * kWarpsPerBlock * R +
          sizeof(uint32_t) * 3 * R;
 }
 
-// Stable scatter of each CTA's segment, tile by tile, to its digits' output ranges.
+constexpr uint32_t kTileWaitLimit = 1u << 22;
+
+// Stable scatter of each CTA's segment, tile by tile, to its digits' output ranges.  A tile's
+// keys, bags (and psw) arrive in shared memory by bulk copies (cp.async.bulk with an mbarrier)
+// issued one tile ahead into the other of two buffers, so the copy engine streams the segment
+// while the CTA ranks and scatters the current tile; the buffer that brought a tile in is then
+// reused for its reordering.  A partial tile whose size is not a multiple of 16 bytes (only the
+// last one of the whole array) is read with plain loads.
 template <int RB, bool PSW>
-__global__ void __launch_bounds__(kThreads, 3) radix_downsweep_kernel(
+__global__ void __launch_bounds__(kThreads, 2) radix_downsweep_kernel(
     const uint32_t* keys_in, const uint32_t* vals_in, const float* psw_in, uint32_t* keys_out,
     uint32_t* vals_out, float* psw_out, const uint32_t* counters, const uint32_t* scanned,
-    const uint32_t* totals, int shift, int G) {
+    const uint32_t* totals, int shift, int G, unsigned long long* stats) {
   constexpr int R = 1 << RB;
   constexpr int DPT = R / kThreads;  // digits per thread
-  extern __shared__ __align__(16) uint32_t s_dyn[];
-  uint32_t* s_keys = s_dyn;
-  uint32_t* s_vals = s_dyn + kSortTile;
-  float* s_psw = reinterpret_cast<float*>(s_dyn + 2 * kSortTile);
-  uint16_t* s_whist = reinterpret_cast<uint16_t*>(s_dyn + (PSW ? 3 : 2) * kSortTile);  // [warps][R]
+  constexpr int NA = PSW ? 3 : 2;    // arrays per tile buffer
+  extern __shared__ __align__(128) uint32_t s_dyn[];
+  uint16_t* s_whist = reinterpret_cast<uint16_t*>(s_dyn + 2 * NA * kSortTile);  // [warps][R]
   uint32_t* s_run = reinterpret_cast<uint32_t*>(s_whist + kWarpsPerBlock * R);
   uint32_t* s_dstart = s_run + R;
   uint32_t* s_tcount = s_dstart + R;
   __shared__ uint32_t s_wsum[kWarpsPerBlock];
+  __shared__ __align__(8) uint64_t s_bar[2];
+  __shared__ int s_bulk[2];
 
   const int lane = lane_id(), w = threadIdx.x / kWarp;
   const unsigned lt = lanemask_lt();
@@ -293,11 +300,45 @@ __global__ void __launch_bounds__(kThreads, 3) radix_downsweep_kernel(
       run += tt[q];
     }
   }
+  // bulk-copy tile tb into buffer b (thread 0); false when its byte count is not a multiple of 16
+  auto issue = [&](int64_t tb, int b) -> int {
+    const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(kSortTile), b1 - tb)) * 4u;
+    if (bytes % 16 != 0) return 0;
+    uint32_t* dst = s_dyn + b * NA * kSortTile;
+    mbar_arrive_expect_tx(&s_bar[b], bytes * NA);
+    bulk_copy_g2s(dst, keys_in + tb, bytes, &s_bar[b]);
+    bulk_copy_g2s(dst + kSortTile, vals_in + tb, bytes, &s_bar[b]);
+    if (PSW) bulk_copy_g2s(dst + 2 * kSortTile, psw_in + tb, bytes, &s_bar[b]);
+    return 1;
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_bulk[0] = b0 < b1 ? issue(b0, 0) : 0;
+  }
+  __syncthreads();
+  uint32_t phase[2] = {0u, 0u};
+  bool failed = false;
 
-  for (int64_t tb = b0; tb < b1; tb += kSortTile) {
+  int cur = 0;
+  for (int64_t tb = b0; tb < b1; tb += kSortTile, cur ^= 1) {
     const int n = static_cast<int>(min(static_cast<int64_t>(kSortTile), b1 - tb));
+    // the next tile into the other buffer (free since the end of the previous tile)
+    if (threadIdx.x == 0) s_bulk[cur ^ 1] = tb + kSortTile < b1 ? issue(tb + kSortTile, cur ^ 1) : 0;
     uint32_t* wh32 = reinterpret_cast<uint32_t*>(s_whist);
     for (int j = threadIdx.x; j < kWarpsPerBlock * R / 2; j += blockDim.x) wh32[j] = 0;
+    uint32_t* s_keys = s_dyn + cur * NA * kSortTile;
+    uint32_t* s_vals = s_keys + kSortTile;
+    float* s_psw = reinterpret_cast<float*>(s_keys + 2 * kSortTile);
+    const bool bulk = s_bulk[cur] != 0;
+    if (bulk) {
+      if (!mbar_wait_bounded(&s_bar[cur], phase[cur], kTileWaitLimit)) {
+        failed = true;
+        if (threadIdx.x == 0) stat_add(stats, TBE_STAT_WAIT_TIMEOUT, 1);
+      }
+      phase[cur] ^= 1u;
+    }
     __syncthreads();
 
     uint32_t k[kSortItems], v[kSortItems], rank[kSortItems];
@@ -306,9 +347,15 @@ __global__ void __launch_bounds__(kThreads, 3) radix_downsweep_kernel(
     for (int i = 0; i < kSortItems; ++i) {
       const int e = w * (kSortItems * kWarp) + i * kWarp + lane;
       const bool ok = e < n;
-      k[i] = ok ? keys_in[tb + e] : 0u;
-      v[i] = ok ? vals_in[tb + e] : 0u;
-      if (PSW) pw[i] = ok ? psw_in[tb + e] : 0.f;
+      if (bulk) {
+        k[i] = ok ? s_keys[e] : 0u;
+        v[i] = ok ? s_vals[e] : 0u;
+        if (PSW) pw[i] = ok ? s_psw[e] : 0.f;
+      } else {
+        k[i] = ok ? keys_in[tb + e] : 0u;
+        v[i] = ok ? vals_in[tb + e] : 0u;
+        if (PSW) pw[i] = ok ? psw_in[tb + e] : 0.f;
+      }
     }
     uint16_t* my_hist = s_whist + w * R;
 #pragma unroll
@@ -326,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 3) radix_downsweep_kernel(
       rank[i] = base + __popc(peers & lt);
       __syncwarp();
     }
-    __syncthreads();
+    __syncthreads();  // also: every thread has read its items out of the buffer
     // per digit: exclusive prefix over the warps (in place) and the tile count, then the
     // exclusive scan of the tile counts over the digits
     uint32_t tc[DPT], tsum = 0;
@@ -372,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 3) radix_downsweep_kernel(
       vals_out[g] = s_vals[j];
       if (PSW) psw_out[g] = s_psw[j];
     }
+    fence_proxy_async_smem();  // this buffer's generic accesses before the next bulk copy into it
     __syncthreads();
 #pragma unroll
     for (int q = 0; q < DPT; ++q) {
@@ -379,6 +427,9 @@ __global__ void __launch_bounds__(kThreads, 3) radix_downsweep_kernel(
       s_run[d] += s_tcount[d];
     }
     __syncthreads();
+  }
+  if (failed) {  // a copy that never signalled: wait once more (bounded) before the CTA exits
+    mbar_wait_bounded(&s_bar[cur ^ 1], phase[cur ^ 1] ^ 1u, kTileWaitLimit);
   }
 }
 
@@ -557,11 +608,11 @@ cudaError_t launch_sort_rb(const Problem& P, const BwdCtx& c, const BwdLayout& L
     if (psw)
       radix_downsweep_kernel<RB, true><<<G, kThreads, smem, s>>>(
           c.keys[cur], c.vals[cur], c.pswbuf[cur], c.keys[cur ^ 1], c.vals[cur ^ 1], c.pswbuf[cur ^ 1],
-          c.counters, c.sort_counts, c.sort_totals, shift, G);
+          c.counters, c.sort_counts, c.sort_totals, shift, G, c.stats);
     else
       radix_downsweep_kernel<RB, false><<<G, kThreads, smem, s>>>(
           c.keys[cur], c.vals[cur], nullptr, c.keys[cur ^ 1], c.vals[cur ^ 1], nullptr, c.counters,
-          c.sort_counts, c.sort_totals, shift, G);
+          c.sort_counts, c.sort_totals, shift, G, c.stats);
     note_launch();
     cur ^= 1;
   }

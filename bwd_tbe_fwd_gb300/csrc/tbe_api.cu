@@ -153,7 +153,7 @@ BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const Device
   if (L.radix_bits < 8) L.radix_bits = 8;
   L.final_buf = L.passes & 1;
   const int64_t tiles = (static_cast<int64_t>(n_cap) + kSortTile - 1) / kSortTile;
-  int64_t sg = dev.sms * 3;
+  int64_t sg = dev.sms * 2;  // two resident radix CTAs per SM (double-buffered tiles)
   if (sg > 1024) sg = 1024;
   if (tiles < sg) sg = tiles;
   L.sort_grid = static_cast<int>(sg < 1 ? 1 : sg);

@@ -330,6 +330,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) global -> shared,
+// completion counted in bytes on the mbarrier.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Orders this thread's earlier shared-memory accesses before later bulk-copy (async proxy)
 // accesses of the same memory, and makes barrier initialisation visible to it.
 __device__ __forceinline__ void fence_proxy_async_smem() {
