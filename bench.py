@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "TBE fwd+bwd lookups/s and achieved HBM GB/s (% of roofline) on 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
-BOUNDS_LAUNCHES = 3  # offsets max, offsets fix, ids check (one tbe_bounds_check call)
+BOUNDS_LAUNCHES = {"separate": 3, "fused": 2}  # offsets max, offsets fix (+ ids check)
 
 
 def parse_args():
@@ -46,6 +46,9 @@ def parse_args():
     ap.add_argument("--scheduler", choices=["grid", "persistent", "clc"], default="persistent")
     ap.add_argument("--merge", choices=["atomic", "bulk"], default="atomic")
     ap.add_argument("--pooling", choices=["sum", "mean"], default="sum")
+    ap.add_argument("--bounds", choices=["fused", "separate"], default="fused",
+                    help="fused: the offsets kernel, then the forward repairs ids as it reads them; "
+                         "separate: tbe_bounds_check repairs offsets and ids before the forward")
     ap.add_argument("--psw-grad", action="store_true",
                     help="weighted workloads: also compute the gradient with respect to the per-sample "
                          "weights (tbe_psw_gradient) in each step, before the update")
@@ -124,7 +127,7 @@ def batch_stats(cfg, batch):
                 hottest=int(cnt.max()) if len(cnt) else 0)
 
 
-def byte_model(cfg, st, threshold=256, chunk=256, passes=None):
+def byte_model(cfg, st, threshold=256, chunk=256, passes=None, bounds_ids=True):
     """Algorithmic bytes of each stage for one step (what the method must move)."""
     wb = {"f32": 4, "f16": 2, "bf16": 2}[cfg.wdtype]
     ib = 4 if cfg.itype == "i32" else 8
@@ -147,7 +150,7 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None):
     # gradient with respect to psw (weighted workloads): the rows again, the ids, one fp32 out per
     # lookup, each bag's gradient row once
     psw_grad = int(np.sum(st["per_table"] * (D * wb + ib + 4)) + TB * ib + cfg.B * int(D.sum()) * 4)
-    bounds = (TB + 1) * ib + N * ib
+    bounds = (TB + 1) * ib + (N * ib if bounds_ids else 0)  # offsets (+ ids unless the forward checks them)
     # the sort only sees the other tables' lookups and runs
     N = N - int(np.sum(st["per_table"][hist]))
     run_keep = ~hist[st["run_table"]]
@@ -365,6 +368,7 @@ def run_ours(args):
     opts = TBEOptions(long_mode={"auto": 0, "two_kernel": 1, "fused": 2}[args.long_mode],
                       scheduler={"grid": 0, "persistent": 1, "clc": 2}[args.scheduler],
                       merge={"atomic": 0, "bulk": 1}[args.merge],
+                      fused_bounds=1 if args.bounds == "fused" else 0,
                       classify_mode={"atomic": 0, "ordered": 1}[args.classify])
     itype = torch.int32 if cfg.itype == "i32" else torch.int64
     tbe = TableBatchedEmbedding(cfg.D, cfg.E, cfg.B, batch.N, torch_dtype(cfg.wdtype), itype,
@@ -394,7 +398,7 @@ def run_ours(args):
         idx, off, psw = ins if ins is not None else inputs
         if bounds_ev is not None:
             bounds_ev[0].record()
-        tbe.bounds_check(idx, off, stats=stats)
+        tbe.bounds_check(idx, off, stats=stats, offsets_only=args.bounds == "fused")
         if bounds_ev is not None:
             bounds_ev[1].record()
         if args.hoist == "on":
@@ -442,7 +446,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(world)
-    gpu_launches = int(launches.value) + K * BOUNDS_LAUNCHES
+    gpu_launches = int(launches.value) + K * BOUNDS_LAUNCHES[args.bounds]
     ms_total = e0.elapsed_time(e1)
     ms_max = all_max(world, ms_total, dev)
     lookups_all = all_sum(world, float(st["N"]) * K, dev)
@@ -458,7 +462,7 @@ def run_ours(args):
         stage_ms[name] = float(np.mean([b[i].elapsed_time(b[i + 1]) for b in src]))
     fwd_ms = float(np.mean([f[0].elapsed_time(f[2]) for f in fevs]))
     bwd_ms = float(np.mean([b[0].elapsed_time(b[-1]) for b in bevs]))
-    model = byte_model(cfg, st, opts.c.long_threshold, opts.c.chunk)
+    model = byte_model(cfg, st, opts.c.long_threshold, opts.c.chunk, bounds_ids=args.bounds != "fused")
     peak, peak_kind = peaks()
     stages = {}
     for name, ms in stage_ms.items():
@@ -545,8 +549,10 @@ def run_ours(args):
                 "workload": f"{cfg.name}: {cfg.description}",
                 "lookups_per_step": st["N"], "distinct_rows": st["U"], "hottest_row_hits": st["hottest"],
                 "long_runs": model["runs_long"], "lookups_in_long_runs": model["lookups_long"],
-                "weights_storage": cfg.wdtype, "step": ("tbe_bounds_check + (tbe_forward || tbe_backward_prepare) + tbe_backward_update(prepared)"
-                         if args.hoist == "on" else "tbe_bounds_check + tbe_forward + tbe_backward_update"),
+                "weights_storage": cfg.wdtype, "step": (("tbe_bounds_check_offsets" if args.bounds == "fused" else "tbe_bounds_check")
+                         + (" + (tbe_forward || tbe_backward_prepare) + tbe_backward_update(prepared)"
+                            if args.hoist == "on" else " + tbe_forward + tbe_backward_update")
+                         + (" (ids repaired inside tbe_forward)" if args.bounds == "fused" else "")),
                 "long_mode": args.long_mode, "scheduler": args.scheduler, "merge": args.merge, "classify": args.classify,
                 "transpose": "hoisted beside the forward (second stream)" if args.hoist == "on" else "in the backward",
                 "pooling": args.pooling, "psw_grad": bool(psw_grad),

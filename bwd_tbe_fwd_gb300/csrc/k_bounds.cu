@@ -178,13 +178,13 @@ __global__ void __launch_bounds__(kThreads) indices_fix_kernel(IT* indices, cons
 
 template <typename IT>
 cudaError_t launch_typed(const Problem& P, const tbe_tables& tab, void* indices, void* offsets,
-                         int64_t* ws, int grid, unsigned long long* stats, cudaStream_t s) {
+                         int64_t* ws, int grid, unsigned long long* stats, bool with_ids, cudaStream_t s) {
   IT* off = static_cast<IT*>(offsets);
   offsets_max_kernel<IT><<<grid, kThreads, 0, s>>>(off, P.TB, P.num_indices, ws);
   note_launch();
   offsets_fix_kernel<IT><<<grid, kThreads, 0, s>>>(off, P.TB, ws, stats);
   note_launch();
-  if (P.num_indices > 0) {
+  if (with_ids && P.num_indices > 0) {
     const size_t smem = sizeof(int32_t) * (2 * P.T + 1);
     const int64_t want = (P.num_indices + 8 * kThreads - 1) / (8 * kThreads);
     const int64_t cap = static_cast<int64_t>(grid) * 2;  // two waves of the bounds grid
@@ -202,9 +202,9 @@ cudaError_t launch_typed(const Problem& P, const tbe_tables& tab, void* indices,
 int bounds_grid(const DeviceInfo& dev) { return dev.sms * 4 < 1024 ? dev.sms * 4 : 1024; }
 
 cudaError_t launch_bounds(const Problem& P, const tbe_tables& tab, void* indices, void* offsets,
-                          int64_t* ws, int grid, unsigned long long* stats, cudaStream_t s) {
-  if (P.itype == TBE_I32) return launch_typed<int32_t>(P, tab, indices, offsets, ws, grid, stats, s);
-  return launch_typed<int64_t>(P, tab, indices, offsets, ws, grid, stats, s);
+                          int64_t* ws, int grid, unsigned long long* stats, bool with_ids, cudaStream_t s) {
+  if (P.itype == TBE_I32) return launch_typed<int32_t>(P, tab, indices, offsets, ws, grid, stats, with_ids, s);
+  return launch_typed<int64_t>(P, tab, indices, offsets, ws, grid, stats, with_ids, s);
 }
 
 }  // namespace tbe

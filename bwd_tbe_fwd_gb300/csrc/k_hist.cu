@@ -52,6 +52,7 @@ struct HistArgs {
   int64_t bag0;          // t * B
   int E, D, N;           // N = D rounded up to a multiple of 16
   int col0, total_D;
+  int fused_bounds;      // repair out-of-range ids in flight (row 0, written back) instead of skipping
   unsigned long long* stats;
 };
 
@@ -205,17 +206,19 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
             cur = nxt;
             nxt = lo + 1 <= nb ? s_rel[lo + 1] : 0x7fffffff;
           }
-          if (r - cur >= kHistIds) continue;  // the scalar path adds it
           if (static_cast<uint64_t>(static_cast<int64_t>(id[j])) >= static_cast<uint64_t>(a.E)) {
             ++bad;
-            continue;
+            if (!a.fused_bounds) continue;  // skipped (the scalar path skips it too)
+            const_cast<IT*>(ids)[r] = IT(0);  // repaired in flight: row 0, written back
+            id[j] = IT(0);
           }
+          if (r - cur >= kHistIds) continue;  // the scalar path adds it
           const uint32_t k = static_cast<uint32_t>(id[j]);
           // two 16-bit counts per word (counts <= 256 never carry into the neighbour)
           atomicAdd(&pairs[lo * (kK / 2) + (k >> 1)], (k & 1u) << 16 | (~k & 1u));
         }
       }
-      if (bad) stat_add(a.stats, TBE_STAT_UNREPAIRED, bad);
+      if (bad) stat_add(a.stats, a.fused_bounds ? TBE_STAT_BAD_INDICES : TBE_STAT_UNREPAIRED, bad);
     }
     __syncthreads();
     // counts -> fp16 A tile (exact: counts <= 256), 8 counts (one 16-byte row of a core matrix)
@@ -609,7 +612,8 @@ bool histogram_supported() { return true; }
 
 cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, const void* weights,
                                      const void* indices, const void* offsets, float* out, int table,
-                                     unsigned long long* stats, const DeviceInfo& dev, cudaStream_t s) {
+                                     bool fused_bounds, unsigned long long* stats, const DeviceInfo& dev,
+                                     cudaStream_t s) {
   (void)tab;
   int64_t woff = 0, col0 = 0;
   for (int t = 0; t < table; ++t) {
@@ -629,6 +633,7 @@ cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, co
   a.N = (a.D + 15) / 16 * 16;
   a.col0 = static_cast<int>(col0);
   a.total_D = P.total_D;
+  a.fused_bounds = fused_bounds ? 1 : 0;
   a.stats = stats;
   if (P.B == 0) return cudaSuccess;
   const size_t smem = 3 * kTileBytes + 1024;  // A, B, count pairs + alignment slack

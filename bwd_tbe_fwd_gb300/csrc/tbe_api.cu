@@ -373,7 +373,23 @@ tbe_status tbe_bounds_check(const tbe_problem* prob, const tbe_tables* tables, v
   if (!aligned(ws, 8)) return TBE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return cuda_status(launch_bounds(P, *tables, indices, offsets, static_cast<int64_t*>(ws), grid,
-                                   reinterpret_cast<unsigned long long*>(d_stats), s));
+                                   reinterpret_cast<unsigned long long*>(d_stats), true, s));
+}
+
+tbe_status tbe_bounds_check_offsets(const tbe_problem* prob, const tbe_tables* tables, void* offsets,
+                                    void* ws, size_t ws_bytes, int64_t* d_stats, void* stream) {
+  Problem P;
+  tbe_status st = make_problem(prob, &P);
+  if (st != TBE_OK) return st;
+  if (!tables_ok(tables) || offsets == nullptr) return TBE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != TBE_OK) return st;
+  const int grid = bounds_grid(dev);
+  if (ws == nullptr || ws_bytes < sizeof(int64_t) * (1 + grid)) return TBE_ERR_WORKSPACE;
+  if (!aligned(ws, 8)) return TBE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch_bounds(P, *tables, nullptr, offsets, static_cast<int64_t*>(ws), grid,
+                                   reinterpret_cast<unsigned long long*>(d_stats), false, s));
 }
 
 size_t tbe_forward_workspace_size(const tbe_problem* prob, const tbe_options* opt) {
@@ -409,7 +425,7 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
   // contiguous table ranges.
   std::vector<int> hist;
   for (int t = 0; t < P.T; ++t)
-    if (!o.fused_bounds && hist_forward_eligible(P, o, t)) hist.push_back(t);
+    if (hist_forward_eligible(P, o, t)) hist.push_back(t);
   int t0 = 0;
   size_t h = 0;
   while (t0 < P.T) {
@@ -427,7 +443,8 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
   }
   record(o, TBE_FWD_EV_GATHER, s);
   for (int t : hist) {
-    cudaError_t e = launch_forward_histogram(P, *tables, weights, indices, offsets, out, t, stats, dev, s);
+    cudaError_t e = launch_forward_histogram(P, *tables, weights, indices, offsets, out, t, o.fused_bounds != 0,
+                                             stats, dev, s);
     if (e != cudaSuccess) return cuda_status(e);
   }
   record(o, TBE_FWD_EV_HISTOGRAM, s);

@@ -147,7 +147,7 @@ struct BwdCtx {
 // Launchers (one translation unit each group); all asynchronous on `s`
 // ------------------------------------------------------------------------------------------
 cudaError_t launch_bounds(const Problem& P, const tbe_tables& tab, void* indices, void* offsets,
-                          int64_t* ws, int grid, unsigned long long* stats, cudaStream_t s);
+                          int64_t* ws, int grid, unsigned long long* stats, bool with_ids, cudaStream_t s);
 int bounds_grid(const DeviceInfo& dev);
 
 cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const void* weights,
@@ -160,7 +160,8 @@ cudaError_t launch_backward_histogram(const Problem& P, const BwdCtx& c, int tab
                                       tbe_optimizer opt, const DeviceInfo& dev, cudaStream_t s);
 cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, const void* weights,
                                      const void* indices, const void* offsets, float* out, int table,
-                                     unsigned long long* stats, const DeviceInfo& dev, cudaStream_t s);
+                                     bool fused_bounds, unsigned long long* stats, const DeviceInfo& dev,
+                                     cudaStream_t s);
 
 cudaError_t launch_psw_gradient(const Problem& P, const tbe_tables& tab, const void* weights,
                                 const void* indices, const void* offsets, const float* grad_out,

@@ -41,6 +41,7 @@ EXPORTED = (
     "tbe_forward_workspace_size", "tbe_forward", "tbe_backward_workspace_size",
     "tbe_backward_update", "tbe_backward_metadata", "tbe_status_string", "tbe_version",
     "tbe_last_cuda_error", "tbe_backward_update_noalloc", "tbe_backward_prepare", "tbe_psw_gradient",
+    "tbe_bounds_check_offsets",
 )
 TBE_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -96,6 +97,7 @@ def load(path: str | None = None):
         lib.tbe_bounds_workspace_size.argtypes = [P]
         lib.tbe_bounds_workspace_size.restype = ctypes.c_size_t
         lib.tbe_bounds_check.argtypes = [P, T, vp, vp, vp, ctypes.c_size_t, vp, vp]
+        lib.tbe_bounds_check_offsets.argtypes = [P, T, vp, vp, ctypes.c_size_t, vp, vp]
         lib.tbe_forward_workspace_size.argtypes = [P, O]
         lib.tbe_forward_workspace_size.restype = ctypes.c_size_t
         lib.tbe_forward.argtypes = [P, O, T, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp, vp]
@@ -110,7 +112,8 @@ def load(path: str | None = None):
         lib.tbe_status_string.restype = ctypes.c_char_p
         lib.tbe_version.restype = ctypes.c_int
         lib.tbe_last_cuda_error.restype = ctypes.c_int
-        for name in ("tbe_table_layout", "tbe_bounds_check", "tbe_forward", "tbe_backward_update",
+        for name in ("tbe_table_layout", "tbe_bounds_check", "tbe_bounds_check_offsets", "tbe_forward",
+                     "tbe_backward_update",
                      "tbe_backward_prepare", "tbe_psw_gradient", "tbe_backward_metadata"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
@@ -244,9 +247,17 @@ class TableBatchedEmbedding:
             raise ValueError(f"{name} must have {numel} elements")
 
     # -- operations --------------------------------------------------------------------------
-    def bounds_check(self, indices, offsets, stats=None, stream=None):
+    def bounds_check(self, indices, offsets, stats=None, stream=None, offsets_only: bool = False):
+        """Repairs offsets and ids in place; offsets_only leaves the ids to a forward with
+        fused_bounds=1."""
         self._idx(indices, offsets)
         self._dev(stats, "stats", torch.int64, TBE_NUM_STATS)
+        if offsets_only:
+            st = self.lib.tbe_bounds_check_offsets(ctypes.byref(self.prob), ctypes.byref(self.tables), _ptr(offsets),
+                                                   _ptr(self.ws_bounds), self.ws_bounds.numel(), _ptr(stats),
+                                                   _stream(stream))
+            _check(self.lib, st, "tbe_bounds_check_offsets")
+            return
         st = self.lib.tbe_bounds_check(ctypes.byref(self.prob), ctypes.byref(self.tables), _ptr(indices),
                                        _ptr(offsets), _ptr(self.ws_bounds), self.ws_bounds.numel(),
                                        _ptr(stats), _stream(stream))

@@ -188,9 +188,16 @@ tbe_status tbe_bounds_check(const tbe_problem* prob, const tbe_tables* tables, v
                             void* offsets, void* ws, size_t ws_bytes, int64_t* d_stats,
                             void* stream);
 
-/* Pooled forward.  With opt->fused_bounds the kernel repairs out-of-range ids as it reads
- * them (writing 0 back into indices, so the backward sees the repaired id); without it the
- * ids must be valid (out-of-range ones are skipped and counted as TBE_STAT_UNREPAIRED).
+/* The offsets half of tbe_bounds_check alone, for callers whose tbe_forward repairs the ids in
+ * flight (opt->fused_bounds = 1; [FBT] section 2: "offset validation and repair remain a
+ * separate small kernel").  Same rule, workspace and counts as tbe_bounds_check. */
+tbe_status tbe_bounds_check_offsets(const tbe_problem* prob, const tbe_tables* tables, void* offsets,
+                                    void* ws, size_t ws_bytes, int64_t* d_stats, void* stream);
+
+/* Pooled forward.  With opt->fused_bounds the kernels (gather and counts x table) repair
+ * out-of-range ids as they read them (writing 0 back into indices, so the backward sees the
+ * repaired id, counted as TBE_STAT_BAD_INDICES); without it the ids must be valid (out-of-range
+ * ones are skipped and counted as TBE_STAT_UNREPAIRED).
  * Offsets must be non-decreasing (tbe_bounds_check makes them so); others are clamped so that
  * no read leaves the index array, and the bags they give are unspecified.  out: [B, sum D] fp32. */
 size_t tbe_forward_workspace_size(const tbe_problem* prob, const tbe_options* opt);

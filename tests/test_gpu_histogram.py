@@ -97,6 +97,24 @@ def test_histogram_backward_equals_sort_path():
     assert not bool(s_hist[torch.from_numpy(~touched).cuda()].any())
 
 
+def test_histogram_forward_repairs_ids_in_flight():
+    """fused_bounds on the counts x table path: out-of-range ids become row 0 (written back,
+    counted), including ids past the 256th of a bag (the scalar tail)."""
+    cfg = hist_config(64, 96, LengthSpec("poisson", 300.0), 300, bad=0.003, name="hist_fused")
+    c = Case(cfg, bounds_check=False)
+    n_bad = len(c.batch.bad_positions)
+    assert n_bad > 0
+    oracle.bounds_repair(c.tables, cfg.B, c.idx_h, c.off_h)
+    c.tbe.bounds_check(c.idx_d, c.off_d, stats=c.stats, offsets_only=True)
+    out = c.tbe.forward(c.w0.cuda(), c.idx_d, c.off_d, stats=c.stats, options=TBEOptions(fused_bounds=1))
+    torch.cuda.synchronize()
+    assert np.array_equal(c.idx_d.cpu().numpy(), c.idx_h)
+    assert c.stats[0].item() == n_bad
+    _, exact, absterms = oracle.forward(c.tables, cfg.B, weights_to_oracle(c.w0, cfg.wdtype), c.idx_h, c.off_h,
+                                        wdtype=cfg.wdtype)
+    check_forward(out.cpu().numpy(), exact, absterms, cfg.wdtype)
+
+
 def test_histogram_backward_counts_out_of_range_ids():
     cfg = hist_config(64, 128, LengthSpec("fixed", 256), 512, bad=0.002, name="hist_bad_bwd")
     c = Case(cfg, bounds_check=False)

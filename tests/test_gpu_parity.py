@@ -190,6 +190,24 @@ def test_fused_bounds_forward_repairs_in_flight():
     check_forward(out.cpu().numpy(), exact, absterms, cfg.wdtype)
 
 
+def test_offsets_only_bounds_check_then_fused_forward_and_backward():
+    """The split the pages describe: a small offsets kernel, ids repaired by the forward itself;
+    the backward then sees the repaired ids and matches the oracle on the repaired batch."""
+    cfg = SMALL["c5"]
+    c = Case(cfg, bounds_check=False)
+    oracle.bounds_repair(c.tables, cfg.B, c.idx_h, c.off_h)
+    c.tbe.bounds_check(c.idx_d, c.off_d, stats=c.stats, offsets_only=True)
+    opts = TBEOptions(fused_bounds=1)
+    out = c.tbe.forward(c.w0.cuda(), c.idx_d, c.off_d, psw=c.psw_d, stats=c.stats, options=opts)
+    torch.cuda.synchronize()
+    assert np.array_equal(c.idx_d.cpu().numpy(), c.idx_h) and np.array_equal(c.off_d.cpu().numpy(), c.off_h)
+    assert c.stats[0].item() == len(c.batch.bad_positions)
+    _, exact, absterms = oracle.forward(c.tables, cfg.B, weights_to_oracle(c.w0, cfg.wdtype), c.idx_h, c.off_h,
+                                        psw=c.psw_h, wdtype=cfg.wdtype)
+    check_forward(out.cpu().numpy(), exact, absterms, cfg.wdtype)
+    c.backward()
+
+
 def test_unrepaired_ids_are_skipped_not_dereferenced():
     cfg = SMALL["c5"]
     c = Case(cfg, bounds_check=False)
