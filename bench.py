@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--long-mode", choices=["auto", "two_kernel", "fused"], default="auto")
     ap.add_argument("--scheduler", choices=["grid", "persistent", "clc"], default="persistent")
     ap.add_argument("--merge", choices=["atomic", "bulk"], default="atomic")
+    ap.add_argument("--gather", choices=["register", "tma"], default="register",
+                    help="forward row gather: tma = tile::gather4 copies (equal-width 16-bit tables)")
     ap.add_argument("--pooling", choices=["sum", "mean"], default="sum")
     ap.add_argument("--bounds", choices=["fused", "separate"], default="fused",
                     help="fused: the offsets kernel, then the forward repairs ids as it reads them; "
@@ -368,6 +370,7 @@ def run_ours(args):
     opts = TBEOptions(long_mode={"auto": 0, "two_kernel": 1, "fused": 2}[args.long_mode],
                       scheduler={"grid": 0, "persistent": 1, "clc": 2}[args.scheduler],
                       merge={"atomic": 0, "bulk": 1}[args.merge],
+                      gather={"register": 0, "tma": 1}[args.gather],
                       fused_bounds=1 if args.bounds == "fused" else 0,
                       classify_mode={"atomic": 0, "ordered": 1}[args.classify])
     itype = torch.int32 if cfg.itype == "i32" else torch.int64
@@ -553,7 +556,7 @@ def run_ours(args):
                          + (" + (tbe_forward || tbe_backward_prepare) + tbe_backward_update(prepared)"
                             if args.hoist == "on" else " + tbe_forward + tbe_backward_update")
                          + (" (ids repaired inside tbe_forward)" if args.bounds == "fused" else "")),
-                "long_mode": args.long_mode, "scheduler": args.scheduler, "merge": args.merge, "classify": args.classify,
+                "long_mode": args.long_mode, "scheduler": args.scheduler, "merge": args.merge, "gather": args.gather, "classify": args.classify,
                 "transpose": "hoisted beside the forward (second stream)" if args.hoist == "on" else "in the backward",
                 "pooling": args.pooling, "psw_grad": bool(psw_grad),
                 "parallelism": f"replicas x{world}",

@@ -27,6 +27,13 @@
 // derivative of bag (t, b)'s pooled row with respect to psw[p] is W_t[idx[p]] (over L for mean
 // pooling), so grad_psw[p] = <grad_out[b, table's columns], W_t[idx[p]]>; each lane holds its
 // slice of the bag's gradient row and the row's dot product replaces its sum.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -44,6 +51,7 @@ struct FwdArgs {
   int64_t B;
   int64_t num_indices;
   int64_t unit_begin, unit_end;
+  int64_t item_base;  // the launch's first work item
   int bags_per_item;  // 1..32
   int mean;           // mean pooling: the sum over the bag length (an empty bag stays 0)
   // dot mode (the gradient with respect to the per-sample weights): grad_out rows in, one fp32
@@ -54,6 +62,12 @@ struct FwdArgs {
   int fused_bounds;
   unsigned long long* stats;
 };
+
+// The bytes of a CUtensorMap (a kernel parameter: 128 bytes, 64-byte aligned).
+struct alignas(64) TmaMap {
+  uint64_t w[16];
+};
+static_assert(sizeof(TmaMap) == sizeof(CUtensorMap), "tensor map size");
 
 __device__ __forceinline__ int next_pow2_int(int v) { return v <= 1 ? 1 : 1 << (32 - __clz(v - 1)); }
 
@@ -142,8 +156,18 @@ __device__ __forceinline__ IdWindow<PSW> load_window(const FwdArgs& a, int pos, 
 // DOT = the gradient with respect to the per-sample weights: the same walk over bags, windows and
 // rows, but each lane keeps its slice of the bag's gradient row and every row is dotted into it
 // (reduced within its row group) instead of being summed.
+// Threads per CTA, and resident CTAs per SM for a 256-thread block (scaled to the block size).
+// Two-warp CTAs: a CTA's slot frees as soon as its two items are done, so items of uneven
+// length leave few warp slots idle (83.9M-lookup stress batch: 2.37 ms with 8-warp CTAs,
+// 2.21 ms with 2-warp CTAs, 2.25 ms with 1-warp CTAs).
+constexpr int kGatherThreads = 64;
+template <typename WT, int MAXV>
+constexpr int gather_min_blocks() {
+  return (MAXV == 1 ? (sizeof(WT) == 4 ? 3 : 4) : (MAXV == 2 ? 2 : 1)) * (256 / kGatherThreads);
+}
+
 template <typename WT, typename IT, bool PSW, int VB, int MAXV, int UNROLL, bool DOT>
-__global__ void __launch_bounds__(256, MAXV == 1 ? (sizeof(WT) == 4 ? 3 : 4) : (MAXV == 2 ? 2 : 1))
+__global__ void __launch_bounds__(kGatherThreads, gather_min_blocks<WT, MAXV>())
 fwd_gather_kernel(FwdArgs a) {
   using IO = VecIO<WT, VB>;
   using Raw = typename IO::Raw;
@@ -151,15 +175,14 @@ fwd_gather_kernel(FwdArgs a) {
   constexpr int NE = IO::N;  // weight elements per vector
   const unsigned FULL = 0xffffffffu;
   const int lane = lane_id();
-  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int K = a.bags_per_item;
   const int64_t items_per_table = (a.B + K - 1) / K;
   const int t_begin = static_cast<int>(a.unit_begin / a.B);
   const int64_t items = static_cast<int64_t>(a.unit_end / a.B - t_begin) * items_per_table;
   const int N = static_cast<int>(a.num_indices);
-
-  for (int64_t g = warp0; g < items; g += nwarps) {
+  // one work item per warp
+  const int64_t g = a.item_base + ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  if (g < items) {
     const int t = t_begin + static_cast<int>(g / items_per_table);
     const int64_t b0 = (g % items_per_table) * K;
     const int nb = static_cast<int>(min(static_cast<int64_t>(K), a.B - b0));
@@ -242,39 +265,43 @@ fwd_gather_kernel(FwdArgs a) {
         const int32_t idb = __shfl_sync(FULL, wb.id, rel & (kWarp - 1));
         const int n = min(kWarp, e - c0);
         const int32_t my_id = lane < n ? (rel < kWarp ? ida : idb) : -1;
-        float my_w = 1.0f;
+        float my_w = 0.0f;  // 0 where no row is read, so a zero vector is never scaled by inf
         if (PSW) {
           const float pa = __shfl_sync(FULL, wa.w, rel & (kWarp - 1));
           const float pb = __shfl_sync(FULL, wb.w, rel & (kWarp - 1));
-          my_w = rel < kWarp ? pa : pb;
+          if (my_id >= 0) my_w = rel < kWarp ? pa : pb;
         }
         const bool chunk_ok = __all_sync(FULL, lane >= n || my_id >= 0);  // no skipped id
         for (int j = 0; j < n; j += rps * qmax) {
           Raw v[UNROLL][MAXV];
-          float w[UNROLL];
-          if (chunk_ok && qmax == UNROLL && j + rps * UNROLL <= n) {
+          int nq = UNROLL;  // load steps of this batch that hold a row (warp-uniform)
+          const bool full = chunk_ok && qmax == UNROLL && j + rps * UNROLL <= n;
+          if (full) {
             // every row of the batch is valid: unpredicated loads
 #pragma unroll
             for (int q = 0; q < UNROLL; ++q) {
               const int r = j + q * rps + slot;
               const int32_t id = __shfl_sync(FULL, my_id, r);
-              w[q] = PSW ? __shfl_sync(FULL, my_w, r) : 1.0f;
               const Raw* row = table + static_cast<int64_t>(id) * nvec;
 #pragma unroll
               for (int m = 0; m < MAXV; ++m) v[q][m] = ldg_raw(row + vk[m]);
             }
           } else {
+            // the bag's last rows (or a batch with a skipped id): only the load steps that hold a
+            // row are issued and summed
+            nq = min(qmax, (n - j + rps - 1) / rps);
 #pragma unroll
             for (int q = 0; q < UNROLL; ++q) {
-              const int r = j + q * rps + slot;  // < 64; lanes past n hold -1
-              const int32_t id = __shfl_sync(FULL, my_id, r & (kWarp - 1));
-              w[q] = PSW ? __shfl_sync(FULL, my_w, r & (kWarp - 1)) : 1.0f;
-              const bool ok = q < qmax && r < n && id >= 0;
-              const Raw* row = table + static_cast<int64_t>(ok ? id : 0) * nvec;
 #pragma unroll
-              for (int m = 0; m < MAXV; ++m) {
-                if (ok && vi + m * kWarp < nvec) v[q][m] = ldg_raw(row + vk[m]);
-                else v[q][m] = Raw{};
+              for (int m = 0; m < MAXV; ++m) v[q][m] = Raw{};
+              if (q < nq) {
+                const int r = j + q * rps + slot;  // < 64; lanes past n hold -1
+                const int32_t id = __shfl_sync(FULL, my_id, r & (kWarp - 1));
+                const bool ok = r < n && id >= 0;
+                const Raw* row = table + static_cast<int64_t>(ok ? id : 0) * nvec;
+#pragma unroll
+                for (int m = 0; m < MAXV; ++m)
+                  if (ok && vi + m * kWarp < nvec) v[q][m] = ldg_raw(row + vk[m]);
               }
             }
           }
@@ -317,42 +344,295 @@ fwd_gather_kernel(FwdArgs a) {
                 if (vi == 0 && q < qmax && r < n) a.grad_psw[c0 + r] = static_cast<float>(d * inv_len);
               }
             }
+          } else if (full) {
+            // the weights are fetched here, after the loads, so they hold no registers meanwhile
+#pragma unroll
+            for (int q = 0; q < UNROLL; ++q) {
+              const float wq = PSW ? __shfl_sync(FULL, my_w, j + q * rps + slot) : 1.0f;
+#pragma unroll
+              for (int m = 0; m < MAXV; ++m) accumulate<WT, VB, PSW>(acc[m], v[q][m], wq);
+            }
           } else {
 #pragma unroll
-            for (int q = 0; q < UNROLL; ++q)
+            for (int q = 0; q < UNROLL; ++q) {
+              if (q < nq) {
+                float wq = 1.0f;
+                if (PSW) {
+                  const int r = j + q * rps + slot;
+                  wq = __shfl_sync(FULL, my_w, r & (kWarp - 1));
+                  if (r >= n) wq = 0.0f;  // a row past the bag: its vector is zero
+                }
 #pragma unroll
-              for (int m = 0; m < MAXV; ++m) accumulate<WT, VB, PSW>(acc[m], v[q][m], w[q]);
+                for (int m = 0; m < MAXV; ++m) accumulate<WT, VB, PSW>(acc[m], v[q][m], wq);
+              }
+            }
           }
         }
       }
-      if constexpr (DOT) continue;  // no pooled row
-      // reduce the row groups of the warp (lanes that share vi)
-      for (int m = lpr; m < kWarp; m <<= 1) {
+      if constexpr (!DOT) {  // dot mode has no pooled row
+        // reduce the row groups of the warp (lanes that share vi)
+        for (int m = lpr; m < kWarp; m <<= 1) {
 #pragma unroll
-        for (int x = 0; x < MAXV; ++x)
+          for (int x = 0; x < MAXV; ++x)
 #pragma unroll
-          for (int i = 0; i < NE; ++i) acc[x][i] += __shfl_xor_sync(FULL, acc[x][i], m);
-      }
-      if (a.mean && e > s) {
+            for (int i = 0; i < NE; ++i) acc[x][i] += __shfl_xor_sync(FULL, acc[x][i], m);
+        }
+        if (a.mean && e > s) {
 #pragma unroll
-        for (int x = 0; x < MAXV; ++x)
+          for (int x = 0; x < MAXV; ++x)
 #pragma unroll
-          for (int i = 0; i < NE; ++i) acc[x][i] /= static_cast<Acc>(e - s);
-      }
-      if (slot == 0) {
+            for (int i = 0; i < NE; ++i) acc[x][i] /= static_cast<Acc>(e - s);
+        }
+        if (slot == 0) {
 #pragma unroll
-        for (int x = 0; x < MAXV; ++x) {
-          if (vi + x * kWarp < nvec) {
-            float o[NE];
+          for (int x = 0; x < MAXV; ++x) {
+            if (vi + x * kWarp < nvec) {
+              float o[NE];
 #pragma unroll
-            for (int i = 0; i < NE; ++i) o[i] = static_cast<float>(acc[x][i]);
-            store_out(orow + x * kWarp * NE, o);
+              for (int i = 0; i < NE; ++i) o[i] = static_cast<float>(acc[x][i]);
+              store_out(orow + x * kWarp * NE, o);
+            }
           }
         }
+        orow += a.total_D;
       }
-      orow += a.total_D;
     }
   }
+}
+
+// ------------------------------------------------------------------------------------------
+// Row gather through the tensor memory accelerator (sm_100+): every table has the same width,
+// so the packed weights are one [sum E, D] matrix and a tile::gather4 copy brings four of its
+// rows (any four row numbers) into shared memory, completion counted in bytes on an mbarrier.
+// A warp owns a work item of up to 32 consecutive bags, as in the register gather, and streams
+// the item's lookups through a ring of kTmaStages four-row stages: lane 0 keeps the ring full
+// (row numbers come from the same 32-position id windows, prefetched one window ahead), and
+// the warp sums each row out of shared memory into the bag's fp32 accumulator, one row per
+// step with each lane owning D/32 columns, so a finished bag needs no cross-lane reduction:
+// the warp stores it as one coalesced row.  Up to 4 x kTmaStages rows per warp are in flight
+// without holding registers (the register gather holds 8).  It is the TBE_GATHER_TMA option:
+// on the 83.9M-lookup stress batch (256-byte rows) it takes 4.0 ms against 2.2 ms for the
+// register gather.
+// Items whose offsets do not tile their span (possible only when the offsets were not
+// repaired) take a plain per-bag loop instead.
+// ------------------------------------------------------------------------------------------
+constexpr int kTmaThreads = 64;
+constexpr int kTmaWarps = kTmaThreads / kWarp;
+constexpr int kTmaStages = 6;
+constexpr uint32_t kTmaWaitLimit = 1u << 22;
+
+__device__ __forceinline__ void tma_gather4(void* dst, const TmaMap* map, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <typename WT, int VB>
+__device__ __forceinline__ typename VecIO<WT, VB>::Raw lds_raw(const uint8_t* p) {
+  return *reinterpret_cast<const typename VecIO<WT, VB>::Raw*>(p);
+}
+
+// One bag's fp32 sums (NE columns per lane) to its output row; mean pooling divides by L.
+template <int NE>
+__device__ __forceinline__ void store_bag(float* orow, float (&acc)[NE], int len, bool mean) {
+  if (mean && len > 0) {
+#pragma unroll
+    for (int i = 0; i < NE; ++i) acc[i] /= static_cast<float>(len);
+  }
+  if constexpr (NE == 2) {
+    __stcs(reinterpret_cast<float2*>(orow), make_float2(acc[0], acc[1]));
+  } else {
+    store_out(orow, acc);
+  }
+#pragma unroll
+  for (int i = 0; i < NE; ++i) acc[i] = 0.0f;
+}
+
+template <typename WT, typename IT, bool PSW, int VB>
+__global__ void __launch_bounds__(kTmaThreads, 16) fwd_tma_gather_kernel(const __grid_constant__ TmaMap tmap,
+                                                                          FwdArgs a) {
+  using IO = VecIO<WT, VB>;
+  using Raw = typename IO::Raw;
+  constexpr int NE = IO::N;          // columns per lane
+  constexpr int RB = VB * kWarp;     // bytes per row (D = 32 * NE)
+  constexpr int SB = 4 * RB;         // bytes per stage
+  constexpr int S = kTmaStages;
+  const unsigned FULL = 0xffffffffu;
+  extern __shared__ __align__(128) uint8_t s_ring[];  // [warp][stage][4 rows]
+  __shared__ __align__(8) uint64_t s_bar[kTmaWarps][S];
+  __shared__ float s_scale[kTmaWarps][S][4];  // per row: psw (weighted) or 1
+  __shared__ int s_mask[kTmaWarps][S];        // bit j: row j of the stage is a lookup to add
+  const int lane = lane_id(), wl = threadIdx.x / kWarp;
+  uint8_t* ring = s_ring + wl * S * SB;
+  uint64_t* bar = s_bar[wl];
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  const int K = a.bags_per_item;
+  const int64_t items_per_table = (a.B + K - 1) / K;
+  const int t_begin = static_cast<int>(a.unit_begin / a.B);
+  const int64_t items = static_cast<int64_t>(a.unit_end / a.B - t_begin) * items_per_table;
+  const int N = static_cast<int>(a.num_indices);
+  const int64_t g = a.item_base + ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  if (g >= items) return;
+  const int t = t_begin + static_cast<int>(g / items_per_table);
+  const int64_t b0 = (g % items_per_table) * K;
+  const int nb = static_cast<int>(min(static_cast<int64_t>(K), a.B - b0));
+  const int64_t u0 = static_cast<int64_t>(t) * a.B + b0;
+  const int col0 = __ldg(a.doff + t);
+  const int64_t rbase64 = __ldg(a.roff + t);
+  const int E = static_cast<int>(__ldg(a.roff + t + 1) - rbase64);  // < 2^31
+  const int rbase = static_cast<int>(rbase64);                     // sum E < 2^31
+  float* orow0 = a.out + b0 * a.total_D + col0 + lane * NE;
+  const bool mean = a.mean != 0;
+
+  int off_s = 0, off_e = 0;
+  if (lane < nb) {
+    off_s = static_cast<int>(clamp64(ld_int<IT>(a.offsets, u0 + lane), 0, N));
+    off_e = static_cast<int>(clamp64(ld_int<IT>(a.offsets, u0 + lane + 1), off_s, N));
+  }
+  int lo = lane < nb ? off_s : N, hi = off_e;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    lo = min(lo, __shfl_xor_sync(FULL, lo, m));
+    hi = max(hi, __shfl_xor_sync(FULL, hi, m));
+  }
+  // do the bags tile [lo, hi) in order (always, once the offsets are repaired)?
+  const int next_s = __shfl_down_sync(FULL, off_s, 1);
+  const bool tiles = __all_sync(FULL, lane >= nb - 1 || off_e == next_s);
+  float acc[NE];
+#pragma unroll
+  for (int i = 0; i < NE; ++i) acc[i] = 0.0f;
+
+  if (!tiles) {
+    // plain per-bag walk: ids through one window per 32 positions, rows by direct loads
+    const Raw* table = reinterpret_cast<const Raw*>(static_cast<const WT*>(a.weights) + __ldg(a.woff + t));
+    for (int k = 0; k < nb; ++k) {
+      const int s = __shfl_sync(FULL, off_s, k), e = __shfl_sync(FULL, off_e, k);
+      for (int c0 = s; c0 < e; c0 += kWarp) {
+        const IdWindow<PSW> w = load_window<IT, PSW>(a, c0 + lane, s, e, E);
+        const int n = min(kWarp, e - c0);
+        for (int r = 0; r < n; ++r) {
+          const int32_t id = __shfl_sync(FULL, w.id, r);
+          const float wr = PSW ? __shfl_sync(FULL, w.w, r) : 1.0f;
+          if (id >= 0) accumulate<WT, VB, PSW>(acc, ldg_raw(table + static_cast<int64_t>(id) * kWarp + lane), wr);
+        }
+      }
+      store_bag<NE>(orow0 + static_cast<int64_t>(k) * a.total_D, acc, e - s, mean);
+    }
+    return;
+  }
+
+  // producer: stage i holds positions lo + 4i .. lo + 4i + 3 (rows past hi or of skipped ids
+  // are fetched from the table's row 0 and left out of the sums)
+  const int nst = (hi - lo + 3) >> 2;
+  int pw = lo;  // window `cur` holds positions pw .. pw + 31, `nxt` the 32 after them
+  IdWindow<PSW> cur = load_window<IT, PSW>(a, pw + lane, lo, hi, E);
+  IdWindow<PSW> nxt = load_window<IT, PSW>(a, pw + kWarp + lane, lo, hi, E);
+  int issued = 0;
+  auto issue = [&]() {
+    const int r = lo + 4 * issued - pw;  // 0, 4, .., 28
+    int row[4];
+    float sc[4];
+    int mask = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int32_t id = __shfl_sync(FULL, cur.id, r + j);
+      sc[j] = PSW ? __shfl_sync(FULL, cur.w, r + j) : 1.0f;
+      const bool ok = lo + 4 * issued + j < hi && id >= 0;
+      row[j] = rbase + (ok ? id : 0);
+      mask |= ok ? 1 << j : 0;
+    }
+    const int slot = issued % S;
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s_scale[wl][slot][j] = sc[j];
+      s_mask[wl][slot] = mask;
+      fence_proxy_async_smem();  // the slot's earlier reads before the copy overwrites it
+      mbar_arrive_expect_tx(&bar[slot], SB);
+      tma_gather4(ring + slot * SB, &tmap, row[0], row[1], row[2], row[3], &bar[slot]);
+    }
+    ++issued;
+    if (r + 4 == kWarp) {
+      cur = nxt;
+      pw += kWarp;
+      nxt = load_window<IT, PSW>(a, pw + kWarp + lane, lo, hi, E);
+    }
+  };
+
+  // bags before the first row (empty ones) are written as zeros
+  int k = 0;
+  int s_k = __shfl_sync(FULL, off_s, 0), e_k = __shfl_sync(FULL, off_e, 0);
+  while (k < nb && e_k == s_k) {
+    store_bag<NE>(orow0 + static_cast<int64_t>(k) * a.total_D, acc, 0, mean);
+    ++k;
+    if (k < nb) {
+      s_k = __shfl_sync(FULL, off_s, k);
+      e_k = __shfl_sync(FULL, off_e, k);
+    }
+  }
+  while (issued < nst && issued < S) issue();
+  __syncwarp();
+
+  bool failed = false;
+  int i = 0;
+  for (; i < nst; ++i) {
+    const int slot = i % S;
+    if (!mbar_wait_bounded(&bar[slot], (i / S) & 1, kTmaWaitLimit)) {
+      failed = true;
+      if (lane == 0) stat_add(a.stats, TBE_STAT_WAIT_TIMEOUT, 1);
+      break;
+    }
+    const uint8_t* st = ring + slot * SB + lane * VB;
+    const int p0 = lo + 4 * i;
+    const int n = min(4, hi - p0);
+    Raw v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = j < n ? lds_raw<WT, VB>(st + j * RB) : Raw{};
+    const int mask = s_mask[wl][slot];
+    const bool plain = !PSW && mask == 0xF;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j < n) {
+        if (plain) accumulate<WT, VB, false>(acc, v[j], 1.0f);
+        else if (mask & (1 << j)) accumulate<WT, VB, PSW>(acc, v[j], s_scale[wl][slot][j]);
+        if (p0 + j + 1 == e_k) {  // bag k ends at this row; empty bags after it are written too
+          store_bag<NE>(orow0 + static_cast<int64_t>(k) * a.total_D, acc, e_k - s_k, mean);
+          ++k;
+          while (k < nb) {
+            s_k = __shfl_sync(FULL, off_s, k);
+            e_k = __shfl_sync(FULL, off_e, k);
+            if (e_k > s_k) break;
+            store_bag<NE>(orow0 + static_cast<int64_t>(k) * a.total_D, acc, 0, mean);
+            ++k;
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane has read the slot
+    if (issued < nst) {
+      issue();
+      __syncwarp();
+    }
+  }
+  if (failed) {
+    // a copy that never signalled: wait once more (bounded) for every stage still in flight
+    // before the warp's shared memory can be released
+    for (int q = i; q < issued; ++q) mbar_wait_bounded(&bar[q % S], (q / S) & 1, kTmaWaitLimit);
+  }
+}
+
+// Bags per work item: about eight items per resident warp, at most 32 bags each.
+inline int bags_per_item_for(int64_t tables, int64_t B, int64_t warps) {
+  const int64_t per_item = tables * B / (8 * warps);
+  return per_item < 1 ? 1 : (per_item > kWarp ? kWarp : static_cast<int>(per_item));
 }
 
 template <typename WT, typename IT, bool PSW, int VB, int MAXV>
@@ -361,22 +641,97 @@ cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   // the gradient with respect to psw does not read psw: it runs the unweighted walk in DOT mode
   auto k = a.grad_psw != nullptr ? fwd_gather_kernel<WT, IT, false, VB, MAXV, UNROLL, true>
                                  : fwd_gather_kernel<WT, IT, PSW, VB, MAXV, UNROLL, false>;
-  const int threads = 256;
+  const int threads = kGatherThreads;
   const int64_t tables = (a.unit_end - a.unit_begin) / a.B;
   const int64_t warps = static_cast<int64_t>(persistent_grid(k, threads, 0, dev, INT64_MAX)) * (threads / kWarp);
   // about eight items per warp, at most 32 bags per item
   FwdArgs ak = a;
-  const int64_t per_item = tables * a.B / (8 * warps);
-  ak.bags_per_item = per_item < 1 ? 1 : (per_item > kWarp ? kWarp : static_cast<int>(per_item));
+  ak.bags_per_item = bags_per_item_for(tables, a.B, warps);
   const int64_t items = tables * ((a.B + ak.bags_per_item - 1) / ak.bags_per_item);
   // One item per warp: CTAs retire as their items finish and the block scheduler hands the SM
   // to the next one, which balances items of uneven length better than a resident grid-stride
-  // loop (the loop stays for grids past the launch limit).
-  const int64_t want = (items + (threads / kWarp) - 1) / (threads / kWarp);
-  const int grid = static_cast<int>(want < 0x7fffffff ? want : 0x7fffffff);
-  k<<<grid, threads, 0, s>>>(ak);
-  note_launch();
+  // loop.  Past the launch's grid limit the items go out in several launches.
+  constexpr int64_t kMaxGrid = 0x7fffffff;
+  const int64_t per_launch = kMaxGrid * (threads / kWarp);
+  for (int64_t base = 0; base < items; base += per_launch) {
+    const int64_t n = items - base < per_launch ? items - base : per_launch;
+    ak.item_base = base;
+    k<<<static_cast<unsigned>((n + (threads / kWarp) - 1) / (threads / kWarp)), threads, 0, s>>>(ak);
+    note_launch();
+  }
   return cudaGetLastError();
+}
+
+template <typename WT, typename IT, bool PSW, int VB>
+cudaError_t launch_tma_t(const FwdArgs& a, const TmaMap& map, const DeviceInfo& dev, cudaStream_t s) {
+  auto k = fwd_tma_gather_kernel<WT, IT, PSW, VB>;
+  const size_t smem = static_cast<size_t>(kTmaWarps) * kTmaStages * 4 * VB * kWarp;
+  if (smem > 48 * 1024) {
+    static std::atomic<uint64_t> attr_set{0};
+    const uint64_t bit = uint64_t(1) << (dev.id & 63);
+    if ((attr_set.load() & bit) == 0) {
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      attr_set.fetch_or(bit);
+    }
+  }
+  const int64_t tables = (a.unit_end - a.unit_begin) / a.B;
+  const int64_t warps = static_cast<int64_t>(persistent_grid(k, kTmaThreads, smem, dev, INT64_MAX)) * kTmaWarps;
+  FwdArgs ak = a;
+  ak.bags_per_item = bags_per_item_for(tables, a.B, warps);
+  const int64_t items = tables * ((a.B + ak.bags_per_item - 1) / ak.bags_per_item);
+  constexpr int64_t kMaxGrid = 0x7fffffff;
+  const int64_t per_launch = kMaxGrid * kTmaWarps;
+  for (int64_t base = 0; base < items; base += per_launch) {
+    const int64_t n = items - base < per_launch ? items - base : per_launch;
+    ak.item_base = base;
+    k<<<static_cast<unsigned>((n + kTmaWarps - 1) / kTmaWarps), kTmaThreads, smem, s>>>(map, ak);
+    note_launch();
+  }
+  return cudaGetLastError();
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The packed weights of equal-width tables as one [rows, D] matrix of 16-bit elements whose
+// copy box is one row: the tensor map of the tile::gather4 loads.
+bool encode_row_map(TmaMap* out, const void* weights, int64_t rows, int D, int wdtype) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return false;
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(D), 1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(&m, wdtype == TBE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                            2, const_cast<void*>(weights), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::memcpy(out, &m, sizeof(m));
+  return true;
+}
+
+template <typename WT, typename IT, bool PSW>
+cudaError_t dispatch_tma(const FwdArgs& a, const TmaMap& map, int D, const DeviceInfo& dev, cudaStream_t s) {
+  switch (D) {
+    case 64: return launch_tma_t<WT, IT, PSW, 4>(a, map, dev, s);
+    case 128: return launch_tma_t<WT, IT, PSW, 8>(a, map, dev, s);
+    default: return launch_tma_t<WT, IT, PSW, 16>(a, map, dev, s);
+  }
 }
 
 template <typename WT, typename IT, bool PSW, int VB>
@@ -412,9 +767,18 @@ cudaError_t dispatch_it(const FwdArgs& a, int itype, bool psw, int vb, int maxv,
 
 }  // namespace
 
+// The TMA row gather takes 16-bit tables of one width D in {64, 128, 256} (the packed weights
+// are then one [sum E, D] matrix; a row is 32 lanes x D/32 elements).
+bool tma_gather_eligible(const Problem& P) {
+  if (P.wbytes != 2 || P.T == 0) return false;
+  for (int t = 0; t < P.T; ++t)
+    if (P.D[t] != P.max_D) return false;
+  return P.max_D == 64 || P.max_D == 128 || P.max_D == 256;
+}
+
 cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const void* weights,
                                   void* indices, const void* offsets, const float* psw, float* out,
-                                  int64_t unit_begin, int64_t unit_end, bool fused_bounds,
+                                  int64_t unit_begin, int64_t unit_end, bool fused_bounds, bool allow_tma,
                                   unsigned long long* stats, const DeviceInfo& dev, cudaStream_t s) {
   if (unit_end <= unit_begin) return cudaSuccess;
   FwdArgs a;
@@ -429,6 +793,7 @@ cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const
   a.B = P.B;
   a.num_indices = P.num_indices;
   a.unit_begin = unit_begin;
+  a.item_base = 0;
   a.unit_end = unit_end;
   a.total_D = P.total_D;
   a.fused_bounds = fused_bounds ? 1 : 0;
@@ -436,12 +801,29 @@ cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const
   a.grad = nullptr;
   a.grad_psw = nullptr;
   a.stats = stats;
+  const bool has_psw = psw != nullptr;
+  if (allow_tma && tma_gather_eligible(P)) {
+    TmaMap map;
+    if (encode_row_map(&map, weights, P.total_rows, P.max_D, P.wdtype)) {
+      if (P.wdtype == TBE_F16) {
+        if (P.itype == TBE_I32)
+          return has_psw ? dispatch_tma<__half, int32_t, true>(a, map, P.max_D, dev, s)
+                         : dispatch_tma<__half, int32_t, false>(a, map, P.max_D, dev, s);
+        return has_psw ? dispatch_tma<__half, int64_t, true>(a, map, P.max_D, dev, s)
+                       : dispatch_tma<__half, int64_t, false>(a, map, P.max_D, dev, s);
+      }
+      if (P.itype == TBE_I32)
+        return has_psw ? dispatch_tma<__nv_bfloat16, int32_t, true>(a, map, P.max_D, dev, s)
+                       : dispatch_tma<__nv_bfloat16, int32_t, false>(a, map, P.max_D, dev, s);
+      return has_psw ? dispatch_tma<__nv_bfloat16, int64_t, true>(a, map, P.max_D, dev, s)
+                     : dispatch_tma<__nv_bfloat16, int64_t, false>(a, map, P.max_D, dev, s);
+    }
+  }
   const int vb = P.vec_bytes;
   const int ne = vb / P.wbytes;
   const int max_nvec = P.max_D / ne;
   int maxv = (max_nvec + kWarp - 1) / kWarp;
   maxv = maxv <= 1 ? 1 : (maxv <= 2 ? 2 : (maxv <= 4 ? 4 : 8));
-  const bool has_psw = psw != nullptr;
   switch (P.wdtype) {
     case TBE_F32: return dispatch_it<float>(a, P.itype, has_psw, vb, maxv, dev, s);
     case TBE_F16: return dispatch_it<__half>(a, P.itype, has_psw, vb, maxv, dev, s);
@@ -467,6 +849,7 @@ cudaError_t launch_psw_gradient(const Problem& P, const tbe_tables& tab, const v
   a.B = P.B;
   a.num_indices = P.num_indices;
   a.unit_begin = 0;
+  a.item_base = 0;
   a.unit_end = P.TB;
   a.total_D = P.total_D;
   a.fused_bounds = 0;

@@ -13,8 +13,9 @@
 //               coalesced; each lookup finds its bag by binary search over the CTA's offsets in
 //               shared memory and writes key = row_offsets[t] + id (uint32) and its bag b
 //               (plus its per-sample weight when weighted).
-//   radix sort  LSD, 8-bit digits, as many passes as the key range needs (ceil(bits/8), the
-//               range being sum E + 1 for an out-of-range sentinel).  Each pass is
+//   radix sort  LSD, digits of 8 to 10 bits, as few passes as the key range allows
+//               (ceil(bits/10), the range being sum E + 1 for an out-of-range sentinel), the
+//               narrower digits first.  Each pass is
 //               reduce-then-scan: a per-CTA digit histogram over a contiguous segment, one
 //               exclusive scan of the [digit][CTA] counts, and a stable scatter in which each
 //               CTA walks its segment in 4096-key tiles, ranks keys with warp-level match
@@ -579,8 +580,11 @@ cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+namespace {
+
+// One LSD pass over digit [shift, shift + RB) of the keys in buffer `cur` into buffer cur ^ 1.
 template <int RB>
-cudaError_t launch_sort_rb(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s) {
+cudaError_t sort_pass(const Problem& P, const BwdCtx& c, const BwdLayout& L, int cur, int shift, cudaStream_t s) {
   const bool psw = P.scaled;
   const size_t smem = downsweep_smem_bytes(RB, psw);
   // the opt-in shared memory size is a per-device function attribute: set it once per device
@@ -598,33 +602,38 @@ cudaError_t launch_sort_rb(const Problem& P, const BwdCtx& c, const BwdLayout& L
     attr_set[psw ? 1 : 0].fetch_or(bit);
   }
   const int G = L.sort_grid;
-  int cur = 0;
-  for (int pass = 0; pass < L.passes; ++pass) {
-    const int shift = pass * RB;
-    radix_upsweep_kernel<RB><<<G, kThreads, 0, s>>>(c.keys[cur], c.counters, shift, c.sort_counts, G);
-    note_launch();
-    digit_scan_kernel<<<1 << RB, kThreads, 0, s>>>(c.sort_counts, c.sort_totals, G);
-    note_launch();
-    if (psw)
-      radix_downsweep_kernel<RB, true><<<G, kThreads, smem, s>>>(
-          c.keys[cur], c.vals[cur], c.pswbuf[cur], c.keys[cur ^ 1], c.vals[cur ^ 1], c.pswbuf[cur ^ 1],
-          c.counters, c.sort_counts, c.sort_totals, shift, G, c.stats);
-    else
-      radix_downsweep_kernel<RB, false><<<G, kThreads, smem, s>>>(
-          c.keys[cur], c.vals[cur], nullptr, c.keys[cur ^ 1], c.vals[cur ^ 1], nullptr, c.counters,
-          c.sort_counts, c.sort_totals, shift, G, c.stats);
-    note_launch();
-    cur ^= 1;
-  }
+  radix_upsweep_kernel<RB><<<G, kThreads, 0, s>>>(c.keys[cur], c.counters, shift, c.sort_counts, G);
+  note_launch();
+  digit_scan_kernel<<<1 << RB, kThreads, 0, s>>>(c.sort_counts, c.sort_totals, G);
+  note_launch();
+  if (psw)
+    radix_downsweep_kernel<RB, true><<<G, kThreads, smem, s>>>(
+        c.keys[cur], c.vals[cur], c.pswbuf[cur], c.keys[cur ^ 1], c.vals[cur ^ 1], c.pswbuf[cur ^ 1],
+        c.counters, c.sort_counts, c.sort_totals, shift, G, c.stats);
+  else
+    radix_downsweep_kernel<RB, false><<<G, kThreads, smem, s>>>(
+        c.keys[cur], c.vals[cur], nullptr, c.keys[cur ^ 1], c.vals[cur ^ 1], nullptr, c.counters,
+        c.sort_counts, c.sort_totals, shift, G, c.stats);
+  note_launch();
   return cudaGetLastError();
 }
 
+}  // namespace
+
 cudaError_t launch_sort(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s) {
-  switch (L.radix_bits) {
-    case 8: return launch_sort_rb<8>(P, c, L, s);
-    case 9: return launch_sort_rb<9>(P, c, L, s);
-    default: return launch_sort_rb<10>(P, c, L, s);
+  int cur = 0, shift = 0;
+  for (int pass = 0; pass < L.passes; ++pass) {
+    cudaError_t e;
+    switch (L.pass_bits[pass]) {
+      case 8: e = sort_pass<8>(P, c, L, cur, shift, s); break;
+      case 9: e = sort_pass<9>(P, c, L, cur, shift, s); break;
+      default: e = sort_pass<10>(P, c, L, cur, shift, s); break;
+    }
+    if (e != cudaSuccess) return e;
+    shift += L.pass_bits[pass];
+    cur ^= 1;
   }
+  return cudaSuccess;
 }
 
 cudaError_t launch_rle(const Problem& P, const BwdCtx& c, const BwdLayout& L, cudaStream_t s) {

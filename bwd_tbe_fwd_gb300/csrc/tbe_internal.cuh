@@ -23,6 +23,7 @@ constexpr int kSortThreads = 256;
 constexpr int kSortItems = 16;
 constexpr int kSortTile = kSortThreads * kSortItems;  // keys per radix-sort tile
 constexpr int kMaxRadixBits = 10;                     // digits of 8..10 bits: passes = ceil(bits/10)
+constexpr int kMaxRadixPasses = 4;                    // 32-bit keys
 constexpr int kMaxRadix = 1 << kMaxRadixBits;
 constexpr int kExpandBags = 512;                        // bags per expand CTA
 
@@ -76,6 +77,7 @@ struct BwdLayout {
   uint32_t short_cap[kNumBuckets] = {0};
   uint32_t long_cap = 0, chunk_cap = 0, u_cap = 0, n_cap = 0;
   int sort_grid = 1, rle_grid = 1, cls_grid = 1, key_bits = 1, passes = 1, radix_bits = 8, final_buf = 0;
+  int pass_bits[4] = {8, 8, 8, 8};  // digit width of each radix pass, low digit first; radix_bits = the widest
   int acc_bytes = 4;  // fp32 workspace rows (fp64 for fp32 tables)
   size_t hist_ws = 0;  // nhist x kHistWsBytes
   int nhist = 0;
@@ -152,7 +154,7 @@ int bounds_grid(const DeviceInfo& dev);
 
 cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const void* weights,
                                   void* indices, const void* offsets, const float* psw, float* out,
-                                  int64_t unit_begin, int64_t unit_end, bool fused_bounds,
+                                  int64_t unit_begin, int64_t unit_end, bool fused_bounds, bool allow_tma,
                                   unsigned long long* stats, const DeviceInfo& dev, cudaStream_t s);
 
 bool histogram_supported();

@@ -25,6 +25,7 @@ TBE_OPT_SGD, TBE_OPT_ROWWISE_ADAGRAD = 0, 1
 TBE_LONG_AUTO, TBE_LONG_TWO_KERNEL, TBE_LONG_FUSED = 0, 1, 2
 TBE_SCHED_GRID, TBE_SCHED_PERSISTENT, TBE_SCHED_CLC = 0, 1, 2
 TBE_MERGE_ATOMIC, TBE_MERGE_BULK = 0, 1
+TBE_GATHER_REGISTER, TBE_GATHER_TMA = 0, 1
 TBE_CLASSIFY_ATOMIC, TBE_CLASSIFY_ORDERED = 0, 1
 TBE_FWD_NUM_EVENTS = 3
 TBE_BWD_NUM_EVENTS = 9
@@ -60,7 +61,7 @@ class Options(ctypes.Structure):
     _fields_ = [("long_threshold", c_i32), ("chunk", c_i32), ("long_mode", c_i32), ("scheduler", c_i32),
                 ("histogram", c_i32), ("fused_bounds", c_i32), ("events", ctypes.POINTER(vp)),
                 ("num_events", c_i32), ("launch_counter", ctypes.POINTER(c_i64)), ("classify_mode", c_i32),
-                ("prepared", c_i32), ("merge", c_i32)]
+                ("prepared", c_i32), ("merge", c_i32), ("gather", c_i32)]
 
 
 class RunMetadata(ctypes.Structure):

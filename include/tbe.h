@@ -105,6 +105,14 @@ typedef enum { TBE_MERGE_ATOMIC = 0, TBE_MERGE_BULK = 1 } tbe_merge_mode;
  * 1.43 -> 1.22 ms). */
 typedef enum { TBE_CLASSIFY_ATOMIC = 0, TBE_CLASSIFY_ORDERED = 1 } tbe_classify_mode;
 
+/* How the forward gather brings rows in ([FBT] section 2, "The general gather path": several
+ * row loads in flight per warp).  REGISTER (the default): 16-byte row loads into registers,
+ * 8 rows in flight per warp.  TMA: tables of one width D in {64, 128, 256} with 16-bit weights
+ * take tile::gather4 copies of four rows of the packed [sum E, D] weights into a shared-memory
+ * ring, up to 24 rows in flight per warp (other problems take REGISTER); on the 83.9M-lookup
+ * stress batch it measures 4.0 ms against 2.2 ms for REGISTER.  Both give the same sums. */
+typedef enum { TBE_GATHER_REGISTER = 0, TBE_GATHER_TMA = 1 } tbe_gather_mode;
+
 /* Host description of the problem.  Nothing here is read from the device. */
 typedef struct {
   int32_t T;                  /* tables */
@@ -156,6 +164,7 @@ typedef struct {
   int32_t prepared;           /* 1: tbe_backward_update takes the transpose from ws, where
                                  tbe_backward_prepare left it, instead of computing it */
   int32_t merge;              /* tbe_merge_mode */
+  int32_t gather;             /* tbe_gather_mode */
 } tbe_options;
 
 /* Indices into d_stats (int64).  Counts accumulate over calls. */
@@ -168,8 +177,8 @@ enum {
   TBE_NUM_STATS = 8
 };
 
-/* The defaults: threshold 256, chunk 256, AUTO long mode, GRID scheduler, histogram on,
- * fused bounds off, no events, ORDERED classifier. */
+/* The defaults: threshold 256, chunk 256, AUTO long mode, PERSISTENT scheduler, histogram on,
+ * fused bounds off, no events, ORDERED classifier, ATOMIC merge, REGISTER gather. */
 void tbe_default_options(tbe_options* opt);
 
 /* Fills the host arrays of the canonical packed layout for the problem; the caller copies

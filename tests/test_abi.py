@@ -47,7 +47,7 @@ def test_version_status_and_defaults(lib):
     lib.tbe_default_options(ctypes.byref(o))
     assert (o.long_threshold, o.chunk, o.long_mode, o.scheduler, o.histogram, o.fused_bounds) == \
         (256, 256, tbe.TBE_LONG_AUTO, tbe.TBE_SCHED_PERSISTENT, 1, 0)
-    assert (o.classify_mode, o.prepared, o.merge) == (tbe.TBE_CLASSIFY_ORDERED, 0, 0)
+    assert (o.classify_mode, o.prepared, o.merge, o.gather) == (tbe.TBE_CLASSIFY_ORDERED, 0, 0, tbe.TBE_GATHER_REGISTER)
 
 
 def test_table_layout(lib):
