@@ -397,27 +397,34 @@ __global__ void __launch_bounds__(kThreads, 2) radix_downsweep_kernel(
       const int d = threadIdx.x * DPT + q;
       s_dstart[d] = run;
       s_tcount[d] = tc[q];
+      // each warp's base for the digit becomes its tile position (one lookup per item below)
+#pragma unroll
+      for (int w2 = 0; w2 < kWarpsPerBlock; ++w2)
+        s_whist[w2 * R + d] = static_cast<uint16_t>(s_whist[w2 * R + d] + run);
       run += tc[q];
     }
     __syncthreads();
+    // the reordered tile as (key, bag) pairs over the keys and bags of the buffer: one 8-byte
+    // store per item at its scattered position (digit-indexed shared-memory accesses of a
+    // tile in batch order are where the bank conflicts are), then conflict-free reads in order
+    uint2* s_kv = reinterpret_cast<uint2*>(s_keys);
 #pragma unroll
     for (int i = 0; i < kSortItems; ++i) {
       const int e = w * (kSortItems * kWarp) + i * kWarp + lane;
       if (e < n) {
         const uint32_t d = (k[i] >> shift) & (R - 1);
-        const uint32_t pos = s_dstart[d] + s_whist[w * R + d] + rank[i];
-        s_keys[pos] = k[i];
-        s_vals[pos] = v[i];
+        const uint32_t pos = s_whist[w * R + d] + rank[i];
+        s_kv[pos] = make_uint2(k[i], v[i]);
         if (PSW) s_psw[pos] = pw[i];
       }
     }
     __syncthreads();
     for (int j = threadIdx.x; j < n; j += blockDim.x) {
-      const uint32_t key = s_keys[j];
-      const uint32_t d = (key >> shift) & (R - 1);
+      const uint2 kv = s_kv[j];
+      const uint32_t d = (kv.x >> shift) & (R - 1);
       const uint32_t g = s_run[d] + (static_cast<uint32_t>(j) - s_dstart[d]);
-      keys_out[g] = key;
-      vals_out[g] = s_vals[j];
+      keys_out[g] = kv.x;
+      vals_out[g] = kv.y;
       if (PSW) psw_out[g] = s_psw[j];
     }
     fence_proxy_async_smem();  // this buffer's generic accesses before the next bulk copy into it
