@@ -53,6 +53,8 @@ struct FwdArgs {
   int64_t unit_begin, unit_end;
   int64_t item_base;  // the launch's first work item
   int bags_per_item;  // 1..32
+  int t_begin;        // first table of the launch (unit_begin / B)
+  int64_t items_per_table, items;  // work items per table, in the launch
   int mean;           // mean pooling: the sum over the bag length (an empty bag stays 0)
   // dot mode (the gradient with respect to the per-sample weights): grad_out rows in, one fp32
   // per lookup out: grad_psw[p] = <grad_out[b, table's columns], W[idx[p]]> (/ L for mean)
@@ -68,6 +70,13 @@ struct alignas(64) TmaMap {
   uint64_t w[16];
 };
 static_assert(sizeof(TmaMap) == sizeof(CUtensorMap), "tensor map size");
+
+// Table (relative to the launch's first) of work item g: a 32-bit division when both fit.
+__device__ __forceinline__ int64_t item_table(int64_t g, int64_t items_per_table) {
+  if (((g | items_per_table) >> 31) == 0)
+    return static_cast<uint32_t>(g) / static_cast<uint32_t>(items_per_table);
+  return g / items_per_table;
+}
 
 __device__ __forceinline__ int next_pow2_int(int v) { return v <= 1 ? 1 : 1 << (32 - __clz(v - 1)); }
 
@@ -176,24 +185,24 @@ fwd_gather_kernel(FwdArgs a) {
   const unsigned FULL = 0xffffffffu;
   const int lane = lane_id();
   const int K = a.bags_per_item;
-  const int64_t items_per_table = (a.B + K - 1) / K;
-  const int t_begin = static_cast<int>(a.unit_begin / a.B);
-  const int64_t items = static_cast<int64_t>(a.unit_end / a.B - t_begin) * items_per_table;
   const int N = static_cast<int>(a.num_indices);
   // one work item per warp
   const int64_t g = a.item_base + ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
-  if (g < items) {
-    const int t = t_begin + static_cast<int>(g / items_per_table);
-    const int64_t b0 = (g % items_per_table) * K;
+  if (g < a.items) {
+    const int64_t tq = item_table(g, a.items_per_table);
+    const int t = a.t_begin + static_cast<int>(tq);
+    const int64_t b0 = (g - tq * a.items_per_table) * K;
     const int nb = static_cast<int>(min(static_cast<int64_t>(K), a.B - b0));
     const int64_t u0 = static_cast<int64_t>(t) * a.B + b0;
     const int col0 = __ldg(a.doff + t);
     const int D = __ldg(a.doff + t + 1) - col0;
     const int E = static_cast<int>(__ldg(a.roff + t + 1) - __ldg(a.roff + t));  // < 2^31
     const int nvec = D / NE;
-    const int lpr = nvec >= kWarp ? kWarp : next_pow2_int(nvec);  // lanes per row
-    const int rps = kWarp / lpr;                                    // rows per load step
-    const int slot = lane / lpr;
+    const int lpr = nvec >= kWarp ? kWarp : next_pow2_int(nvec);  // lanes per row (a power of 2)
+    const int lpr_log = __ffs(lpr) - 1;
+    const int rps_log = 5 - lpr_log;
+    const int rps = 1 << rps_log;                                  // rows per load step
+    const int slot = lane >> lpr_log;
     const int vi = lane & (lpr - 1);
     // row 0 of the table; this lane's vectors of a row (lanes past the row width re-read its last
     // vector in full batches: their sums are never stored); the item's first output row
@@ -202,7 +211,7 @@ fwd_gather_kernel(FwdArgs a) {
 #pragma unroll
     for (int m = 0; m < MAXV; ++m) vk[m] = min(vi + m * kWarp, nvec - 1);
     float* orow = a.out + b0 * a.total_D + col0 + vi * NE;
-    const int qmax = min(UNROLL, kWarp / rps);  // a batch covers at most 32 positions
+    const int qmax = min(UNROLL, lpr);  // a batch (qmax * rps rows) covers at most 32 positions
 
     // bag k of the item owns positions [s_k, e_k): lane k holds s_k in off_s and e_k in off_e
     int off_s = 0, off_e = 0;
@@ -289,7 +298,7 @@ fwd_gather_kernel(FwdArgs a) {
           } else {
             // the bag's last rows (or a batch with a skipped id): only the load steps that hold a
             // row are issued and summed
-            nq = min(qmax, (n - j + rps - 1) / rps);
+            nq = min(qmax, (n - j + rps - 1) >> rps_log);
 #pragma unroll
             for (int q = 0; q < UNROLL; ++q) {
 #pragma unroll
@@ -411,14 +420,16 @@ fwd_gather_kernel(FwdArgs a) {
 // step with each lane owning D/32 columns, so a finished bag needs no cross-lane reduction:
 // the warp stores it as one coalesced row.  Up to 4 x kTmaStages rows per warp are in flight
 // without holding registers (the register gather holds 8).  It is the TBE_GATHER_TMA option:
-// on the 83.9M-lookup stress batch (256-byte rows) it takes 4.0 ms against 2.2 ms for the
-// register gather.
+// on the 83.9M-lookup stress batch (256-byte rows, mostly L2 hits) it takes 3.1 ms against
+// 2.1 ms for the register gather, whose instructions per lookup are fewer (23 against 30);
+// on uniform ids over a 1M-row table (DRAM-bound) it is the faster one (0.048 vs 0.056 ms).
 // Items whose offsets do not tile their span (possible only when the offsets were not
 // repaired) take a plain per-bag loop instead.
 // ------------------------------------------------------------------------------------------
 constexpr int kTmaThreads = 64;
 constexpr int kTmaWarps = kTmaThreads / kWarp;
-constexpr int kTmaStages = 6;
+constexpr int kTmaStages = 8;
+constexpr int kTmaMinBlocks = 12;  // 16 KB of ring per CTA at D = 128
 constexpr uint32_t kTmaWaitLimit = 1u << 22;
 
 __device__ __forceinline__ void tma_gather4(void* dst, const TmaMap* map, int r0, int r1, int r2, int r3,
@@ -452,19 +463,21 @@ __device__ __forceinline__ void store_bag(float* orow, float (&acc)[NE], int len
 }
 
 template <typename WT, typename IT, bool PSW, int VB>
-__global__ void __launch_bounds__(kTmaThreads, 16) fwd_tma_gather_kernel(const __grid_constant__ TmaMap tmap,
-                                                                          FwdArgs a) {
+__global__ void __launch_bounds__(kTmaThreads, kTmaMinBlocks) fwd_tma_gather_kernel(
+    const __grid_constant__ TmaMap tmap, FwdArgs a) {
   using IO = VecIO<WT, VB>;
   using Raw = typename IO::Raw;
   constexpr int NE = IO::N;          // columns per lane
   constexpr int RB = VB * kWarp;     // bytes per row (D = 32 * NE)
   constexpr int SB = 4 * RB;         // bytes per stage
-  constexpr int S = kTmaStages;
+  constexpr int S = kTmaStages;      // a power of 2, at most 8 (two id windows cover the ring)
+  static_assert((S & (S - 1)) == 0 && S <= 8, "stage ring");
   const unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(128) uint8_t s_ring[];  // [warp][stage][4 rows]
   __shared__ __align__(8) uint64_t s_bar[kTmaWarps][S];
-  __shared__ float s_scale[kTmaWarps][S][4];  // per row: psw (weighted) or 1
-  __shared__ int s_mask[kTmaWarps][S];        // bit j: row j of the stage is a lookup to add
+  __shared__ __align__(16) int s_rows[kTmaWarps][2][kWarp];  // row numbers of two id windows
+  __shared__ float s_psw[kTmaWarps][2][kWarp];               // their psw (weighted)
+  __shared__ int s_mask[kTmaWarps][S];                        // bit j: row j of the stage is a lookup
   const int lane = lane_id(), wl = threadIdx.x / kWarp;
   uint8_t* ring = s_ring + wl * S * SB;
   uint64_t* bar = s_bar[wl];
@@ -476,14 +489,12 @@ __global__ void __launch_bounds__(kTmaThreads, 16) fwd_tma_gather_kernel(const _
   __syncwarp();
 
   const int K = a.bags_per_item;
-  const int64_t items_per_table = (a.B + K - 1) / K;
-  const int t_begin = static_cast<int>(a.unit_begin / a.B);
-  const int64_t items = static_cast<int64_t>(a.unit_end / a.B - t_begin) * items_per_table;
   const int N = static_cast<int>(a.num_indices);
   const int64_t g = a.item_base + ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
-  if (g >= items) return;
-  const int t = t_begin + static_cast<int>(g / items_per_table);
-  const int64_t b0 = (g % items_per_table) * K;
+  if (g >= a.items) return;
+  const int64_t tq = item_table(g, a.items_per_table);
+  const int t = a.t_begin + static_cast<int>(tq);
+  const int64_t b0 = (g - tq * a.items_per_table) * K;
   const int nb = static_cast<int>(min(static_cast<int64_t>(K), a.B - b0));
   const int64_t u0 = static_cast<int64_t>(t) * a.B + b0;
   const int col0 = __ldg(a.doff + t);
@@ -530,61 +541,60 @@ __global__ void __launch_bounds__(kTmaThreads, 16) fwd_tma_gather_kernel(const _
     return;
   }
 
-  // producer: stage i holds positions lo + 4i .. lo + 4i + 3 (rows past hi or of skipped ids
-  // are fetched from the table's row 0 and left out of the sums)
+  // Producer.  Stage i holds positions lo + 4i .. lo + 4i + 3; id window m (positions
+  // lo + 32m .. +31, stages 8m .. 8m + 7) is turned into row numbers (the table's row 0 where a
+  // lookup is skipped or past hi) and a validity mask by the whole warp, one position per lane,
+  // into shared slot m & 1, while window m + 1's ids are already on their way.  Lane 0 then
+  // issues a stage with one 16-byte read of four row numbers.
   const int nst = (hi - lo + 3) >> 2;
-  int pw = lo;  // window `cur` holds positions pw .. pw + 31, `nxt` the 32 after them
-  IdWindow<PSW> cur = load_window<IT, PSW>(a, pw + lane, lo, hi, E);
-  IdWindow<PSW> nxt = load_window<IT, PSW>(a, pw + kWarp + lane, lo, hi, E);
+  IdWindow<PSW> pre = load_window<IT, PSW>(a, lo + lane, lo, hi, E);
+  uint32_t wbits = 0;  // validity of the producer's current window
+  auto stage_window = [&](int m) {
+    const IdWindow<PSW> cur = pre;
+    pre = load_window<IT, PSW>(a, lo + (m + 1) * kWarp + lane, lo, hi, E);
+    const bool ok = cur.id >= 0;  // false past hi (the window reads nothing there)
+    s_rows[wl][m & 1][lane] = rbase + (ok ? cur.id : 0);
+    if (PSW) s_psw[wl][m & 1][lane] = cur.w;
+    wbits = __ballot_sync(FULL, ok);
+    __syncwarp();
+  };
   int issued = 0;
   auto issue = [&]() {
-    const int r = lo + 4 * issued - pw;  // 0, 4, .., 28
-    int row[4];
-    float sc[4];
-    int mask = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int32_t id = __shfl_sync(FULL, cur.id, r + j);
-      sc[j] = PSW ? __shfl_sync(FULL, cur.w, r + j) : 1.0f;
-      const bool ok = lo + 4 * issued + j < hi && id >= 0;
-      row[j] = rbase + (ok ? id : 0);
-      mask |= ok ? 1 << j : 0;
-    }
-    const int slot = issued % S;
+    if ((issued & 7) == 0) stage_window(issued >> 3);
+    const int slot = issued & (S - 1);
+    const int r = (issued & 7) * 4;
     if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) s_scale[wl][slot][j] = sc[j];
-      s_mask[wl][slot] = mask;
+      const int4 rows = *reinterpret_cast<const int4*>(&s_rows[wl][(issued >> 3) & 1][r]);
+      s_mask[wl][slot] = static_cast<int>((wbits >> r) & 0xFu);
       fence_proxy_async_smem();  // the slot's earlier reads before the copy overwrites it
       mbar_arrive_expect_tx(&bar[slot], SB);
-      tma_gather4(ring + slot * SB, &tmap, row[0], row[1], row[2], row[3], &bar[slot]);
+      tma_gather4(ring + slot * SB, &tmap, rows.x, rows.y, rows.z, rows.w, &bar[slot]);
     }
     ++issued;
-    if (r + 4 == kWarp) {
-      cur = nxt;
-      pw += kWarp;
-      nxt = load_window<IT, PSW>(a, pw + kWarp + lane, lo, hi, E);
-    }
   };
 
   // bags before the first row (empty ones) are written as zeros
   int k = 0;
   int s_k = __shfl_sync(FULL, off_s, 0), e_k = __shfl_sync(FULL, off_e, 0);
-  while (k < nb && e_k == s_k) {
-    store_bag<NE>(orow0 + static_cast<int64_t>(k) * a.total_D, acc, 0, mean);
+  auto next_bag = [&]() {  // store bag k, then move to the next non-empty bag (storing empty ones)
+    store_bag<NE>(orow0 + static_cast<int64_t>(k) * a.total_D, acc, e_k - s_k, mean);
     ++k;
-    if (k < nb) {
+    while (k < nb) {
       s_k = __shfl_sync(FULL, off_s, k);
       e_k = __shfl_sync(FULL, off_e, k);
+      if (e_k > s_k) break;
+      store_bag<NE>(orow0 + static_cast<int64_t>(k) * a.total_D, acc, 0, mean);
+      ++k;
     }
-  }
+  };
+  if (e_k == s_k) next_bag();  // a leading empty bag (stored as zeros)
   while (issued < nst && issued < S) issue();
   __syncwarp();
 
   bool failed = false;
   int i = 0;
   for (; i < nst; ++i) {
-    const int slot = i % S;
+    const int slot = i & (S - 1);
     if (!mbar_wait_bounded(&bar[slot], (i / S) & 1, kTmaWaitLimit)) {
       failed = true;
       if (lane == 0) stat_add(a.stats, TBE_STAT_WAIT_TIMEOUT, 1);
@@ -592,31 +602,27 @@ __global__ void __launch_bounds__(kTmaThreads, 16) fwd_tma_gather_kernel(const _
     }
     const uint8_t* st = ring + slot * SB + lane * VB;
     const int p0 = lo + 4 * i;
-    const int n = min(4, hi - p0);
-    Raw v[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = j < n ? lds_raw<WT, VB>(st + j * RB) : Raw{};
     const int mask = s_mask[wl][slot];
-    const bool plain = !PSW && mask == 0xF;
+    const float* wv = &s_psw[wl][(i >> 3) & 1][(i & 7) * 4];
+    if (mask == 0xF && e_k >= p0 + 4) {
+      // four lookups of bag k
+      Raw v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (j < n) {
-        if (plain) accumulate<WT, VB, false>(acc, v[j], 1.0f);
-        else if (mask & (1 << j)) accumulate<WT, VB, PSW>(acc, v[j], s_scale[wl][slot][j]);
-        if (p0 + j + 1 == e_k) {  // bag k ends at this row; empty bags after it are written too
-          store_bag<NE>(orow0 + static_cast<int64_t>(k) * a.total_D, acc, e_k - s_k, mean);
-          ++k;
-          while (k < nb) {
-            s_k = __shfl_sync(FULL, off_s, k);
-            e_k = __shfl_sync(FULL, off_e, k);
-            if (e_k > s_k) break;
-            store_bag<NE>(orow0 + static_cast<int64_t>(k) * a.total_D, acc, 0, mean);
-            ++k;
-          }
+      for (int j = 0; j < 4; ++j) v[j] = lds_raw<WT, VB>(st + j * RB);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) accumulate<WT, VB, PSW>(acc, v[j], PSW ? wv[j] : 1.0f);
+      if (e_k == p0 + 4) next_bag();
+    } else {
+      const int n = min(4, hi - p0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j < n) {
+          if (mask & (1 << j)) accumulate<WT, VB, PSW>(acc, lds_raw<WT, VB>(st + j * RB), PSW ? wv[j] : 1.0f);
+          if (p0 + j + 1 == e_k) next_bag();
         }
       }
     }
-    __syncwarp();  // every lane has read the slot
+    __syncwarp();  // every lane has read the slot (and the window entries of the stage)
     if (issued < nst) {
       issue();
       __syncwarp();
@@ -625,7 +631,7 @@ __global__ void __launch_bounds__(kTmaThreads, 16) fwd_tma_gather_kernel(const _
   if (failed) {
     // a copy that never signalled: wait once more (bounded) for every stage still in flight
     // before the warp's shared memory can be released
-    for (int q = i; q < issued; ++q) mbar_wait_bounded(&bar[q % S], (q / S) & 1, kTmaWaitLimit);
+    for (int q = i; q < issued; ++q) mbar_wait_bounded(&bar[q & (S - 1)], (q / S) & 1, kTmaWaitLimit);
   }
 }
 
@@ -647,7 +653,10 @@ cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   // about eight items per warp, at most 32 bags per item
   FwdArgs ak = a;
   ak.bags_per_item = bags_per_item_for(tables, a.B, warps);
-  const int64_t items = tables * ((a.B + ak.bags_per_item - 1) / ak.bags_per_item);
+  ak.t_begin = static_cast<int>(a.unit_begin / a.B);
+  ak.items_per_table = (a.B + ak.bags_per_item - 1) / ak.bags_per_item;
+  const int64_t items = tables * ak.items_per_table;
+  ak.items = items;
   // One item per warp: CTAs retire as their items finish and the block scheduler hands the SM
   // to the next one, which balances items of uneven length better than a resident grid-stride
   // loop.  Past the launch's grid limit the items go out in several launches.
@@ -679,7 +688,10 @@ cudaError_t launch_tma_t(const FwdArgs& a, const TmaMap& map, const DeviceInfo& 
   const int64_t warps = static_cast<int64_t>(persistent_grid(k, kTmaThreads, smem, dev, INT64_MAX)) * kTmaWarps;
   FwdArgs ak = a;
   ak.bags_per_item = bags_per_item_for(tables, a.B, warps);
-  const int64_t items = tables * ((a.B + ak.bags_per_item - 1) / ak.bags_per_item);
+  ak.t_begin = static_cast<int>(a.unit_begin / a.B);
+  ak.items_per_table = (a.B + ak.bags_per_item - 1) / ak.bags_per_item;
+  const int64_t items = tables * ak.items_per_table;
+  ak.items = items;
   constexpr int64_t kMaxGrid = 0x7fffffff;
   const int64_t per_launch = kMaxGrid * kTmaWarps;
   for (int64_t base = 0; base < items; base += per_launch) {
