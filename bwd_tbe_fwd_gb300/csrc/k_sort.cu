@@ -107,42 +107,94 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
     s_shift[k] = static_cast<uint32_t>(shift);
   }
   __syncthreads();
-  constexpr int U = 4;  // consecutive lookups per thread
-  for (int64_t pb = p0 + static_cast<int64_t>(threadIdx.x) * U; pb < p1; pb += static_cast<int64_t>(U) * blockDim.x) {
+  // Each thread takes a 4-aligned group of 4 consecutive lookups: 16- or 32-byte loads of
+  // their ids (and psw), and, when no counts-path table moves lookups (each lands at its own
+  // position), 16-byte stores of their keys, bags and factors.  Groups that straddle the CTA's
+  // range or the buffers' alignment take scalar accesses.
+  constexpr int U = 4;
+  const int64_t pa = p0 & ~static_cast<int64_t>(U - 1);
+  const bool in_place = a.nhist == 0;
+  const bool vec_in = (reinterpret_cast<uintptr_t>(a.indices) & 15) == 0 &&
+                      (!PSW || a.psw == nullptr || (reinterpret_cast<uintptr_t>(a.psw) & 15) == 0);
+  for (int64_t pb = pa + static_cast<int64_t>(threadIdx.x) * U; pb < p1; pb += static_cast<int64_t>(U) * blockDim.x) {
+    const bool whole = pb >= p0 && pb + U <= p1;
     int64_t id[U];
     float w[U];
+    if (whole && vec_in) {
+      if constexpr (sizeof(IT) == 8) {
+        const longlong2* v = reinterpret_cast<const longlong2*>(static_cast<const IT*>(a.indices) + pb);
+        const longlong2 x = __ldg(v), y = __ldg(v + 1);
+        id[0] = x.x; id[1] = x.y; id[2] = y.x; id[3] = y.y;
+      } else {
+        const int4 x = __ldg(reinterpret_cast<const int4*>(static_cast<const IT*>(a.indices) + pb));
+        id[0] = x.x; id[1] = x.y; id[2] = x.z; id[3] = x.w;
+      }
+      if (PSW) {
+        if (a.psw != nullptr) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(a.psw + pb));
+          w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+        } else {
+          w[0] = w[1] = w[2] = w[3] = 1.f;
+        }
+      }
+    } else {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t p = pb + u;
-      id[u] = p < p1 ? ld_int<IT>(a.indices, p) : 0;
-      if (PSW) w[u] = p < p1 ? (a.psw != nullptr ? __ldg(a.psw + p) : 1.f) : 0.f;
+      for (int u = 0; u < U; ++u) {
+        const int64_t p = pb + u;
+        const bool in = p >= p0 && p < p1;
+        id[u] = in ? ld_int<IT>(a.indices, p) : 0;
+        if (PSW) w[u] = in ? (a.psw != nullptr ? __ldg(a.psw + p) : 1.f) : 0.f;
+      }
     }
-    int lo = 0, hi = nb;  // s_off[lo] <= pb < s_off[hi] (for non-decreasing offsets)
+    const int64_t pf = pb < p0 ? p0 : pb;  // the group's first lookup of this CTA
+    int lo = 0, hi = nb;  // s_off[lo] <= pf < s_off[hi] (for non-decreasing offsets)
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (s_off[mid] <= pb) lo = mid;
+      if (s_off[mid] <= pf) lo = mid;
       else hi = mid;
     }
+    uint32_t kk[U], vv[U];
+    float ff[U];
+    int64_t qq[U];  // where each lookup lands among the kept ones; -1: not this CTA's, or dropped
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t p = pb + u;
-      if (p >= p1) break;
+      kk[u] = 0;
+      vv[u] = 0;
+      ff[u] = 0.f;
+      qq[u] = -1;
+      if (p < p0 || p >= p1) continue;
       while (lo + 1 < nb && s_off[lo + 1] <= p) ++lo;  // the next bags (possibly empty ones)
       const uint32_t E = s_E[lo];
       const bool hist_bag = a.nhist > 0 && E == 0;
-      const int64_t q = p - s_shift[lo];  // where the lookup lands among the kept ones
+      const int64_t q = p - s_shift[lo];
       if (hist_bag || q < 0 || q >= n_kept) continue;  // (out of range only for unrepaired offsets)
-      uint32_t key;
+      qq[u] = q;
       if (id[u] >= 0 && id[u] < static_cast<int64_t>(E)) {
-        key = s_rb[lo] + static_cast<uint32_t>(id[u]);
+        kk[u] = s_rb[lo] + static_cast<uint32_t>(id[u]);
       } else {
-        key = a.sentinel;
+        kk[u] = a.sentinel;
         ++bad;
       }
-      a.keys[q] = key;
-      a.vals[q] = s_b[lo];
+      vv[u] = s_b[lo];
       // the lookup's factor: psw, over the bag length for mean pooling (correctly rounded)
-      if (PSW) a.psw_out[q] = a.mean ? __fdiv_rn(w[u], static_cast<float>(s_off[lo + 1] - s_off[lo])) : w[u];
+      if (PSW) ff[u] = a.mean ? __fdiv_rn(w[u], static_cast<float>(s_off[lo + 1] - s_off[lo])) : w[u];
+    }
+    bool vec_out = whole && in_place;
+#pragma unroll
+    for (int u = 0; u < U; ++u) vec_out = vec_out && qq[u] == pb + u;
+    if (vec_out) {  // one 16-byte store per array
+      *reinterpret_cast<uint4*>(a.keys + pb) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+      *reinterpret_cast<uint4*>(a.vals + pb) = make_uint4(vv[0], vv[1], vv[2], vv[3]);
+      if (PSW) *reinterpret_cast<float4*>(a.psw_out + pb) = make_float4(ff[0], ff[1], ff[2], ff[3]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (qq[u] < 0) continue;
+        a.keys[qq[u]] = kk[u];
+        a.vals[qq[u]] = vv[u];
+        if (PSW) a.psw_out[qq[u]] = ff[u];
+      }
     }
   }
   if (bad) atomicAdd(&s_bad, bad);
