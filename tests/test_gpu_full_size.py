@@ -1,12 +1,15 @@
-"""The CUDA library at the full large-skew size (32 tables of 4M fp16 rows x 128, 131,072 bags
-per table, ~83.9M Zipf-skewed lookups) in the launch configuration the benchmark times
+"""The CUDA library at the workloads' full sizes, in the launch configuration the benchmark times
 (offsets-only bounds check with ids repaired inside the forward, default scheduler and run
-lists), checked against the oracle where it can follow one output at a time and against
-properties that hold at any size:
+lists): the large-skew batch (32 tables of 4M fp16 rows x 128, ~83.9M Zipf-skewed lookups),
+the mixed batch (64 tables of widths 32-256, bf16, per-sample weights, 0.1% out-of-range ids,
+~29.9M lookups), the histogram batch (a 64-row table on the counts x table path beside a 1M-row
+table) and the mid batch (int32).  Each is checked against the oracle where it can follow one
+output at a time and against properties that hold at any size:
 
   * repaired ids and offsets: bit-exact over the whole batch (the oracle's repair);
   * sorted keys, sorted bags, unique keys, run offsets and run lengths: bit-exact over the
-    whole batch, against a stable host sort of the linear keys;
+    whole batch, against a stable host sort of the linear keys (lookups of counts-path tables
+    left out, as the library leaves them out of the sort);
   * pooled outputs: sampled bags (and the longest one), each through the oracle on its own;
   * updated rows and Adagrad state: the hottest rows, a random sample of touched rows and a few
     rows no lookup touched, each through the oracle on the lookups that hit it.
@@ -31,9 +34,17 @@ N_ROWS = 40     # random touched rows
 N_COLD = 4      # rows no lookup touched
 
 
-@pytest.fixture(scope="module")
-def full():
-    cfg = get_config("c3")
+def counts_path_tables(cfg):
+    """Tables the library runs on the counts x table path with default options (at most 8)."""
+    if cfg.wdtype != "f16" or cfg.weighted:
+        return []
+    return [t for t, spec in enumerate(cfg.tables)
+            if spec.histogram and spec.E <= 64 and 64 <= spec.D <= 128][:8]
+
+
+@pytest.fixture(scope="module", params=["c3", "c5", "c4", "c2"])
+def full(request):
+    cfg = get_config(request.param)
     batch = make_batch(cfg)
     dev = torch.device("cuda", 0)
     itype = torch.int32 if cfg.itype == "i32" else torch.int64
@@ -70,17 +81,22 @@ def full():
     table_of = np.repeat(np.arange(cfg.T, dtype=np.int64), cfg.B)
     keys = (np.repeat(roff[:-1][table_of], lens) + idx_h.astype(np.int64)).astype(np.int32)
     bag_of = np.repeat(np.arange(cfg.T * cfg.B, dtype=np.int64) % cfg.B, lens)
-    # a stable host sort of the keys: the runs the library must produce
+    # a stable host sort of the keys: every row's lookups (for the updates) and the runs the
+    # library must produce (without the counts-path tables' lookups)
     order = np.argsort(keys, kind="stable")
     sk = keys[order]
     head = np.ones(len(sk), dtype=bool)
     head[1:] = sk[1:] != sk[:-1]
     starts = np.flatnonzero(head)
+    hist = counts_path_tables(cfg)
+    sorted_mask = np.ones(len(keys), dtype=bool)
+    for t in hist:
+        sorted_mask[off64[t * cfg.B]:off64[(t + 1) * cfg.B]] = False
     ns = SimpleNamespace(cfg=cfg, batch=batch, tbe=tbe, weights=weights, state=state, out=out,
                          stats=stats, meta=meta, idx=idx, off=off, idx_h=idx_h, off_h=off64,
                          per_table=per_table, n_off=n_off, roff=roff, keys=keys, bag_of=bag_of,
                          order=order, sorted_keys=sk, unique=sk[starts],
-                         run_off=np.append(starts, len(sk)))
+                         run_off=np.append(starts, len(sk)), sorted_mask=sorted_mask)
     yield ns
     del ns, tbe, weights, state, grad, idx, off, psw, out, stats, meta
     torch.cuda.empty_cache()
@@ -95,15 +111,24 @@ def test_full_bounds_repair_is_the_oracles(full):
 
 def test_full_run_metadata_bit_exact(full):
     m = full.meta
-    N = len(full.keys)
+    keep = full.sorted_mask[full.order]  # the runs of the sort path, in key order
+    order = full.order[keep]
+    sk = full.sorted_keys[keep]
+    N = len(sk)
     assert m["N"] == N
-    assert np.array_equal(m["sorted_keys"].cpu().numpy(), full.sorted_keys), "sorted keys differ"
-    assert np.array_equal(m["sorted_bags"].cpu().numpy().astype(np.int64), full.bag_of[full.order]), \
+    assert np.array_equal(m["sorted_keys"].cpu().numpy(), sk), "sorted keys differ"
+    assert np.array_equal(m["sorted_bags"].cpu().numpy().astype(np.int64), full.bag_of[order]), \
         "sorted bags differ"
-    assert m["U"] == len(full.unique)
-    assert np.array_equal(m["unique_keys"].cpu().numpy(), full.unique), "unique keys differ"
-    assert np.array_equal(m["run_offsets"].cpu().numpy().astype(np.int64), full.run_off), "run offsets differ"
-    assert np.array_equal(m["run_lengths"].cpu().numpy().astype(np.int64), np.diff(full.run_off)), \
+    if full.batch.psw is not None and "sorted_psw" in m:
+        assert np.array_equal(m["sorted_psw"].cpu().numpy(), full.batch.psw[order]), "sorted psw differ"
+    head = np.ones(N, dtype=bool)
+    head[1:] = sk[1:] != sk[:-1]
+    starts = np.flatnonzero(head)
+    run_off = np.append(starts, N)
+    assert m["U"] == len(starts)
+    assert np.array_equal(m["unique_keys"].cpu().numpy(), sk[starts]), "unique keys differ"
+    assert np.array_equal(m["run_offsets"].cpu().numpy().astype(np.int64), run_off), "run offsets differ"
+    assert np.array_equal(m["run_lengths"].cpu().numpy().astype(np.int64), np.diff(run_off)), \
         "run lengths differ"
 
 
