@@ -103,7 +103,7 @@ tbe_status make_problem(const tbe_problem* p, Problem* out) {
   }
   P.vec_bytes = all_vec16 ? 16 : 8;
   if (P.itype == TBE_I32 && (P.total_rows > INT32_MAX || P.num_indices > INT32_MAX)) return TBE_ERR_RANGE;
-  if (P.B >= (int64_t(1) << 31) || P.num_indices >= (int64_t(1) << 31) ||
+  if (P.B >= (int64_t(1) << 31) || P.num_indices > kMaxIndices ||
       P.total_rows >= (int64_t(1) << 31))
     return TBE_ERR_UNSUPPORTED;
   return TBE_OK;

@@ -19,6 +19,10 @@ constexpr int kWarp = 32;
 constexpr int kMaxTables = 4096;
 constexpr int kNumBuckets = TBE_NUM_BUCKETS;  // short-run buckets: next_pow2(D) = 2^k
 constexpr int kMaxD = 1024;
+// Most lookups a problem may hold.  Kernels keep lookup positions in 32-bit ints and compute
+// positions up to 127 past a bag's end (the gather's 32-position id windows run up to four
+// windows ahead); 2^16 below 2^31 keeps every such position representable.
+constexpr int64_t kMaxIndices = (int64_t(1) << 31) - (int64_t(1) << 16);
 constexpr int kSortThreads = 256;
 constexpr int kSortItems = 16;
 constexpr int kSortTile = kSortThreads * kSortItems;  // keys per radix-sort tile

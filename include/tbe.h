@@ -40,9 +40,11 @@
  *     and reads it whenever it likes).  Kernels never dereference an id outside its table.
  *   - The workspace is caller-owned device memory of at least the size the matching
  *     *_workspace_size() call returns for the same problem and options; 256-byte aligned.
- *   - Limits: 1 <= T <= 4096, 0 <= B, D[t] % 4 == 0 and 4 <= D[t] <= 1024, num_indices < 2^31,
- *     sum_t E[t] < 2^31, B < 2^31; TBE_I32 additionally needs sum_t E[t] and num_indices to fit in
- *     int32 ([FBT] section 2: int32 indices/offsets when the linearized range fits below 2^31).
+ *   - Limits: 1 <= T <= 4096, 0 <= B, D[t] % 4 == 0 and 4 <= D[t] <= 1024,
+ *     num_indices <= 2^31 - 2^16 (lookup positions, and the few positions past a bag's end that
+ *     the gather computes, stay 32-bit), sum_t E[t] < 2^31, B < 2^31; TBE_I32 additionally needs
+ *     sum_t E[t] and num_indices to fit in int32 ([FBT] section 2: int32 indices/offsets when the
+ *     linearized range fits below 2^31).
  */
 #ifndef TBE_H
 #define TBE_H

@@ -68,6 +68,10 @@ def test_table_layout(lib):
     ([8], [2 ** 31], tbe.TBE_I32, 16, tbe.TBE_ERR_RANGE),         # int32 ids cannot address the rows
     ([8], [2 ** 31], tbe.TBE_I64, 16, tbe.TBE_ERR_UNSUPPORTED),   # linear keys are 31-bit
     ([8], [10], tbe.TBE_I64, 2 ** 31, tbe.TBE_ERR_UNSUPPORTED),   # lookups beyond 2^31
+    ([8], [10], tbe.TBE_I64, 2 ** 31 - 2 ** 16 + 1, tbe.TBE_ERR_UNSUPPORTED),  # within 2^16 of 2^31
+    ([8], [10], tbe.TBE_I32, 2 ** 31 - 2 ** 16 + 1, tbe.TBE_ERR_UNSUPPORTED),
+    ([8], [10], tbe.TBE_I64, 2 ** 31 - 2 ** 16, tbe.TBE_OK),                   # the largest accepted
+    ([8], [10], tbe.TBE_I32, 2 ** 31 - 2 ** 16, tbe.TBE_OK),
 ])
 def test_layout_rejects(lib, D, E, itype, n, expect):
     p, keep = _problem(D, E, itype=itype, n=n)
