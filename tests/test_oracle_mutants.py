@@ -61,6 +61,26 @@ MUTANTS = [
     ("forward_drops_last_lookup",
      "for (int64_t p = s; p < e; ++p) {\n        const int64_t row = load_int(indices, itype, p);",
      "for (int64_t p = s; p + 1 < e; ++p) {\n        const int64_t row = load_int(indices, itype, p);"),
+    # run metadata: run offsets not accumulated; bags numbered across tables instead of per table
+    ("run_offsets_not_accumulated", "res->run_offsets.push_back(res->run_offsets.back() + len);",
+     "res->run_offsets.push_back(len);"),
+    ("bags_numbered_across_tables", "r.bags.push_back(b);", "r.bags.push_back(t * B + b);"),
+    # Adagrad: |g| summed instead of g^2
+    ("adagrad_abs_not_square", "sumsq += r.g[d] * r.g[d];", "sumsq += std::fabs(r.g[d]);"),
+    # mean pooling: the empty-bag guard dropped (0 / 0)
+    ("mean_empty_bag_divides", "if (pooling == 1 && e > s) {", "if (pooling == 1) {"),
+    # a key on the first row of the next table attributed to the previous table
+    ("table_of_key_boundary", "if (key < L.row_begin[t + 1]) return t;", "if (key <= L.row_begin[t + 1]) return t;"),
+    # conversions: the fp16 overflow test off by one; the subnormal scale off by one
+    ("half_overflow_boundary", "if (biased >= (1 << exp_bits) - 1) return", "if (biased > (1 << exp_bits) - 1) return"),
+    ("half_subnormal_scale", "double q = std::nearbyint(std::ldexp(a, frac_bits - emin));",
+     "double q = std::nearbyint(std::ldexp(a, frac_bits - emin - 1));"),
+    # Adagrad: eps subtracted
+    ("adagrad_eps_sign", "(std::sqrt(s_new) + static_cast<double>(eps))", "(std::sqrt(s_new) - static_cast<double>(eps))"),
+    # bounds: a bad id repaired to the table's last row; the first offset left as given
+    ("bounds_repairs_to_last_row", "if (idx < 0 || idx >= E[t]) { store_int(indices, itype, p, 0); ++bad; }",
+     "if (idx < 0 || idx >= E[t]) { store_int(indices, itype, p, E[t] - 1); ++bad; }"),
+    ("bounds_first_offset_kept", "if (TB > 0 && load_int(offsets, itype, 0) != 0) {", "if (false) {"),
 ]
 
 
