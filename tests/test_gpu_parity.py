@@ -208,6 +208,54 @@ def test_offsets_only_bounds_check_then_fused_forward_and_backward():
     c.backward()
 
 
+def corrupt_offsets(off: np.ndarray, seed: int) -> np.ndarray:
+    """Offsets broken in every way the repair rule covers: a first offset that is not 0, negative
+    ones, decreases, values past the last offset, one jump far ahead (the prefix maximum then
+    raises every offset after it up to the jump, across the segments of many CTAs) and a last
+    offset above num_indices."""
+    rng = np.random.default_rng(seed)
+    o = off.astype(np.int64).copy()
+    TB = len(o) - 1
+    N = int(o[-1])
+    k = max(1, TB // 200)
+    pos = rng.choice(np.arange(1, TB), size=3 * k, replace=False)
+    neg, dec, past = pos[:k], pos[k:2 * k], pos[2 * k:]
+    o[neg] = -rng.integers(1, 1000, size=k)
+    o[dec] = o[dec] - rng.integers(1, 64, size=k)
+    o[past] = N + rng.integers(1, 1000, size=k)
+    o[TB // 3] = o[2 * TB // 3]
+    o[0] = 7
+    o[TB] = N + 50
+    return o.astype(off.dtype)
+
+
+@pytest.mark.parametrize("offsets_only", [False, True])
+@pytest.mark.parametrize("name", ["c5", "c2"])
+def test_corrupted_offsets_repaired_as_the_oracle(name, offsets_only):
+    """Offsets and ids repaired on the device exactly as the oracle repairs them (bit-exact,
+    with the same counts), then forward and backward parity on the repaired batch.  With
+    offsets_only the ids are repaired by the forward (fused bounds) instead."""
+    cfg = SMALL[name]
+    c = Case(cfg, bounds_check=False)
+    bad = corrupt_offsets(c.off_h, seed=17)
+    c.off_h[:] = bad
+    c.off_d.copy_(torch.from_numpy(bad))
+    if not offsets_only:
+        per_table, n_off = c.run_bounds()
+        assert n_off > 0
+        c.forward()
+    else:
+        per_table, n_off = oracle.bounds_repair(c.tables, cfg.B, c.idx_h, c.off_h)
+        c.tbe.bounds_check(c.idx_d, c.off_d, stats=c.stats, offsets_only=True)
+        torch.cuda.synchronize()
+        assert np.array_equal(c.off_d.cpu().numpy(), c.off_h), "repaired offsets differ"
+        assert c.stats[1].item() == n_off > 0
+        c.forward(options=TBEOptions(fused_bounds=1))
+        assert np.array_equal(c.idx_d.cpu().numpy(), c.idx_h), "ids repaired in flight differ"
+        assert c.stats[0].item() == per_table.sum()
+    c.backward()
+
+
 def test_unrepaired_ids_are_skipped_not_dereferenced():
     cfg = SMALL["c5"]
     c = Case(cfg, bounds_check=False)
