@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kThreads) offsets_max_kernel(const IT* offsets
   const int64_t seg = (inner + gridDim.x - 1) / gridDim.x;
   const int64_t i0 = 1 + seg * blockIdx.x, i1 = min(1 + inner, i0 + seg);
   int64_t m = 0;
+#pragma unroll 8
   for (int64_t i = i0 + threadIdx.x; i < i1; i += blockDim.x)
     m = max(m, clamp64(static_cast<int64_t>(offsets[i]), 0, last));
   m = block_reduce_max(m, sh);
@@ -61,10 +62,16 @@ __global__ void __launch_bounds__(kThreads) offsets_max_kernel(const IT* offsets
   }
 }
 
+// Each thread repairs kFixPerThread consecutive offsets per tile: a running maximum over its
+// own offsets, then one block-wide scan of the threads' maxima (a tile of 2048 offsets per
+// round of barriers rather than 256: the stress batch's 4.2M offsets take 4 rounds per CTA).
+constexpr int kFixPerThread = 8;
+
 template <typename IT>
 __global__ void __launch_bounds__(kThreads) offsets_fix_kernel(IT* offsets, int64_t TB,
                                                               const int64_t* ws,
                                                               unsigned long long* stats) {
+  constexpr int V = kFixPerThread;
   __shared__ int64_t sh[kThreads / kWarp];
   __shared__ unsigned long long shc[kThreads / kWarp];
   const int lane = lane_id(), w = threadIdx.x / kWarp;
@@ -78,27 +85,41 @@ __global__ void __launch_bounds__(kThreads) offsets_fix_kernel(IT* offsets, int6
   const int64_t seg = (inner + gridDim.x - 1) / gridDim.x;
   const int64_t i0 = 1 + seg * blockIdx.x, i1 = min(1 + inner, i0 + seg);
   unsigned long long changed = 0;
-  for (int64_t base = i0; base < i1; base += blockDim.x) {
-    const int64_t i = base + threadIdx.x;
-    const bool in = i < i1;
-    const int64_t orig = in ? static_cast<int64_t>(offsets[i]) : 0;
-    int64_t v = in ? clamp64(orig, 0, last) : 0;
-    // inclusive prefix maximum over the block
-    for (int d = 1; d < kWarp; d <<= 1) {
-      const int64_t o = __shfl_up_sync(0xffffffffu, v, d);
-      if (lane >= d) v = max(v, o);
+  for (int64_t base = i0; base < i1; base += static_cast<int64_t>(blockDim.x) * V) {  // block-uniform
+    const int64_t ib = base + static_cast<int64_t>(threadIdx.x) * V;
+    int64_t orig[V], v[V];
+#pragma unroll
+    for (int u = 0; u < V; ++u) orig[u] = ib + u < i1 ? static_cast<int64_t>(offsets[ib + u]) : 0;
+    // inclusive prefix maximum over the thread's own offsets (clamped into [0, last]; a slot
+    // past the segment holds 0, which changes no maximum)
+    int64_t run = 0;
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      run = max(run, clamp64(orig[u], 0, last));
+      v[u] = run;
     }
+    // inclusive prefix maximum of the threads' maxima over the block
+    int64_t x = run;
+    for (int d = 1; d < kWarp; d <<= 1) {
+      const int64_t o = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x = max(x, o);
+    }
+    const int64_t x_prev = __shfl_up_sync(0xffffffffu, x, 1);
     __syncthreads();
-    if (lane == kWarp - 1) sh[w] = v;
+    if (lane == kWarp - 1) sh[w] = x;
     __syncthreads();
-    int64_t before = carry;
+    int64_t before = carry;  // the largest offset before this thread's first
     for (int k = 0; k < w; ++k) before = max(before, sh[k]);
+    if (lane > 0) before = max(before, x_prev);
     int64_t tile_max = carry;
     for (int k = 0; k < static_cast<int>(blockDim.x / kWarp); ++k) tile_max = max(tile_max, sh[k]);
-    v = max(v, before);
-    if (in && v != orig) {
-      offsets[i] = static_cast<IT>(v);
-      ++changed;
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const int64_t f = max(v[u], before);
+      if (ib + u < i1 && f != orig[u]) {
+        offsets[ib + u] = static_cast<IT>(f);
+        ++changed;
+      }
     }
     carry = tile_max;
   }

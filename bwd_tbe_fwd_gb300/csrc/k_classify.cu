@@ -105,11 +105,12 @@ struct RunRoute {
   int t, D;
 };
 
-__device__ __forceinline__ RunRoute route_run(const BwdCtx& c, uint32_t r) {
+// The route of the run with linear key `key` covering sorted positions [start, end).
+__device__ __forceinline__ RunRoute route_of(const BwdCtx& c, uint32_t key, uint32_t start, uint32_t end) {
   RunRoute x;
-  x.key = c.unique[r];
-  x.start = c.run_off[r];
-  x.len = c.run_off[r + 1] - x.start;
+  x.key = key;
+  x.start = start;
+  x.len = end - start;
   x.list = -1;
   x.nch = 0;
   x.t = 0;
@@ -127,6 +128,10 @@ __device__ __forceinline__ RunRoute route_run(const BwdCtx& c, uint32_t r) {
   return x;
 }
 
+__device__ __forceinline__ RunRoute route_run(const BwdCtx& c, uint32_t r) {
+  return route_of(c, c.unique[r], c.run_off[r], c.run_off[r + 1]);
+}
+
 __global__ void __launch_bounds__(kThreads) classify_count_kernel(BwdCtx c) {
   __shared__ uint32_t s_cnt[kLists];
   if (threadIdx.x < kLists) s_cnt[threadIdx.x] = 0;
@@ -134,6 +139,7 @@ __global__ void __launch_bounds__(kThreads) classify_count_kernel(BwdCtx c) {
   const uint32_t U = min(c.counters[TBE_CNT_RUNS], c.u_cap);
   uint32_t r0, r1;
   cls_segment(U, blockIdx.x, gridDim.x, &r0, &r1);
+#pragma unroll 4
   for (uint32_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
     const RunRoute x = route_run(c, r);
     if (x.list >= 0) atomicAdd(&s_cnt[x.list], 1u);
@@ -180,7 +186,20 @@ __global__ void __launch_bounds__(kThreads) classify_write_kernel(BwdCtx c) {
   const uint32_t U = min(c.counters[TBE_CNT_RUNS], c.u_cap);
   uint32_t r0, r1;
   cls_segment(U, blockIdx.x, gridDim.x, &r0, &r1);
+  // this thread's run of the next tile (key, start, end), loaded while the current tile is
+  // ranked and written, so a tile's run records are not one DRAM round trip on its own path
+  uint32_t nkey = 0, nstart = 0, nend = 0;
+  auto fetch = [&](uint32_t r) {
+    if (r < r1) {
+      nkey = c.unique[r];
+      nstart = c.run_off[r];
+      nend = c.run_off[r + 1];
+    }
+  };
+  fetch(r0 + threadIdx.x);
   for (uint32_t tb = r0; tb < r1; tb += kThreads) {  // block-uniform
+    const uint32_t key = nkey, start = nstart, end = nend;
+    fetch(tb + kThreads + threadIdx.x);
     for (int i = threadIdx.x; i < W * kLists; i += blockDim.x) (&s_wc[0][0])[i] = 0;
     __syncthreads();
     const uint32_t r = tb + threadIdx.x;
@@ -188,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) classify_write_kernel(BwdCtx c) {
     x.list = -1;
     x.nch = 0;
     if (r < r1) {
-      x = route_run(c, r);
+      x = route_of(c, key, start, end);
       c.run_len[r] = x.len;
     }
     // rank among the warp's lanes of the same list; the chunk list by an inclusive scan
