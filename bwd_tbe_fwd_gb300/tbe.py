@@ -134,8 +134,9 @@ def _ptr(t: torch.Tensor | None):
     return None if t is None else vp(t.data_ptr())
 
 
-def _stream(stream) -> vp:
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _stream(stream, device) -> vp:
+    """The cudaStream_t of `stream`, or of the current stream of `device` when None."""
+    s = stream if stream is not None else torch.cuda.current_stream(device)
     return vp(s.cuda_stream)
 
 
@@ -180,7 +181,9 @@ class TBEOptions:
 
 class TableBatchedEmbedding:
     """One problem shape (tables, batch size, index capacity) with its device layout arrays and
-    caller-owned workspaces, and the three operations of the library."""
+    caller-owned workspaces, and the three operations of the library.  Every call runs with the
+    problem's device current (the library launches on the current device) and on the stream
+    passed, else on that device's current stream."""
 
     def __init__(self, D, E, B: int, num_indices: int, weight_dtype: torch.dtype,
                  index_dtype: torch.dtype = torch.int64, weighted: bool = False, long_bags=None,
@@ -253,15 +256,16 @@ class TableBatchedEmbedding:
         fused_bounds=1."""
         self._idx(indices, offsets)
         self._dev(stats, "stats", torch.int64, TBE_NUM_STATS)
-        if offsets_only:
-            st = self.lib.tbe_bounds_check_offsets(ctypes.byref(self.prob), ctypes.byref(self.tables), _ptr(offsets),
-                                                   _ptr(self.ws_bounds), self.ws_bounds.numel(), _ptr(stats),
-                                                   _stream(stream))
-            _check(self.lib, st, "tbe_bounds_check_offsets")
-            return
-        st = self.lib.tbe_bounds_check(ctypes.byref(self.prob), ctypes.byref(self.tables), _ptr(indices),
-                                       _ptr(offsets), _ptr(self.ws_bounds), self.ws_bounds.numel(),
-                                       _ptr(stats), _stream(stream))
+        with torch.cuda.device(self.device):
+            if offsets_only:
+                st = self.lib.tbe_bounds_check_offsets(ctypes.byref(self.prob), ctypes.byref(self.tables),
+                                                       _ptr(offsets), _ptr(self.ws_bounds), self.ws_bounds.numel(),
+                                                       _ptr(stats), _stream(stream, self.device))
+                _check(self.lib, st, "tbe_bounds_check_offsets")
+                return
+            st = self.lib.tbe_bounds_check(ctypes.byref(self.prob), ctypes.byref(self.tables), _ptr(indices),
+                                           _ptr(offsets), _ptr(self.ws_bounds), self.ws_bounds.numel(),
+                                           _ptr(stats), _stream(stream, self.device))
         _check(self.lib, st, "tbe_bounds_check")
 
     def forward(self, weights, indices, offsets, psw=None, out=None, stats=None, stream=None,
@@ -274,9 +278,11 @@ class TableBatchedEmbedding:
             out = torch.empty(self.B, self.total_D, dtype=torch.float32, device=self.device)
         self._dev(out, "out", torch.float32, self.B * self.total_D)
         o = (options or self.options).c
-        st = self.lib.tbe_forward(ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables),
-                                  _ptr(weights), _ptr(indices), _ptr(offsets), _ptr(psw), _ptr(out),
-                                  _ptr(self.ws_forward), self.ws_forward.numel(), _ptr(stats), _stream(stream))
+        with torch.cuda.device(self.device):
+            st = self.lib.tbe_forward(ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables),
+                                      _ptr(weights), _ptr(indices), _ptr(offsets), _ptr(psw), _ptr(out),
+                                      _ptr(self.ws_forward), self.ws_forward.numel(), _ptr(stats),
+                                      _stream(stream, self.device))
         _check(self.lib, st, "tbe_forward")
         return out
 
@@ -291,9 +297,10 @@ class TableBatchedEmbedding:
             grad_psw = torch.zeros(self.num_indices, dtype=torch.float32, device=self.device)
         self._dev(grad_psw, "grad_psw", torch.float32, self.num_indices)
         o = (options or self.options).c
-        st = self.lib.tbe_psw_gradient(ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables),
-                                       _ptr(weights), _ptr(indices), _ptr(offsets), _ptr(grad_out), _ptr(grad_psw),
-                                       _stream(stream))
+        with torch.cuda.device(self.device):
+            st = self.lib.tbe_psw_gradient(ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables),
+                                           _ptr(weights), _ptr(indices), _ptr(offsets), _ptr(grad_out),
+                                           _ptr(grad_psw), _stream(stream, self.device))
         _check(self.lib, st, "tbe_psw_gradient")
         return grad_psw
 
@@ -307,9 +314,11 @@ class TableBatchedEmbedding:
         o = (options or self.options).c
         if o.long_threshold != self.options.c.long_threshold or o.chunk != self.options.c.chunk:
             raise ValueError("threshold/chunk differ from the options the workspace was sized for")
-        st = self.lib.tbe_backward_prepare(
-            ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables), _ptr(indices), _ptr(offsets),
-            _ptr(psw), _ptr(self.ws_backward), self.ws_backward.numel(), _ptr(stats), _stream(stream))
+        with torch.cuda.device(self.device):
+            st = self.lib.tbe_backward_prepare(
+                ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables), _ptr(indices), _ptr(offsets),
+                _ptr(psw), _ptr(self.ws_backward), self.ws_backward.numel(), _ptr(stats),
+                _stream(stream, self.device))
         _check(self.lib, st, "tbe_backward_prepare")
 
     def backward_update(self, weights, state, indices, offsets, grad_out, psw=None, optimizer="adagrad",
@@ -328,10 +337,11 @@ class TableBatchedEmbedding:
         if bool(o.prepared) != prepared:
             o = Options.from_buffer_copy(o)
             o.prepared = 1 if prepared else 0
-        st = self.lib.tbe_backward_update(
-            ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables), _ptr(weights), _ptr(state),
-            _ptr(indices), _ptr(offsets), _ptr(psw), _ptr(grad_out), opt, c_f32(lr), c_f32(eps),
-            _ptr(self.ws_backward), self.ws_backward.numel(), _ptr(stats), _stream(stream))
+        with torch.cuda.device(self.device):
+            st = self.lib.tbe_backward_update(
+                ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables), _ptr(weights), _ptr(state),
+                _ptr(indices), _ptr(offsets), _ptr(psw), _ptr(grad_out), opt, c_f32(lr), c_f32(eps),
+                _ptr(self.ws_backward), self.ws_backward.numel(), _ptr(stats), _stream(stream, self.device))
         _check(self.lib, st, "tbe_backward_update")
 
     def metadata(self) -> dict:
@@ -397,7 +407,8 @@ def tbe_backward_update_noalloc(tbe: TableBatchedEmbedding, weights, state, indi
     tbe._dev(stats, "stats", torch.int64, TBE_NUM_STATS)
     opt = {"sgd": TBE_OPT_SGD, "adagrad": TBE_OPT_ROWWISE_ADAGRAD}[optimizer]
     o = (options or tbe.options).c
-    st = fn(ctypes.byref(tbe.prob), ctypes.byref(o), ctypes.byref(tbe.tables), _ptr(weights), _ptr(state),
-            _ptr(indices), _ptr(offsets), _ptr(psw), _ptr(grad_out), opt, c_f32(lr), c_f32(eps), _ptr(stats),
-            _stream(stream))
+    with torch.cuda.device(tbe.device):
+        st = fn(ctypes.byref(tbe.prob), ctypes.byref(o), ctypes.byref(tbe.tables), _ptr(weights), _ptr(state),
+                _ptr(indices), _ptr(offsets), _ptr(psw), _ptr(grad_out), opt, c_f32(lr), c_f32(eps), _ptr(stats),
+                _stream(stream, tbe.device))
     _check(lib, st, "tbe_backward_update_noalloc")
