@@ -286,7 +286,19 @@ BwdCtx make_ctx(const Problem& P, const tbe_options& o, const BwdLayout& L, cons
 
 bool tables_ok(const tbe_tables* tab) {
   return tab != nullptr && tab->weight_offsets != nullptr && tab->D_offsets != nullptr &&
-         tab->row_offsets != nullptr;
+         tab->row_offsets != nullptr && aligned(tab->weight_offsets, 8) && aligned(tab->D_offsets, 4) &&
+         aligned(tab->row_offsets, 8);
+}
+
+// Element alignment of the buffers the kernels read or update element by element (a misaligned
+// one would fault on the device instead of failing here): indices and offsets by the index
+// width, fp32 arrays by 4 bytes, the int64 counters by 8 (they take 64-bit atomics).  NULL
+// passes; the callers check for NULL separately.
+bool elements_aligned(const Problem& P, const void* indices, const void* offsets, const float* psw,
+                      const void* f32_array, const int64_t* d_stats) {
+  const size_t ib = P.itype == TBE_I64 ? 8 : 4;
+  return aligned(indices, ib) && aligned(offsets, ib) && aligned(psw, 4) && aligned(f32_array, 4) &&
+         aligned(d_stats, 8);
 }
 
 // expand, sort, RLE and classify: the transpose half of the backward
@@ -382,6 +394,7 @@ tbe_status tbe_bounds_check(const tbe_problem* prob, const tbe_tables* tables, v
   if (st != TBE_OK) return st;
   if (!tables_ok(tables) || offsets == nullptr || (P.num_indices > 0 && indices == nullptr))
     return TBE_ERR_INVALID_ARG;
+  if (!elements_aligned(P, indices, offsets, nullptr, nullptr, d_stats)) return TBE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != TBE_OK) return st;
   const int grid = bounds_grid(dev);
@@ -398,6 +411,7 @@ tbe_status tbe_bounds_check_offsets(const tbe_problem* prob, const tbe_tables* t
   tbe_status st = make_problem(prob, &P);
   if (st != TBE_OK) return st;
   if (!tables_ok(tables) || offsets == nullptr) return TBE_ERR_INVALID_ARG;
+  if (!elements_aligned(P, nullptr, offsets, nullptr, nullptr, d_stats)) return TBE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != TBE_OK) return st;
   const int grid = bounds_grid(dev);
@@ -430,6 +444,7 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
   if ((P.weighted && psw == nullptr && P.num_indices > 0) || (!P.weighted && psw != nullptr))
     return TBE_ERR_INVALID_ARG;
   if (!aligned(weights, 16) || !aligned(out, 16)) return TBE_ERR_INVALID_ARG;
+  if (!elements_aligned(P, indices, offsets, psw, nullptr, d_stats)) return TBE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != TBE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -490,6 +505,7 @@ tbe_status tbe_psw_gradient(const tbe_problem* prob, const tbe_options* opt, con
       (P.num_indices > 0 && (indices == nullptr || grad_psw == nullptr)))
     return TBE_ERR_INVALID_ARG;
   if (!aligned(weights, 16) || !aligned(grad_out, 16)) return TBE_ERR_INVALID_ARG;
+  if (!elements_aligned(P, indices, offsets, nullptr, grad_psw, nullptr)) return TBE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != TBE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -511,6 +527,7 @@ tbe_status tbe_backward_prepare(const tbe_problem* prob, const tbe_options* opt,
   if ((P.weighted && psw == nullptr && P.num_indices > 0) || (!P.weighted && psw != nullptr))
     return TBE_ERR_INVALID_ARG;
   if (!aligned(ws, 256)) return TBE_ERR_INVALID_ARG;
+  if (!elements_aligned(P, indices, offsets, psw, nullptr, d_stats)) return TBE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != TBE_OK) return st;
   const BwdLayout L = make_bwd_layout(P, o, dev);
@@ -542,6 +559,7 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
   if ((P.weighted && psw == nullptr && P.num_indices > 0) || (!P.weighted && psw != nullptr))
     return TBE_ERR_INVALID_ARG;
   if (!aligned(weights, 16) || !aligned(grad_out, 16) || !aligned(ws, 256)) return TBE_ERR_INVALID_ARG;
+  if (!elements_aligned(P, indices, offsets, psw, state, d_stats)) return TBE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != TBE_OK) return st;
   const BwdLayout L = make_bwd_layout(P, o, dev);

@@ -109,3 +109,34 @@ def test_entry_points_validate_before_touching_the_device(lib):
 def test_library_refuses_to_hide_a_missing_build(tmp_path):
     with pytest.raises(tbe.TBEError):
         tbe.load(str(tmp_path / "missing.so"))
+
+
+def test_misaligned_buffers_are_rejected_on_the_host(lib):
+    """Buffers the kernels read element by element must be aligned to their element (8 bytes for
+    int64 indices, offsets, layout arrays and counters; 4 for fp32 arrays): a misaligned one is
+    an argument error here rather than a fault on the device."""
+    p, keep = _problem([8], [10])
+    o = tbe.Options()
+    lib.tbe_default_options(ctypes.byref(o))
+    ok = ctypes.c_void_p(256)
+    odd8, odd4 = ctypes.c_void_p(260), ctypes.c_void_p(258)
+    t_ok = tbe.Tables(ok, ok, ok)
+    for bad_tables in (tbe.Tables(odd8, ok, ok), tbe.Tables(ok, odd4, ok), tbe.Tables(ok, ok, odd8)):
+        assert lib.tbe_forward(ctypes.byref(p), ctypes.byref(o), ctypes.byref(bad_tables), ok, ok, ok, None, ok,
+                               None, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
+    # int64 indices / offsets at a 4-byte boundary
+    assert lib.tbe_forward(ctypes.byref(p), ctypes.byref(o), ctypes.byref(t_ok), ok, odd8, ok, None, ok,
+                           None, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
+    assert lib.tbe_bounds_check_offsets(ctypes.byref(p), ctypes.byref(t_ok), odd8, ok, 4096, None,
+                                        None) == tbe.TBE_ERR_INVALID_ARG
+    # the int64 counters
+    assert lib.tbe_bounds_check(ctypes.byref(p), ctypes.byref(t_ok), ok, ok, ok, 4096, odd8,
+                                None) == tbe.TBE_ERR_INVALID_ARG
+    # the fp32 Adagrad state
+    assert lib.tbe_backward_update(ctypes.byref(p), ctypes.byref(o), ctypes.byref(t_ok), ok, odd4, ok, ok, None,
+                                   ok, tbe.TBE_OPT_ROWWISE_ADAGRAD, 0.1, 1e-8, ok, 1 << 30, None,
+                                   None) == tbe.TBE_ERR_INVALID_ARG
+    # int32 ids are fine at a 4-byte boundary but not at a 2-byte one
+    p32, keep32 = _problem([8], [10], itype=tbe.TBE_I32)
+    assert lib.tbe_forward(ctypes.byref(p32), ctypes.byref(o), ctypes.byref(t_ok), ok, ctypes.c_void_p(258), ok,
+                           None, ok, None, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
