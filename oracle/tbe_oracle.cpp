@@ -13,6 +13,8 @@
  *   [TUT]  "Table-Batched Embeddings in Triton: Gather, Pool, and Run-Length Backward"
  * What each function follows is stated beside it.  Accumulation is fp64 throughout, as the
  * oracle's precision; results stored in a narrower type are rounded to nearest, ties to even.
+ * Parity unpinned: oracle_bounds_repair (the pages give no repair rule; see tbe_oracle.h).
+ * Every other function is pinned by the tests to values or laws outside this file.
  */
 #include "tbe_oracle.h"
 

@@ -42,7 +42,9 @@ int oracle_version(void);
  *   clamped into [0, offsets[T*B]] and raised to the previous (repaired) offset so that the
  *   sequence never decreases; then every index of bag (t, b) outside [0, E[t]) becomes 0.
  * Repairs are applied in place.  repaired_per_table[T] (nullable) receives the number of
- * repaired indices per table; *repaired_offsets (nullable) the number of changed offsets. */
+ * repaired indices per table; *repaired_offsets (nullable) the number of changed offsets.
+ * PARITY UNPINNED: the pages state no repair rule, so nothing outside this oracle fixes its
+ * result; the tests check it only against hand-worked cases of the rule written above. */
 int oracle_bounds_repair(int32_t T, int64_t B, int64_t num_indices, const int64_t* E, int32_t itype,
                          void* indices, void* offsets, int64_t* repaired_per_table,
                          int64_t* repaired_offsets);
