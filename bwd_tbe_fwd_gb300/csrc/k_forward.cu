@@ -635,6 +635,108 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaMinBlocks) fwd_tma_gather_ker
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// Very long bags of 16-bit tables, summed again in segments.  The gathers above keep one fp32
+// running sum per lane over a whole bag, which is all the fp32 accumulation the pages prescribe
+// needs for ordinary bags; but a bag of 10^5 - 10^6 lookups of a few hot rows adds the same value
+// into one fp32 sum 10^5 times, each addition rounding the same way, and drifts by about 2e-3 of
+// the sum (at kLongBag = 16384 lookups the same drift is under 1e-4).  This pass finds the bags
+// longer than kLongBag lookups and writes their output rows again from sums of kSegment-lookup
+// segments, each segment summed in fp32 and the segment sums added in fp32, which keeps the error
+// near (kSegment + L / kSegment) roundings.  It runs after the gather (and after the counts x
+// table path, whose scalar tail past the 256th id also sums sequentially), reads ids the forward
+// has already repaired (skipping out-of-range ones without counting them: the gather counted
+// them), and leaves every other bag alone: for batches without such bags it costs one coalesced
+// read of the offsets (the bag walk is a rare path, kept out of the scan's registers).
+// ------------------------------------------------------------------------------------------
+constexpr int kLongBag = 16384;
+constexpr int kSegment = 1024;
+constexpr int kLongThreads = 128;
+
+template <typename WT, typename IT, bool PSW>
+__global__ void __launch_bounds__(kLongThreads, 8) fwd_long_bags_kernel(FwdArgs a) {
+  using IO = VecIO<WT, 16>;
+  constexpr int NE = IO::N;
+  constexpr int UNROLL = PSW ? 4 : 8;
+  const unsigned FULL = 0xffffffffu;
+  const int lane = lane_id();
+  const int N = static_cast<int>(a.num_indices);
+  const int64_t units = a.unit_end - a.unit_begin;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t base = warp0 * kWarp; base < units; base += warps * kWarp) {
+    const int64_t u = a.unit_begin + base + lane;
+    int s = 0, e = 0;
+    if (base + lane < units) {
+      s = static_cast<int>(clamp64(ld_int<IT>(a.offsets, u), 0, N));
+      e = static_cast<int>(clamp64(ld_int<IT>(a.offsets, u + 1), s, N));
+    }
+    unsigned m = __ballot_sync(FULL, e - s > kLongBag);
+    while (m != 0) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1;
+      const int64_t ub = a.unit_begin + base + j;
+      const int bs = __shfl_sync(FULL, s, j), be = __shfl_sync(FULL, e, j);
+      const int t = static_cast<int>(ub / a.B);
+      const int64_t b = ub - static_cast<int64_t>(t) * a.B;
+      const int col0 = __ldg(a.doff + t);
+      const int nvec = (__ldg(a.doff + t + 1) - col0) * static_cast<int>(sizeof(WT)) / 16;
+      const int E = static_cast<int>(__ldg(a.roff + t + 1) - __ldg(a.roff + t));
+      const uint4* table = reinterpret_cast<const uint4*>(static_cast<const WT*>(a.weights) + __ldg(a.woff + t));
+      const int lpr = nvec >= kWarp ? kWarp : (nvec <= 1 ? 1 : 1 << (32 - __clz(nvec - 1)));
+      const int rps = kWarp / lpr, slot = lane / lpr, vi = lane % lpr;
+      const float inv = a.mean ? 1.0f / static_cast<float>(be - bs) : 1.0f;
+      float* orow = a.out + b * a.total_D + col0;
+      // one pass over the bag per 32 vectors of the row (one pass for rows of up to 512 bytes)
+      for (int c = vi; c - vi < nvec; c += kWarp) {
+        float tot[NE], seg[NE];
+#pragma unroll
+        for (int i = 0; i < NE; ++i) tot[i] = seg[i] = 0.0f;
+        for (int g0 = bs; g0 < be; g0 += kSegment) {
+          const int g1 = be - g0 > kSegment ? g0 + kSegment : be;
+          for (int p = g0; p < g1; p += rps * UNROLL) {
+            uint4 v[UNROLL];
+            float w[UNROLL];
+#pragma unroll
+            for (int q = 0; q < UNROLL; ++q) {
+              const int pos = p + q * rps + slot;  // this slot's row of load step q
+              int64_t id = -1;
+              w[q] = 0.0f;
+              if (pos < g1) {
+                id = ld_int<IT>(a.indices, pos);
+                if (id < 0 || id >= E) id = -1;  // skipped (and counted) by the gather
+                else if (PSW) w[q] = __ldg(a.psw + pos);
+              }
+              v[q] = make_uint4(0, 0, 0, 0);
+              if (id >= 0 && c < nvec) v[q] = __ldg(table + id * nvec + c);
+            }
+#pragma unroll
+            for (int q = 0; q < UNROLL; ++q) {
+              float f[NE];
+              IO::unpack(v[q], f);
+#pragma unroll
+              for (int i = 0; i < NE; ++i) seg[i] += PSW ? f[i] * w[q] : f[i];
+            }
+          }
+          // the segment's sum over the row slots, added into the bag's total
+#pragma unroll
+          for (int i = 0; i < NE; ++i) {
+            float v = seg[i];
+            for (int o = lpr; o < kWarp; o <<= 1) v += __shfl_xor_sync(FULL, v, o);
+            tot[i] += v;
+            seg[i] = 0.0f;
+          }
+        }
+        if (slot == 0 && c < nvec) {
+#pragma unroll
+          for (int i = 0; i < NE; ++i) tot[i] *= inv;
+          store_out(orow + c * NE, tot);
+        }
+      }
+    }
+  }
+}
+
 // Bags per work item: about eight items per resident warp, at most 32 bags each.
 inline int bags_per_item_for(int64_t tables, int64_t B, int64_t warps) {
   const int64_t per_item = tables * B / (8 * warps);
@@ -841,6 +943,50 @@ cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const
     case TBE_F16: return dispatch_it<__half>(a, P.itype, has_psw, vb, maxv, dev, s);
     default: return dispatch_it<__nv_bfloat16>(a, P.itype, has_psw, vb, maxv, dev, s);
   }
+}
+
+// Long bags of 16-bit tables in units [unit_begin, unit_end), summed again in segments (see
+// fwd_long_bags_kernel); fp32 tables sum in fp64 and need no second pass.
+cudaError_t launch_forward_long_bags(const Problem& P, const tbe_tables& tab, const void* weights,
+                                     const void* indices, const void* offsets, const float* psw, float* out,
+                                     int64_t unit_begin, int64_t unit_end, const DeviceInfo& dev, cudaStream_t s) {
+  if (unit_end <= unit_begin || P.wbytes != 2 || P.vec_bytes != 16 || P.max_D * P.wbytes > 16 * 4 * kWarp)
+    return cudaSuccess;
+  if (P.num_indices <= kLongBag) return cudaSuccess;  // no bag can be long
+  FwdArgs a{};
+  a.weights = weights;
+  a.woff = tab.weight_offsets;
+  a.doff = tab.D_offsets;
+  a.roff = tab.row_offsets;
+  a.indices = const_cast<void*>(indices);  // read only
+  a.offsets = offsets;
+  a.psw = psw;
+  a.out = out;
+  a.B = P.B;
+  a.num_indices = P.num_indices;
+  a.unit_begin = unit_begin;
+  a.unit_end = unit_end;
+  a.total_D = P.total_D;
+  a.mean = P.pooling == TBE_POOL_MEAN;
+  const int64_t warps_needed = (unit_end - unit_begin + kWarp - 1) / kWarp;
+  int64_t blocks = (warps_needed + (kLongThreads / kWarp) - 1) / (kLongThreads / kWarp);
+  const int64_t cap = static_cast<int64_t>(dev.sms) * 8;
+  if (blocks > cap) blocks = cap;
+  const bool w = psw != nullptr;
+  const bool i32 = P.itype == TBE_I32;
+  if (P.wdtype == TBE_F16) {
+    if (i32) w ? fwd_long_bags_kernel<__half, int32_t, true><<<blocks, kLongThreads, 0, s>>>(a)
+             : fwd_long_bags_kernel<__half, int32_t, false><<<blocks, kLongThreads, 0, s>>>(a);
+    else w ? fwd_long_bags_kernel<__half, int64_t, true><<<blocks, kLongThreads, 0, s>>>(a)
+           : fwd_long_bags_kernel<__half, int64_t, false><<<blocks, kLongThreads, 0, s>>>(a);
+  } else {
+    if (i32) w ? fwd_long_bags_kernel<__nv_bfloat16, int32_t, true><<<blocks, kLongThreads, 0, s>>>(a)
+             : fwd_long_bags_kernel<__nv_bfloat16, int32_t, false><<<blocks, kLongThreads, 0, s>>>(a);
+    else w ? fwd_long_bags_kernel<__nv_bfloat16, int64_t, true><<<blocks, kLongThreads, 0, s>>>(a)
+           : fwd_long_bags_kernel<__nv_bfloat16, int64_t, false><<<blocks, kLongThreads, 0, s>>>(a);
+  }
+  note_launch();
+  return cudaGetLastError();
 }
 
 // The gradient with respect to the per-sample weights: the gather's walk in dot mode over every

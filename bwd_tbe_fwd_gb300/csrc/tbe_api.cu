@@ -470,6 +470,8 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
     cudaError_t e = launch_forward_gather(P, *tables, weights, indices, offsets, psw, out, t0 * P.B,
                                           t1 * P.B, o.fused_bounds != 0, o.gather == TBE_GATHER_TMA, stats,
                                           dev, s);
+    if (e == cudaSuccess)  // bags of more than a segment of lookups, summed again in segments
+      e = launch_forward_long_bags(P, *tables, weights, indices, offsets, psw, out, t0 * P.B, t1 * P.B, dev, s);
     if (e != cudaSuccess) return cuda_status(e);
     t0 = t1;
   }
@@ -477,6 +479,8 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
   for (int t : hist) {
     cudaError_t e = launch_forward_histogram(P, *tables, weights, indices, offsets, out, t, o.fused_bounds != 0,
                                              stats, dev, s);
+    if (e == cudaSuccess)
+      e = launch_forward_long_bags(P, *tables, weights, indices, offsets, psw, out, t * P.B, (t + 1) * P.B, dev, s);
     if (e != cudaSuccess) return cuda_status(e);
   }
   record(o, TBE_FWD_EV_HISTOGRAM, s);

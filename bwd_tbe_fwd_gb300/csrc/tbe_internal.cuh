@@ -161,6 +161,10 @@ cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const
                                   int64_t unit_begin, int64_t unit_end, bool fused_bounds, bool allow_tma,
                                   unsigned long long* stats, const DeviceInfo& dev, cudaStream_t s);
 
+cudaError_t launch_forward_long_bags(const Problem& P, const tbe_tables& tab, const void* weights,
+                                     const void* indices, const void* offsets, const float* psw, float* out,
+                                     int64_t unit_begin, int64_t unit_end, const DeviceInfo& dev, cudaStream_t s);
+
 bool histogram_supported();
 cudaError_t launch_backward_histogram(const Problem& P, const BwdCtx& c, int table, void* hist_ws,
                                       tbe_optimizer opt, const DeviceInfo& dev, cudaStream_t s);

@@ -210,26 +210,22 @@ def test_offsets_only_bounds_check_then_fused_forward_and_backward():
 
 def corrupt_offsets(off: np.ndarray, seed: int) -> np.ndarray:
     """Offsets broken in every way the repair rule covers: a first offset that is not 0, negative
-    ones, decreases, values past the last offset, one jump ahead over about TB/200 offsets (the
-    prefix maximum raises all of them to the jump, across the segments of several CTAs) and a
-    last offset above num_indices.  Values past the end sit in the last 1% of the offsets only:
-    clamped to N they raise every later offset to N, so one early in the batch would merge most
-    of it into one bag of ~N lookups, whose fp32 sum drifts past the fp16 tolerance (a hot row's
-    value added 10^5 times rounds the same way each time)."""
+    ones, decreases, values past the last offset anywhere in the batch (clamped to N, each one
+    raises every later offset to N, so the bag before the first of them takes the rest of the
+    batch: hundreds of thousands of lookups of hot rows in one pooled sum), one jump far ahead
+    (the prefix maximum raises every offset after it up to the jump, across the segments of many
+    CTAs) and a last offset above num_indices."""
     rng = np.random.default_rng(seed)
     o = off.astype(np.int64).copy()
     TB = len(o) - 1
     N = int(o[-1])
     k = max(1, TB // 200)
-    tail0 = TB - max(2, TB // 100)
-    pos = rng.choice(np.arange(1, tail0), size=2 * k, replace=False)
-    neg, dec = pos[:k], pos[k:]
+    pos = rng.choice(np.arange(1, TB), size=3 * k, replace=False)
+    neg, dec, past = pos[:k], pos[k:2 * k], pos[2 * k:]
     o[neg] = -rng.integers(1, 1000, size=k)
     o[dec] = o[dec] - rng.integers(1, 64, size=k)
-    past = rng.choice(np.arange(tail0, TB), size=max(1, TB // 1000), replace=False)
-    o[past] = N + rng.integers(1, 1000, size=len(past))
-    j = TB // 3
-    o[j] = o[j + max(1, TB // 200)]
+    o[past] = N + rng.integers(1, 1000, size=k)
+    o[TB // 3] = o[2 * TB // 3]
     o[0] = 7
     o[TB] = N + 50
     return o.astype(off.dtype)
@@ -332,3 +328,34 @@ def test_graph_capture_no_host_sync():
     # reproducible; compare within the fp16 tolerance
     assert torch.allclose(w.float(), w_eager.float(), rtol=2e-3, atol=1e-6)
     assert torch.allclose(state, s_eager, rtol=1e-5, atol=0)
+
+
+@pytest.mark.parametrize("gather", ["register", "tma"])
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("lengths", [(600_000, 3, 7), (1_050_000,)])
+def test_very_long_bags_hold_the_tolerance(lengths, D, gather):
+    """Bags of 6*10^5 and 1.05*10^6 lookups of Zipf-hot fp16 rows (the stress workload's id law
+    over a table of 61 rows, so the hottest rows are each added 4*10^4 - 10^5 times into one bag)
+    beside short ones: every pooled element within the fp16 bound of the oracle's exact sum.  At
+    D = 256 every lane of the register gather sums one column over the whole bag (at D = 128 two
+    row slots share it), which is where a single fp32 running sum drifts furthest."""
+    import dataclasses
+    from synth.configs import LengthSpec
+    from bwd_tbe_fwd_gb300.tbe import TBE_GATHER_REGISTER, TBE_GATHER_TMA
+    base = get_config("c3").shrink(B=len(lengths), T=1, E_div=65536, name=f"long_bags_{lengths[0]}_D{D}")
+    cfg = dataclasses.replace(base, tables=tuple(dataclasses.replace(t, D=D, lengths=LengthSpec("fixed", 1))
+                                                 for t in base.tables))
+    c = Case(cfg, bounds_check=False)
+    # bag lengths as given, ids drawn from the table's law by a second, longer draw
+    big = dataclasses.replace(cfg, B=sum(lengths), name=cfg.name + "_ids")
+    from synth import make_batch
+    draw = make_batch(big)
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(c.off_h.dtype)
+    idx = draw.indices[:off[-1]].astype(c.idx_h.dtype)
+    c.idx_h, c.off_h = idx.copy(), off.copy()
+    c.idx_d = torch.from_numpy(idx.copy()).cuda()
+    c.off_d = torch.from_numpy(off.copy()).cuda()
+    c.tbe = type(c.tbe)(cfg.D, cfg.E, cfg.B, len(idx), c.tbe.weight_dtype, c.tbe.index_dtype, device="cuda")
+    hot = np.bincount(idx[:lengths[0]].astype(np.int64)).max()
+    assert hot > 40_000, hot
+    c.forward(options=TBEOptions(gather={"register": TBE_GATHER_REGISTER, "tma": TBE_GATHER_TMA}[gather]))
