@@ -62,6 +62,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tables", type=int, default=0,
                     help="keep only the first T tables of the workload (small cases for profiling)")
+    ap.add_argument("--bags", type=int, default=0,
+                    help="bags per table (B) of the workload (small cases for profiling)")
+    ap.add_argument("--per-config", default="c1,c2,c4,c5",
+                    help="comma-separated other workloads timed after the headline one (empty: none)")
     ap.add_argument("--cpu-sample-bags", type=int, default=0,
                     help="bags per table in the CPU oracle sample (0: sized for ~15 s)")
     return ap.parse_args()
@@ -173,10 +177,12 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None, bounds_ids=True):
     nch = -(-L[~short] // chunk)
     upd_long = int(np.sum(L[~short] * (4 + pw + Dr[~short] * 4) + nch * Dr[~short] * 8
                           + 2 * Dr[~short] * wb + 8 + Dr[~short] * 4))
+    n_hist = int(np.sum(st["per_table"][hist]))
     return dict(bounds=bounds, gather=fwd, histogram=hist_bytes, histogram_flops=hist_flops, expand=expand,
                 sort=sort, rle=rle, classify=classify, short=upd_short, long=upd_long, apply=0,
                 bwd_histogram=bwd_hist, bwd_histogram_flops=bwd_hist_flops, lookups_sorted=N, psw_grad=psw_grad,
                 lookups_short=int(L[short].sum()), lookups_long=int(L[~short].sum()),
+                lookups_gathered=st["N"] - n_hist, lookups_histogram=n_hist,
                 runs_short=int(short.sum()), runs_long=int((~short).sum()), passes=passes)
 
 
@@ -324,9 +330,17 @@ KERNEL_SOURCES = {
     "histogram": [_CSRC + "k_hist.cu", _CSRC + "tbe_internal.cuh"],
     "bwd_histogram": [_CSRC + "k_hist.cu", _CSRC + "tbe_internal.cuh"],
 }
+# the lookups a stage's DRAM traffic is normalised by (ncu captures on smaller cases of the same
+# workload, scaled to the full batch by these counts)
+STAGE_UNITS = {"gather": "lookups_gathered", "short": "lookups_short", "long": "lookups_long",
+               "sort": "lookups_sorted", "histogram": "lookups_histogram", "bwd_histogram": "lookups_histogram"}
 
 
-def profiled_traffic(stage: str, workload: str):
+def profiled_traffic(stage: str, workload: str, model: dict):
+    """DRAM bytes (read + write) of one launch of the stage's kernel(s) on the full workload, from
+    the ncu captures recorded in profiles/dram_traffic.json (bytes per lookup, scaled by the
+    stage's lookups), with the capture's tensor-pipe utilisation if it has one; None when no
+    capture exists or the kernel source changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path) or stage not in KERNEL_SOURCES:
         return None
@@ -335,7 +349,11 @@ def profiled_traffic(stage: str, workload: str):
     rec = table.get(f"{workload}:{stage}")
     if not rec or rec.get("source_digest") != source_digest(KERNEL_SOURCES[stage]):
         return None
-    return rec.get("bytes_per_launch")
+    units = model.get(STAGE_UNITS[stage], 0)
+    if not units or "bytes_per_lookup" not in rec:
+        return None
+    return {"bytes": int(round(rec["bytes_per_lookup"] * units)), "from": rec.get("from"),
+            "tensor_pipe_pct": rec.get("tensor_pipe_pct")}
 
 
 def peaks():
@@ -350,14 +368,197 @@ def peaks():
 # ------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------
-def run_ours(args):
-    import ctypes
+class Workload:
+    """One workload on the device: the batch, the library object, weights, state, gradients and
+    the step of the hot path (bounds check, forward, backward update) through the C-ABI."""
 
+    def __init__(self, args, cfg, dev, count_launches=False):
+        import ctypes
+
+        import torch
+        from bwd_tbe_fwd_gb300 import TableBatchedEmbedding, TBEOptions
+        from synth import make_batch
+        from synth.gen import grad_out_tensor, torch_dtype, weights_tensor
+
+        self.args, self.cfg, self.dev = args, cfg, dev
+        self.batch = make_batch(cfg)
+        self.st = batch_stats(cfg, self.batch)
+        self.opts = TBEOptions(long_mode={"auto": 0, "two_kernel": 1, "fused": 2}[args.long_mode],
+                               scheduler={"grid": 0, "persistent": 1, "clc": 2}[args.scheduler],
+                               merge={"atomic": 0, "bulk": 1}[args.merge],
+                               gather={"register": 0, "tma": 1}[args.gather],
+                               fused_bounds=1 if args.bounds == "fused" else 0,
+                               classify_mode={"atomic": 0, "ordered": 1}[args.classify])
+        itype = torch.int32 if cfg.itype == "i32" else torch.int64
+        self.tbe = TableBatchedEmbedding(cfg.D, cfg.E, cfg.B, self.batch.N, torch_dtype(cfg.wdtype), itype,
+                                         weighted=cfg.weighted, long_bags=[t.histogram for t in cfg.tables],
+                                         device=dev, options=self.opts, pooling=args.pooling)
+        self.psw_grad = args.psw_grad and cfg.weighted
+        self.grad_psw = torch.empty(self.batch.N, dtype=torch.float32, device=dev) if self.psw_grad else None
+        self.weights = weights_tensor(cfg, device=dev)
+        self.state = (torch.zeros(cfg.total_rows, dtype=torch.float32, device=dev)
+                      if cfg.optimizer == "adagrad" else None)
+        self.grad = grad_out_tensor(cfg, device=dev)
+        self.idx_h = torch.from_numpy(self.batch.indices)
+        self.off_h = torch.from_numpy(self.batch.offsets)
+        self.psw_h = None if self.batch.psw is None else torch.from_numpy(self.batch.psw)
+        self.inputs = (self.idx_h.to(dev), self.off_h.to(dev), None if self.psw_h is None else self.psw_h.to(dev))
+        self.out = torch.empty(cfg.B, cfg.total_D, dtype=torch.float32, device=dev)
+        self.stats = torch.zeros(8, dtype=torch.int64, device=dev)
+        self.launches = ctypes.c_int64(0)
+        if count_launches:
+            self.opts.count_launches(self.launches)
+        self.main = torch.cuda.current_stream(dev)
+        self.side = torch.cuda.Stream(device=dev, priority=-1)  # its CTAs go first when SMs free up
+        self.model = byte_model(cfg, self.st, self.opts.c.long_threshold, self.opts.c.chunk,
+                                bounds_ids=args.bounds != "fused")
+
+    def step(self, fev=None, bev=None, bounds_ev=None, pev=None, gev=None, ins=None):
+        args, tbe, cfg = self.args, self.tbe, self.cfg
+        idx, off, psw = ins if ins is not None else self.inputs
+        if bounds_ev is not None:
+            bounds_ev[0].record()
+        tbe.bounds_check(idx, off, stats=self.stats, offsets_only=args.bounds == "fused")
+        if bounds_ev is not None:
+            bounds_ev[1].record()
+        if args.hoist == "on":
+            # the transpose needs only the repaired ids: run it beside the forward gather
+            self.side.wait_stream(self.main)
+            self.opts.with_events(pev)
+            tbe.backward_prepare(idx, off, psw=psw, stats=self.stats, stream=self.side)
+        self.opts.with_events(fev)
+        tbe.forward(self.weights, idx, off, psw=psw, out=self.out, stats=self.stats)
+        if args.hoist == "on":
+            self.main.wait_stream(self.side)
+        if self.psw_grad:
+            if gev is not None:
+                gev[0].record()
+            tbe.psw_gradient(self.weights, idx, off, self.grad, grad_psw=self.grad_psw)
+            if gev is not None:
+                gev[1].record()
+        self.opts.with_events(bev)
+        tbe.backward_update(self.weights, self.state, idx, off, self.grad, psw=psw, optimizer=cfg.optimizer,
+                            lr=cfg.lr, eps=cfg.eps, stats=self.stats, prepared=args.hoist == "on")
+        self.opts.with_events(None)
+
+    def timed(self, K, W, world=1, clocks=None):
+        """W untimed steps, then K timed ones (CUDA events on the launching stream, barrier and
+        synchronize on both sides); per-stage device times from the library's stage events."""
+        import torch
+        from bwd_tbe_fwd_gb300.tbe import BWD_STAGES, TBE_BWD_NUM_EVENTS, TBE_FWD_NUM_EVENTS
+        for _ in range(W):
+            self.step()
+        torch.cuda.synchronize()
+        mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        fevs = [[mk() for _ in range(TBE_FWD_NUM_EVENTS)] for _ in range(K)]
+        bevs = [[mk() for _ in range(TBE_BWD_NUM_EVENTS)] for _ in range(K)]
+        bnds = [[mk(), mk()] for _ in range(K)]
+        pevs = [[mk() for _ in range(TBE_BWD_NUM_EVENTS)] for _ in range(K)]
+        gevs = [[mk(), mk()] for _ in range(K)]
+        e0, e1 = mk(), mk()
+        hoist = self.args.hoist == "on"
+        self.launches.value = 0
+        barrier(world)
+        torch.cuda.synchronize()
+        if clocks is not None:
+            clocks.start()
+            time.sleep(0.4)  # let the sampler take a first sample
+        e0.record()
+        for k in range(K):
+            self.step(fevs[k], bevs[k], bnds[k], pevs[k] if hoist else None, gevs[k])
+        e1.record()
+        torch.cuda.synchronize()
+        clk = clocks.stop() if clocks is not None else None
+        barrier(world)
+        stage_ms = {"bounds": np.mean([b[0].elapsed_time(b[1]) for b in bnds]),
+                    "psw_grad": np.mean([g[0].elapsed_time(g[1]) for g in gevs]) if self.psw_grad else 0.0,
+                    "gather": np.mean([f[0].elapsed_time(f[1]) for f in fevs]),
+                    "histogram": np.mean([f[1].elapsed_time(f[2]) for f in fevs])}
+        for i, name in enumerate(BWD_STAGES):
+            # with the transpose hoisted, its stages ran on the side stream between the prepare's events
+            src = pevs if hoist and name in ("expand", "sort", "rle", "classify") else bevs
+            stage_ms[name] = float(np.mean([b[i].elapsed_time(b[i + 1]) for b in src]))
+        return {"ms_total": e0.elapsed_time(e1), "stage_ms": stage_ms, "clocks": clk,
+                "launches": int(self.launches.value),
+                "fwd_ms": float(np.mean([f[0].elapsed_time(f[2]) for f in fevs])),
+                "bwd_ms": float(np.mean([b[0].elapsed_time(b[-1]) for b in bevs]))}
+
+    def roofline(self, stage_ms, peak, peak_kind):
+        """Per-stage algorithmic bytes and, where an ncu capture of the current kernel source exists,
+        DRAM bytes; the roofline of the slowest kernel stage against the HBM copy peak, by DRAM bytes.
+        Algorithmic bytes count every row read, most of which the skewed ids make L2 hits, so their
+        rate is an L2-served figure, not a fraction of HBM."""
+        model, cfg = self.model, self.cfg
+        stages = {}
+        for name, ms in stage_ms.items():
+            gb = model.get(name, 0) / 1e9
+            rec = {"ms": round(float(ms), 4), "algorithmic_GB": round(gb, 4),
+                   "algorithmic_GBps": round(gb / (ms / 1e3), 1) if ms > 0 and gb > 0 else None}
+            tr = profiled_traffic(name, cfg.name, model) if ms > 0 else None
+            if tr is not None:
+                rec["dram_GB"] = round(tr["bytes"] / 1e9, 4)
+                rec["dram_GBps"] = round(tr["bytes"] / 1e9 / (ms / 1e3), 1)
+                rec["dram_frac"] = round(tr["bytes"] / 1e9 / (ms / 1e3) / peak, 4)
+                if tr.get("tensor_pipe_pct") is not None:
+                    rec["tensor_pipe_pct"] = tr["tensor_pipe_pct"]
+            stages[name] = rec
+        for name in ("histogram", "bwd_histogram"):
+            if model[name + "_flops"] > 0 and stage_ms[name] > 0:
+                stages[name]["tensor_TFLOPs"] = round(model[name + "_flops"] / (stage_ms[name] / 1e3) / 1e12, 3)
+        kernel_stages = ("gather", "histogram", "short", "long", "bwd_histogram")
+        dom = max(kernel_stages, key=lambda n: stage_ms[n])
+        tr = profiled_traffic(dom, cfg.name, model)
+        ms = stage_ms[dom]
+        achieved = tr["bytes"] / 1e9 / (ms / 1e3) if tr is not None else None
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1) if achieved is not None else None,
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / peak, 4) if achieved is not None else None,
+                "traffic": tr["bytes"] if tr is not None else None,
+                "traffic_from": tr["from"] if tr is not None else None,
+                "algorithmic_bytes": model[dom],
+                "algorithmic_GBps": round(model[dom] / 1e9 / (ms / 1e3), 1),
+                "basis": "achieved = ncu DRAM bytes (read + write) of the kernel per launch, from a capture of "
+                         "the current kernel source scaled to this batch by its lookups, over the kernel's CUDA-event "
+                         "time; algorithmic_GBps counts every row read (mostly L2 hits) and is not an HBM fraction"}
+        return stages, roof
+
+    def release(self):
+        import torch
+        for k in ("tbe", "weights", "state", "grad", "inputs", "out", "stats", "grad_psw"):
+            setattr(self, k, None)
+        torch.cuda.empty_cache()
+
+
+def per_config_lines(args, dev, K, W, peak, peak_kind):
+    """The other workloads, each timed in this process after the headline one."""
+    from synth import get_config
+    res = {}
+    for name in args.per_config.split(","):
+        name = name.strip()
+        if not name or name == args.config:
+            continue
+        cfg = get_config(name)
+        wl = Workload(args, cfg, dev)
+        t = wl.timed(K, W)
+        stages, roof = wl.roofline(t["stage_ms"], peak, peak_kind)
+        line = {"workload": f"{cfg.name}: {cfg.description}", "lookups_per_step": wl.st["N"],
+                "ms_per_step": round(t["ms_total"] / K, 4),
+                "value": wl.st["N"] * K / (t["ms_total"] / 1e3), "unit": "lookups/s",
+                "fwd_ms": round(t["fwd_ms"], 4), "bwd_ms": round(t["bwd_ms"], 4), "steps": K, "warmup": W,
+                "roofline": roof,
+                "dram_frac": {n: stages[n].get("dram_frac") for n in ("gather", "short", "long", "histogram",
+                                                                     "bwd_histogram") if stages[n]["ms"] > 0.003},
+                "stages": stages}
+        res[cfg.name] = line
+        wl.release()
+        del wl
+    return res
+
+
+def run_ours(args):
     import torch
-    from bwd_tbe_fwd_gb300 import TableBatchedEmbedding, TBEOptions, build
-    from bwd_tbe_fwd_gb300.tbe import BWD_STAGES, TBE_BWD_NUM_EVENTS, TBE_FWD_NUM_EVENTS
-    from synth import get_config, make_batch
-    from synth.gen import grad_out_tensor, torch_dtype, weights_tensor
+    from bwd_tbe_fwd_gb300 import build
+    from synth import get_config
 
     world, rank, local = dist_setup("nccl")
     build.build()
@@ -365,128 +566,27 @@ def run_ours(args):
     cfg = get_config(args.config)
     if args.tables:
         cfg = cfg.shrink(T=args.tables, name=f"{cfg.name}[T={args.tables}]")
-    batch = make_batch(cfg)
-    st = batch_stats(cfg, batch)
-    opts = TBEOptions(long_mode={"auto": 0, "two_kernel": 1, "fused": 2}[args.long_mode],
-                      scheduler={"grid": 0, "persistent": 1, "clc": 2}[args.scheduler],
-                      merge={"atomic": 0, "bulk": 1}[args.merge],
-                      gather={"register": 0, "tma": 1}[args.gather],
-                      fused_bounds=1 if args.bounds == "fused" else 0,
-                      classify_mode={"atomic": 0, "ordered": 1}[args.classify])
-    itype = torch.int32 if cfg.itype == "i32" else torch.int64
-    tbe = TableBatchedEmbedding(cfg.D, cfg.E, cfg.B, batch.N, torch_dtype(cfg.wdtype), itype,
-                                weighted=cfg.weighted, long_bags=[t.histogram for t in cfg.tables],
-                                device=dev, options=opts, pooling=args.pooling)
-    psw_grad = args.psw_grad and cfg.weighted
-    grad_psw = torch.empty(batch.N, dtype=torch.float32, device=dev) if psw_grad else None
-    weights = weights_tensor(cfg, device=dev)
-    state = torch.zeros(cfg.total_rows, dtype=torch.float32, device=dev) if cfg.optimizer == "adagrad" else None
-    grad = grad_out_tensor(cfg, device=dev)
-    idx_h = torch.from_numpy(batch.indices)
-    off_h = torch.from_numpy(batch.offsets)
-    psw_h = None if batch.psw is None else torch.from_numpy(batch.psw)
-    idx = idx_h.to(dev)
-    off = off_h.to(dev)
-    psw = None if psw_h is None else psw_h.to(dev)
-    out = torch.empty(cfg.B, cfg.total_D, dtype=torch.float32, device=dev)
-    stats = torch.zeros(8, dtype=torch.int64, device=dev)
-    launches = ctypes.c_int64(0)
-    opts.count_launches(launches)
-
-    main = torch.cuda.current_stream(dev)
-    side = torch.cuda.Stream(device=dev, priority=-1)  # its CTAs go first when SMs free up
-    inputs = (idx, off, psw)
-
-    def step(fev=None, bev=None, bounds_ev=None, pev=None, gev=None, ins=None):
-        idx, off, psw = ins if ins is not None else inputs
-        if bounds_ev is not None:
-            bounds_ev[0].record()
-        tbe.bounds_check(idx, off, stats=stats, offsets_only=args.bounds == "fused")
-        if bounds_ev is not None:
-            bounds_ev[1].record()
-        if args.hoist == "on":
-            # the transpose needs only the repaired ids: run it beside the forward gather
-            side.wait_stream(main)
-            opts.with_events(pev)
-            tbe.backward_prepare(idx, off, psw=psw, stats=stats, stream=side)
-        opts.with_events(fev)
-        tbe.forward(weights, idx, off, psw=psw, out=out, stats=stats)
-        if args.hoist == "on":
-            main.wait_stream(side)
-        if psw_grad:
-            if gev is not None:
-                gev[0].record()
-            tbe.psw_gradient(weights, idx, off, grad, grad_psw=grad_psw)
-            if gev is not None:
-                gev[1].record()
-        opts.with_events(bev)
-        tbe.backward_update(weights, state, idx, off, grad, psw=psw, optimizer=cfg.optimizer, lr=cfg.lr,
-                            eps=cfg.eps, stats=stats, prepared=args.hoist == "on")
-        opts.with_events(None)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-
+    if args.bags:
+        cfg = cfg.shrink(B=args.bags, name=f"{cfg.name}[B={args.bags}]")
+    wl = Workload(args, cfg, dev, count_launches=True)
+    st, model = wl.st, wl.model
     K = args.steps
-    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    fevs = [[mk() for _ in range(TBE_FWD_NUM_EVENTS)] for _ in range(K)]
-    bevs = [[mk() for _ in range(TBE_BWD_NUM_EVENTS)] for _ in range(K)]
-    bnds = [[mk(), mk()] for _ in range(K)]
-    pevs = [[mk() for _ in range(TBE_BWD_NUM_EVENTS)] for _ in range(K)]
-    gevs = [[mk(), mk()] for _ in range(K)]
-    e0, e1 = mk(), mk()
     clocks = ClockSampler(local)
-    launches.value = 0
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.4)  # let the sampler take a first sample
-    e0.record()
-    for k in range(K):
-        step(fevs[k], bevs[k], bnds[k], pevs[k] if args.hoist == "on" else None, gevs[k])
-    e1.record()
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    barrier(world)
-    gpu_launches = int(launches.value) + K * BOUNDS_LAUNCHES[args.bounds]
-    ms_total = e0.elapsed_time(e1)
+    t = wl.timed(K, args.warmup, world, clocks)
+    clk = t["clocks"]
+    gpu_launches = t["launches"] + K * BOUNDS_LAUNCHES[args.bounds]
+    ms_total = t["ms_total"]
     ms_max = all_max(world, ms_total, dev)
     lookups_all = all_sum(world, float(st["N"]) * K, dev)
-
-    # per-stage device times (ms per step)
-    stage_ms = {"bounds": np.mean([b[0].elapsed_time(b[1]) for b in bnds]),
-                "psw_grad": np.mean([g[0].elapsed_time(g[1]) for g in gevs]) if psw_grad else 0.0,
-                "gather": np.mean([f[0].elapsed_time(f[1]) for f in fevs]),
-                "histogram": np.mean([f[1].elapsed_time(f[2]) for f in fevs])}
-    for i, name in enumerate(BWD_STAGES):
-        # with the transpose hoisted, its stages ran on the side stream between the prepare's events
-        src = pevs if args.hoist == "on" and name in ("expand", "sort", "rle", "classify") else bevs
-        stage_ms[name] = float(np.mean([b[i].elapsed_time(b[i + 1]) for b in src]))
-    fwd_ms = float(np.mean([f[0].elapsed_time(f[2]) for f in fevs]))
-    bwd_ms = float(np.mean([b[0].elapsed_time(b[-1]) for b in bevs]))
-    model = byte_model(cfg, st, opts.c.long_threshold, opts.c.chunk, bounds_ids=args.bounds != "fused")
     peak, peak_kind = peaks()
-    stages = {}
-    for name, ms in stage_ms.items():
-        gb = model.get(name, 0) / 1e9
-        stages[name] = {"ms": round(float(ms), 4), "algorithmic_GB": round(gb, 4),
-                        "GBps": round(gb / (ms / 1e3), 1) if ms > 0 and gb > 0 else None,
-                        "frac": round(gb / (ms / 1e3) / peak, 4) if ms > 0 and gb > 0 else None}
-    for name in ("histogram", "bwd_histogram"):
-        if model[name + "_flops"] > 0 and stage_ms[name] > 0:
-            stages[name]["tensor_TFLOPs"] = round(model[name + "_flops"] / (stage_ms[name] / 1e3) / 1e12, 3)
-    kernel_stages = ("gather", "histogram", "short", "long", "bwd_histogram")
-    dom = max(kernel_stages, key=lambda n: stage_ms[n])
-    achieved = model[dom] / 1e9 / (stage_ms[dom] / 1e3)
-    traffic = profiled_traffic(dom, cfg.name)
+    stages, roof = wl.roofline(t["stage_ms"], peak, peak_kind)
 
     # end to end: host inputs copied in, the step, the step's counters read back
     e2e = None
     if not args.no_e2e:
-        idx_p = idx_h.pin_memory()
-        off_p = off_h.pin_memory()
-        psw_p = None if psw_h is None else psw_h.pin_memory()
+        idx_p = wl.idx_h.pin_memory()
+        off_p = wl.off_h.pin_memory()
+        psw_p = None if wl.psw_h is None else wl.psw_h.pin_memory()
         stats_p = torch.zeros(8, dtype=torch.int64).pin_memory()
         h2d = idx_p.numel() * idx_p.element_size() + off_p.numel() * off_p.element_size()
         if psw_p is not None:
@@ -494,7 +594,8 @@ def run_ours(args):
         # Two device copies of the inputs: step k's copy (on a copy stream) overlaps step k-1's
         # work; a step starts when its inputs have landed, a buffer is refilled once the step
         # that used it is done.
-        bufs = [inputs, (torch.empty_like(idx), torch.empty_like(off), None if psw is None else torch.empty_like(psw))]
+        idx, off, psw = wl.inputs
+        bufs = [wl.inputs, (torch.empty_like(idx), torch.empty_like(off), None if psw is None else torch.empty_like(psw))]
         copy = torch.cuda.Stream(device=dev)
         landed = [torch.cuda.Event(), torch.cuda.Event()]
         used = [torch.cuda.Event(), torch.cuda.Event()]
@@ -517,10 +618,10 @@ def run_ours(args):
         for k in range(K):
             if k + 1 < K:
                 upload(k + 1)
-            main.wait_event(landed[k % 2])
-            step(ins=bufs[k % 2])
-            used[k % 2].record(main)
-            stats_p.copy_(stats, non_blocking=True)
+            wl.main.wait_event(landed[k % 2])
+            wl.step(ins=bufs[k % 2])
+            used[k % 2].record(wl.main)
+            stats_p.copy_(wl.stats, non_blocking=True)
         torch.cuda.synchronize()
         dt = time.perf_counter() - t0
         dt = all_max(world, dt, dev)
@@ -532,7 +633,14 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(cfg, batch, args.cpu_sample_bags)
+        cpu = cpu_baseline(cfg, wl.batch, args.cpu_sample_bags)
+    batch_desc = {"lookups_per_step": st["N"], "distinct_rows": st["U"], "hottest_row_hits": st["hottest"],
+                  "long_runs": model["runs_long"], "lookups_in_long_runs": model["lookups_long"]}
+    wl.release()
+
+    per_config = None
+    if rank == 0 and world == 1 and args.per_config:
+        per_config = per_config_lines(args, dev, min(K, 20), max(3, min(args.warmup, 5)), peak, peak_kind)
 
     if rank == 0:
         line = {
@@ -550,23 +658,21 @@ def run_ours(args):
             "data": "synthetic",
             "config": {
                 "workload": f"{cfg.name}: {cfg.description}",
-                "lookups_per_step": st["N"], "distinct_rows": st["U"], "hottest_row_hits": st["hottest"],
-                "long_runs": model["runs_long"], "lookups_in_long_runs": model["lookups_long"],
+                **batch_desc,
                 "weights_storage": cfg.wdtype, "step": (("tbe_bounds_check_offsets" if args.bounds == "fused" else "tbe_bounds_check")
                          + (" + (tbe_forward || tbe_backward_prepare) + tbe_backward_update(prepared)"
                             if args.hoist == "on" else " + tbe_forward + tbe_backward_update")
                          + (" (ids repaired inside tbe_forward)" if args.bounds == "fused" else "")),
                 "long_mode": args.long_mode, "scheduler": args.scheduler, "merge": args.merge, "gather": args.gather, "classify": args.classify,
                 "transpose": "hoisted beside the forward (second stream)" if args.hoist == "on" else "in the backward",
-                "pooling": args.pooling, "psw_grad": bool(psw_grad),
+                "pooling": args.pooling, "psw_grad": bool(wl.psw_grad),
                 "parallelism": f"replicas x{world}",
                 "l2": "inputs larger than L2 (weights alone exceed 129 MB); no flush between steps",
-                "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
+                "fwd_ms": round(t["fwd_ms"], 4), "bwd_ms": round(t["bwd_ms"], 4),
             },
-            "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                         "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": traffic, "algorithmic_bytes": model[dom]},
+            "roofline": roof,
             "stages": stages,
+            "per_config": per_config,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clk,

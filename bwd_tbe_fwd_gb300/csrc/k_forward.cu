@@ -386,11 +386,12 @@ fwd_gather_kernel(FwdArgs a) {
 #pragma unroll
             for (int i = 0; i < NE; ++i) acc[x][i] += __shfl_xor_sync(FULL, acc[x][i], m);
         }
-        if (a.mean && e > s) {
+        if (a.mean && e > s) {  // times 1 / L: within an ulp of the quotient, one division a bag
+          const Acc inv = Acc(1) / static_cast<Acc>(e - s);
 #pragma unroll
           for (int x = 0; x < MAXV; ++x)
 #pragma unroll
-            for (int i = 0; i < NE; ++i) acc[x][i] /= static_cast<Acc>(e - s);
+            for (int i = 0; i < NE; ++i) acc[x][i] *= inv;
         }
         if (slot == 0) {
 #pragma unroll
@@ -449,9 +450,10 @@ __device__ __forceinline__ typename VecIO<WT, VB>::Raw lds_raw(const uint8_t* p)
 // One bag's fp32 sums (NE columns per lane) to its output row; mean pooling divides by L.
 template <int NE>
 __device__ __forceinline__ void store_bag(float* orow, float (&acc)[NE], int len, bool mean) {
-  if (mean && len > 0) {
+  if (mean && len > 0) {  // times 1 / L: within an ulp of the quotient, one division a bag
+    const float inv = 1.0f / static_cast<float>(len);
 #pragma unroll
-    for (int i = 0; i < NE; ++i) acc[i] /= static_cast<float>(len);
+    for (int i = 0; i < NE; ++i) acc[i] *= inv;
   }
   if constexpr (NE == 2) {
     __stcs(reinterpret_cast<float2*>(orow), make_float2(acc[0], acc[1]));

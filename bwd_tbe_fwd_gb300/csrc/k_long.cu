@@ -69,11 +69,12 @@ __device__ __forceinline__ void apply_from_workspace(const BwdCtx& c, uint32_t k
 
 // Sum of one chunk of a long run merged into the run's workspace row; with FUSED, the chunk
 // that takes the run's countdown to zero applies the optimizer.
-template <typename WT, bool PSW, int OPT, int MAXV, bool FUSED>
+template <typename WT, int FAC, int OPT, int MAXV, bool FUSED>
 __device__ __forceinline__ void long_chunk_body(const BwdCtx& c, int64_t ci, const uint32_t* __restrict__ sorted_vals,
                                                 const float* __restrict__ sorted_psw, bool merge_bulk,
                                                 void* srow) {
   using Acc = typename WTraits<WT>::Acc;
+  constexpr bool PSW = FAC != FAC_NONE;  // gradient rows are scaled by a per-lookup factor
   constexpr int UNROLL = 8 / MAXV > 0 ? 8 / MAXV : 1;  // rows in flight per lane: 8 float4 loads
   const int lane = lane_id();
   const size_t row_bytes = static_cast<size_t>(c.max_D) * sizeof(Acc);
@@ -105,11 +106,13 @@ __device__ __forceinline__ void long_chunk_body(const BwdCtx& c, int64_t ci, con
     // The bags of the chunk's lookups, 32 at a time, with the next 32 in flight.  Bags come
     // from the expand step and are < B; the clamp only keeps garbage (offsets that were not
     // repaired) from reading outside grad_out.
+    const float* bag_inv = FAC == FAC_INV_LEN ? c.inv_len + static_cast<int64_t>(t) * c.B : nullptr;
     uint32_t nxt_b = 0;
     float nxt_w = 1.f;
     if (s + lane < e) {
       nxt_b = min(__ldg(sorted_vals + s + lane), last_bag);
-      if (PSW) nxt_w = __ldg(sorted_psw + s + lane);
+      if (FAC == FAC_PSW) nxt_w = __ldg(sorted_psw + s + lane);
+      if (FAC == FAC_INV_LEN) nxt_w = __ldg(bag_inv + nxt_b);
     }
     for (uint32_t base = s; base < e; base += kWarp) {
       const int n = static_cast<int>(min(static_cast<uint32_t>(kWarp), e - base));
@@ -118,7 +121,8 @@ __device__ __forceinline__ void long_chunk_body(const BwdCtx& c, int64_t ci, con
       nxt_b = 0;
       if (base + kWarp + lane < e) {
         nxt_b = min(__ldg(sorted_vals + base + kWarp + lane), last_bag);
-        if (PSW) nxt_w = __ldg(sorted_psw + base + kWarp + lane);
+        if (FAC == FAC_PSW) nxt_w = __ldg(sorted_psw + base + kWarp + lane);
+        if (FAC == FAC_INV_LEN) nxt_w = __ldg(bag_inv + nxt_b);
       }
       if (fast && n == kWarp) {
         // all 32 rows valid: unpredicated loads
@@ -225,7 +229,7 @@ __device__ __forceinline__ void long_chunk_body(const BwdCtx& c, int64_t ci, con
 // CTA per 8 chunks, whose CTAs, when done, cancel a CTA that has not started yet (cluster launch
 // control) and take its chunks instead, so an SM keeps its CTA rather than launching a new one
 // ([FBT] section 4, Problem 1, Solution 1.2).
-template <typename WT, bool PSW, int OPT, int MAXV, bool FUSED>
+template <typename WT, int FAC, int OPT, int MAXV, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 4) long_chunk_kernel(BwdCtx c,
                                                                 const uint32_t* __restrict__ sorted_vals,
                                                                 const float* __restrict__ sorted_psw,
@@ -266,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 4) long_chunk_kernel(BwdCtx c,
       ci = gw + it * nw;
       if (ci >= nchunks) break;
     }
-    if (ci < nchunks) long_chunk_body<WT, PSW, OPT, MAXV, FUSED>(c, ci, sorted_vals, sorted_psw, merge_bulk, srow);
+    if (ci < nchunks) long_chunk_body<WT, FAC, OPT, MAXV, FUSED>(c, ci, sorted_vals, sorted_psw, merge_bulk, srow);
   }
 }
 
@@ -285,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) long_apply_kernel(BwdCtx c) {
   }
 }
 
-template <typename WT, bool PSW, int OPT, int MAXV>
+template <typename WT, int FAC, int OPT, int MAXV>
 cudaError_t launch_long_t(const BwdCtx& c, const uint32_t* vals, const float* psw, bool fused, int sched,
                           int merge, const DeviceInfo& dev, cudaStream_t s) {
   using Acc = typename WTraits<WT>::Acc;
@@ -294,7 +298,7 @@ cudaError_t launch_long_t(const BwdCtx& c, const uint32_t* vals, const float* ps
   size_t smem = static_cast<size_t>(kThreads / kWarp) * c.max_D * sizeof(Acc);
   if (merge == TBE_MERGE_BULK && smem > 48 * 1024) merge = TBE_MERGE_ATOMIC;
   if (merge != TBE_MERGE_BULK) smem = 0;
-  auto k = fused ? long_chunk_kernel<WT, PSW, OPT, MAXV, true> : long_chunk_kernel<WT, PSW, OPT, MAXV, false>;
+  auto k = fused ? long_chunk_kernel<WT, FAC, OPT, MAXV, true> : long_chunk_kernel<WT, FAC, OPT, MAXV, false>;
   const int64_t resident = persistent_grid(k, kThreads, smem, dev, INT64_MAX);
   int64_t grid;
   if (sched == TBE_SCHED_PERSISTENT) grid = resident;                      // claims from a counter
@@ -307,14 +311,14 @@ cudaError_t launch_long_t(const BwdCtx& c, const uint32_t* vals, const float* ps
   return cudaGetLastError();
 }
 
-template <typename WT, bool PSW, int OPT>
+template <typename WT, int FAC, int OPT>
 cudaError_t launch_long_maxv(const BwdCtx& c, const uint32_t* vals, const float* psw, bool fused, int sched,
                              int merge, int maxv, const DeviceInfo& dev, cudaStream_t s) {
   switch (maxv) {
-    case 1: return launch_long_t<WT, PSW, OPT, 1>(c, vals, psw, fused, sched, merge, dev, s);
-    case 2: return launch_long_t<WT, PSW, OPT, 2>(c, vals, psw, fused, sched, merge, dev, s);
-    case 4: return launch_long_t<WT, PSW, OPT, 4>(c, vals, psw, fused, sched, merge, dev, s);
-    default: return launch_long_t<WT, PSW, OPT, 8>(c, vals, psw, fused, sched, merge, dev, s);
+    case 1: return launch_long_t<WT, FAC, OPT, 1>(c, vals, psw, fused, sched, merge, dev, s);
+    case 2: return launch_long_t<WT, FAC, OPT, 2>(c, vals, psw, fused, sched, merge, dev, s);
+    case 4: return launch_long_t<WT, FAC, OPT, 4>(c, vals, psw, fused, sched, merge, dev, s);
+    default: return launch_long_t<WT, FAC, OPT, 8>(c, vals, psw, fused, sched, merge, dev, s);
   }
 }
 
@@ -351,14 +355,20 @@ cudaError_t launch_long_updates(const Problem& P, const BwdCtx& c, const BwdLayo
     using WT = decltype(w);
     if (P.scaled) {
       return opt == TBE_OPT_SGD
-                 ? launch_long_maxv<WT, true, TBE_OPT_SGD>(c, vals, psw, fused, scheduler, merge, maxv, dev, s)
-                 : launch_long_maxv<WT, true, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, scheduler, merge, maxv,
-                                                                       dev, s);
+                 ? launch_long_maxv<WT, FAC_PSW, TBE_OPT_SGD>(c, vals, psw, fused, scheduler, merge, maxv, dev, s)
+                 : launch_long_maxv<WT, FAC_PSW, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, scheduler, merge,
+                                                                          maxv, dev, s);
+    }
+    if (P.mean_inv) {
+      return opt == TBE_OPT_SGD
+                 ? launch_long_maxv<WT, FAC_INV_LEN, TBE_OPT_SGD>(c, vals, psw, fused, scheduler, merge, maxv, dev, s)
+                 : launch_long_maxv<WT, FAC_INV_LEN, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, scheduler, merge,
+                                                                              maxv, dev, s);
     }
     return opt == TBE_OPT_SGD
-               ? launch_long_maxv<WT, false, TBE_OPT_SGD>(c, vals, psw, fused, scheduler, merge, maxv, dev, s)
-               : launch_long_maxv<WT, false, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, scheduler, merge, maxv,
-                                                                      dev, s);
+               ? launch_long_maxv<WT, FAC_NONE, TBE_OPT_SGD>(c, vals, psw, fused, scheduler, merge, maxv, dev, s)
+               : launch_long_maxv<WT, FAC_NONE, TBE_OPT_ROWWISE_ADAGRAD>(c, vals, psw, fused, scheduler, merge,
+                                                                         maxv, dev, s);
   });
 }
 

@@ -18,7 +18,9 @@ namespace {
 // ------------------------------------------------------------------------------------------
 // short runs
 // ------------------------------------------------------------------------------------------
-template <typename WT, bool PSW, int OPT, int LPR, int VPL, bool PERSIST>
+constexpr uint32_t kNoBag = 0xffffffffu;  // B < 2^31: never a bag id
+
+template <typename WT, int FAC, int OPT, int LPR, int VPL, bool PERSIST>
 __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucket,
                                                             const uint32_t* __restrict__ sorted_vals,
                                                             const float* __restrict__ sorted_psw) {
@@ -34,6 +36,7 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) / kWarp;
   using IO = VecIO<WT, 4 * sizeof(WT)>;
   using Raw = typename IO::Raw;
+  constexpr bool PSW = FAC != FAC_NONE;  // gradient rows are scaled by a per-lookup factor
 
   int64_t claim_base = 0, claim_left = 0;
   int64_t it = 0;
@@ -83,13 +86,15 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
       for (int q = 0; q < 4; ++q) acc[j][q] = Acc(0);
 
     for (uint32_t j0 = 0; j0 < maxlen; j0 += LPR) {
-      uint32_t my_b = 0;
+      // this lane's lookup of the window: its bag (kNoBag past the run, or for a bag id outside
+      // the batch, which only offsets left unrepaired can give: no row is read) and its factor
+      uint32_t my_b = kNoBag;
       float my_w = 1.f;
-      bool my_ok = false;
       if (j0 + li < len) {
         my_b = __ldg(sorted_vals + off + j0 + li);
-        if (PSW) my_w = __ldg(sorted_psw + off + j0 + li);
-        my_ok = my_b < c.B;
+        if (my_b >= static_cast<uint32_t>(c.B)) my_b = kNoBag;
+        if (FAC == FAC_PSW) my_w = __ldg(sorted_psw + off + j0 + li);
+        if (FAC == FAC_INV_LEN && my_b != kNoBag) my_w = __ldg(c.inv_len + static_cast<int64_t>(t) * c.B + my_b);
       }
       const int steps = static_cast<int>(min(static_cast<uint32_t>(LPR), maxlen - j0));
       for (int q0 = 0; q0 < steps; q0 += UNROLL) {
@@ -99,9 +104,7 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
         for (int u = 0; u < UNROLL; ++u) {
           const int src = g * LPR + ((q0 + u) & (LPR - 1));
           const uint32_t b = __shfl_sync(FULL, my_b, src);
-          const bool ok = __shfl_sync(FULL, static_cast<int>(my_ok), src) && (q0 + u < steps) &&
-                          (j0 + q0 + u < len);
-          w[u] = PSW ? __shfl_sync(FULL, my_w, src) : 1.f;
+          const bool ok = b != kNoBag && q0 + u < steps;
           const float4* grow = reinterpret_cast<const float4*>(c.grad_out + static_cast<int64_t>(b) * c.total_D + col0);
 #pragma unroll
           for (int jj = 0; jj < VPL; ++jj) {
@@ -109,6 +112,10 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
             v[u][jj] = (ok && vec < nv) ? __ldg(grow + vec) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
+        // the factors after the row loads: with FAC_INV_LEN each one is a load that depends on
+        // the bag, which must not hold the row loads back
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) w[u] = PSW ? __shfl_sync(FULL, my_w, g * LPR + ((q0 + u) & (LPR - 1))) : 1.f;
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u)
 #pragma unroll
@@ -126,19 +133,19 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
   }
 }
 
-template <typename WT, bool PSW, int OPT, int LPR, int VPL>
+template <typename WT, int FAC, int OPT, int LPR, int VPL>
 cudaError_t launch_short_t(const BwdCtx& c, int bucket, const uint32_t* vals, const float* psw,
                            bool persist, const DeviceInfo& dev, cudaStream_t s) {
   constexpr int GPW = kWarp / LPR;
   const int64_t groups_per_cta = (kThreads / kWarp) * GPW;
   const int64_t want = (static_cast<int64_t>(c.short_cap[bucket]) + groups_per_cta - 1) / groups_per_cta;
   if (persist) {
-    auto k = short_run_kernel<WT, PSW, OPT, LPR, VPL, true>;
+    auto k = short_run_kernel<WT, FAC, OPT, LPR, VPL, true>;
     const int grid = persistent_grid(k, kThreads, 0, dev, want);
     k<<<grid, kThreads, 0, s>>>(c, bucket, vals, psw);
     note_launch();
   } else {
-    auto k = short_run_kernel<WT, PSW, OPT, LPR, VPL, false>;
+    auto k = short_run_kernel<WT, FAC, OPT, LPR, VPL, false>;
     // sixteen waves of CTAs (capped by the list capacity): CTAs that finish early hand their SM
     // to the next, which evens out runs of uneven length better than one resident wave
     const int64_t g16 = static_cast<int64_t>(persistent_grid(k, kThreads, 0, dev, INT64_MAX)) * 16;
@@ -149,20 +156,20 @@ cudaError_t launch_short_t(const BwdCtx& c, int bucket, const uint32_t* vals, co
   return cudaGetLastError();
 }
 
-template <typename WT, bool PSW, int OPT>
+template <typename WT, int FAC, int OPT>
 cudaError_t launch_short_bucket(const BwdCtx& c, int bucket, const uint32_t* vals, const float* psw,
                                 bool persist, const DeviceInfo& dev, cudaStream_t s) {
   // next_pow2(D) = 2^bucket; float4 slices per row = 2^(bucket-2): min(32, slices) lanes per run
   switch (bucket) {
-    case 2: return launch_short_t<WT, PSW, OPT, 1, 1>(c, bucket, vals, psw, persist, dev, s);
-    case 3: return launch_short_t<WT, PSW, OPT, 2, 1>(c, bucket, vals, psw, persist, dev, s);
-    case 4: return launch_short_t<WT, PSW, OPT, 4, 1>(c, bucket, vals, psw, persist, dev, s);
-    case 5: return launch_short_t<WT, PSW, OPT, 8, 1>(c, bucket, vals, psw, persist, dev, s);
-    case 6: return launch_short_t<WT, PSW, OPT, 16, 1>(c, bucket, vals, psw, persist, dev, s);
-    case 7: return launch_short_t<WT, PSW, OPT, 32, 1>(c, bucket, vals, psw, persist, dev, s);
-    case 8: return launch_short_t<WT, PSW, OPT, 32, 2>(c, bucket, vals, psw, persist, dev, s);
-    case 9: return launch_short_t<WT, PSW, OPT, 32, 4>(c, bucket, vals, psw, persist, dev, s);
-    case 10: return launch_short_t<WT, PSW, OPT, 32, 8>(c, bucket, vals, psw, persist, dev, s);
+    case 2: return launch_short_t<WT, FAC, OPT, 1, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 3: return launch_short_t<WT, FAC, OPT, 2, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 4: return launch_short_t<WT, FAC, OPT, 4, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 5: return launch_short_t<WT, FAC, OPT, 8, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 6: return launch_short_t<WT, FAC, OPT, 16, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 7: return launch_short_t<WT, FAC, OPT, 32, 1>(c, bucket, vals, psw, persist, dev, s);
+    case 8: return launch_short_t<WT, FAC, OPT, 32, 2>(c, bucket, vals, psw, persist, dev, s);
+    case 9: return launch_short_t<WT, FAC, OPT, 32, 4>(c, bucket, vals, psw, persist, dev, s);
+    case 10: return launch_short_t<WT, FAC, OPT, 32, 8>(c, bucket, vals, psw, persist, dev, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -180,11 +187,15 @@ cudaError_t launch_short_updates(const Problem& P, const BwdCtx& c, const BwdLay
     cudaError_t e = by_weight_type(P.wdtype, [&](auto w) -> cudaError_t {
       using WT = decltype(w);
       if (P.scaled) {
-        return opt == TBE_OPT_SGD ? launch_short_bucket<WT, true, TBE_OPT_SGD>(c, k, vals, psw, persist, dev, s)
-                                  : launch_short_bucket<WT, true, TBE_OPT_ROWWISE_ADAGRAD>(c, k, vals, psw, persist, dev, s);
+        return opt == TBE_OPT_SGD ? launch_short_bucket<WT, FAC_PSW, TBE_OPT_SGD>(c, k, vals, psw, persist, dev, s)
+                                  : launch_short_bucket<WT, FAC_PSW, TBE_OPT_ROWWISE_ADAGRAD>(c, k, vals, psw, persist, dev, s);
       }
-      return opt == TBE_OPT_SGD ? launch_short_bucket<WT, false, TBE_OPT_SGD>(c, k, vals, psw, persist, dev, s)
-                                : launch_short_bucket<WT, false, TBE_OPT_ROWWISE_ADAGRAD>(c, k, vals, psw, persist, dev, s);
+      if (P.mean_inv) {
+        return opt == TBE_OPT_SGD ? launch_short_bucket<WT, FAC_INV_LEN, TBE_OPT_SGD>(c, k, vals, psw, persist, dev, s)
+                                  : launch_short_bucket<WT, FAC_INV_LEN, TBE_OPT_ROWWISE_ADAGRAD>(c, k, vals, psw, persist, dev, s);
+      }
+      return opt == TBE_OPT_SGD ? launch_short_bucket<WT, FAC_NONE, TBE_OPT_SGD>(c, k, vals, psw, persist, dev, s)
+                                : launch_short_bucket<WT, FAC_NONE, TBE_OPT_ROWWISE_ADAGRAD>(c, k, vals, psw, persist, dev, s);
     });
     if (e != cudaSuccess) return e;
   }

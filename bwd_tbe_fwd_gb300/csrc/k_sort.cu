@@ -50,6 +50,7 @@ struct ExpandArgs {
   float* psw_out;
   uint32_t* counters;
   unsigned long long* stats;
+  float* inv_len;              // NULL, or [TB]: 1 / L of each bag (unweighted mean pooling)
   int mean;                    // mean pooling: the factor is psw / L (1 / L unweighted)
   int nhist;                   // tables whose lookups stay out of the sort
   int hist_t[kMaxHistTables];  // ascending
@@ -105,6 +106,10 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(ExpandArgs a) {
     }
     s_E[k] = E;
     s_shift[k] = static_cast<uint32_t>(shift);
+    if (a.inv_len != nullptr) {  // the correctly rounded 1 / L of the bag's lookups, as psw / L with psw = 1
+      const int64_t L = s_off[k + 1] - s_off[k];
+      a.inv_len[u] = L > 0 ? __frcp_rn(static_cast<float>(L)) : 0.0f;
+    }
   }
   __syncthreads();
   // Each thread takes a 4-aligned group of 4 consecutive lookups: 16- or 32-byte loads of
@@ -617,6 +622,7 @@ cudaError_t launch_expand(const Problem& P, const BwdCtx& c, cudaStream_t s) {
   a.psw_out = c.pswbuf[0];
   a.counters = c.counters;
   a.stats = c.stats;
+  a.inv_len = c.inv_len;
   a.mean = P.pooling == TBE_POOL_MEAN;
   a.nhist = c.nhist;
   for (int h = 0; h < kMaxHistTables; ++h) a.hist_t[h] = h < c.nhist ? c.hist_t[h] : 0;

@@ -100,6 +100,11 @@ __device__ __forceinline__ void apply_row_prefetched(
   }
 }
 
+// Per-lookup factor of the backward: FAC_NONE (sum pooling, unweighted), FAC_PSW (the sorted
+// per-sample weights, over L for mean pooling), FAC_INV_LEN (unweighted mean pooling: 1 / L of
+// the lookup's bag, which the expand step writes once per bag into c.inv_len).
+enum { FAC_NONE = 0, FAC_PSW = 1, FAC_INV_LEN = 2 };
+
 int maxv_for(int max_D) {
   const int nv = max_D / 4;
   const int m = (nv + kWarp - 1) / kWarp;

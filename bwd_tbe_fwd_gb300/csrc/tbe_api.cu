@@ -6,6 +6,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -23,12 +25,6 @@ struct LaunchTally {
   }
 };
 
-tbe_status cuda_status(cudaError_t e) {
-  if (e == cudaSuccess) return TBE_OK;
-  g_last_cuda_error = static_cast<int>(e);
-  return TBE_ERR_CUDA;
-}
-
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -39,10 +35,43 @@ int bucket_of(int D) {
   return k;
 }
 
-void record(const tbe_options& opt, int i, cudaStream_t s) {
+// NVTX range names: event i ends stage i and begins stage i + 1 (event 0 begins stage 1).
+const char* const kFwdRanges[TBE_FWD_NUM_EVENTS] = {"tbe_forward", "tbe_forward.gather", "tbe_forward.histogram"};
+const char* const kBwdRanges[TBE_BWD_NUM_EVENTS] = {
+    "tbe_backward",         "tbe_backward.expand", "tbe_backward.sort",  "tbe_backward.rle",
+    "tbe_backward.classify", "tbe_backward.short",  "tbe_backward.long", "tbe_backward.apply",
+    "tbe_backward.histogram"};
+thread_local int g_nvtx_open = 0;  // ranges this thread has pushed and not yet popped
+
+// Records stage-boundary event i (if the caller asked for events) and, with opt.nvtx, closes the
+// NVTX range of the stage that ends here and opens the next one.
+void record(const tbe_options& opt, int i, cudaStream_t s, const char* const* names, int n) {
   if (opt.events != nullptr && i < opt.num_events && opt.events[i] != nullptr)
     cudaEventRecord(static_cast<cudaEvent_t>(opt.events[i]), s);
+  if (opt.nvtx) {
+    if (i > 0 && g_nvtx_open > 0) {
+      nvtxRangePop();
+      --g_nvtx_open;
+    }
+    if (i + 1 < n) {
+      nvtxRangePushA(names[i + 1]);
+      ++g_nvtx_open;
+    }
+  }
 }
+void record(const tbe_options& opt, int i, cudaStream_t s) {  // backward stages
+  record(opt, i, s, kBwdRanges, TBE_BWD_NUM_EVENTS);
+}
+void record_fwd(const tbe_options& opt, int i, cudaStream_t s) {
+  record(opt, i, s, kFwdRanges, TBE_FWD_NUM_EVENTS);
+}
+
+// Closes the NVTX ranges a call left open (it returned early on an error).
+struct RangeGuard {
+  ~RangeGuard() {
+    for (; g_nvtx_open > 0; --g_nvtx_open) nvtxRangePop();
+  }
+};
 
 tbe_options resolve(const tbe_options* opt) {
   tbe_options o;
@@ -65,6 +94,12 @@ tbe_status check_options(const tbe_options& o) {
 }
 }  // namespace
 
+tbe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return TBE_OK;
+  g_last_cuda_error = static_cast<int>(e);
+  return TBE_ERR_CUDA;
+}
+
 void note_launch(int n) { g_launches += n; }
 
 tbe_status make_problem(const tbe_problem* p, Problem* out) {
@@ -85,7 +120,10 @@ tbe_status make_problem(const tbe_problem* p, Problem* out) {
   P.itype = p->itype;
   P.weighted = p->weighted != 0;
   P.pooling = p->pooling;
-  P.scaled = P.weighted || P.pooling == TBE_POOL_MEAN;
+  // weighted problems carry psw (over L for mean pooling) through the sort; unweighted mean
+  // pooling needs only 1 / L, which the update kernels take from the offsets by the bag id
+  P.scaled = P.weighted;
+  P.mean_inv = !P.weighted && P.pooling == TBE_POOL_MEAN;
   P.wbytes = p->wdtype == TBE_F32 ? 4 : 2;
   P.D.assign(p->D, p->D + p->T);
   P.E.assign(p->E, p->E + p->T);
@@ -217,6 +255,7 @@ BwdLayout make_bwd_layout(const Problem& P, const tbe_options& opt, const Device
   L.ws_rows = take(static_cast<size_t>(L.long_cap) * P.max_D * L.acc_bytes);
   L.cls_counts = take(sizeof(uint32_t) * (kNumBuckets + 2) * L.cls_grid);
   L.hist_ws = take(kHistWsBytes * L.nhist);
+  L.inv_len = P.mean_inv ? take(sizeof(float) * static_cast<size_t>(P.TB)) : 0;
   L.total = off;
   return L;
 }
@@ -281,6 +320,7 @@ BwdCtx make_ctx(const Problem& P, const tbe_options& o, const BwdLayout& L, cons
   c.nhist = L.nhist;
   for (int h = 0; h < kMaxHistTables; ++h) c.hist_t[h] = L.hist_t[h];
   c.hist_ws = base + L.hist_ws;
+  c.inv_len = P.mean_inv ? reinterpret_cast<float*>(base + L.inv_len) : nullptr;
   return c;
 }
 
@@ -450,7 +490,8 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned long long* stats = reinterpret_cast<unsigned long long*>(d_stats);
   LaunchTally tally(o);
-  record(o, TBE_FWD_EV_START, s);
+  RangeGuard ranges;
+  record_fwd(o, TBE_FWD_EV_START, s);
 
   // Tables on the counts x table path are skipped by the gather, which walks the remaining
   // contiguous table ranges.
@@ -475,7 +516,7 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
     if (e != cudaSuccess) return cuda_status(e);
     t0 = t1;
   }
-  record(o, TBE_FWD_EV_GATHER, s);
+  record_fwd(o, TBE_FWD_EV_GATHER, s);
   for (int t : hist) {
     cudaError_t e = launch_forward_histogram(P, *tables, weights, indices, offsets, out, t, o.fused_bounds != 0,
                                              stats, dev, s);
@@ -483,7 +524,7 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
       e = launch_forward_long_bags(P, *tables, weights, indices, offsets, psw, out, t * P.B, (t + 1) * P.B, dev, s);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  record(o, TBE_FWD_EV_HISTOGRAM, s);
+  record_fwd(o, TBE_FWD_EV_HISTOGRAM, s);
   return TBE_OK;
 }
 
@@ -540,6 +581,7 @@ tbe_status tbe_backward_prepare(const tbe_problem* prob, const tbe_options* opt,
                             d_stats);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   LaunchTally tally(o);
+  RangeGuard ranges;
   record(o, TBE_BWD_EV_START, s);
   const cudaError_t e = run_transpose(P, o, L, c, dev, s);
   return e == cudaSuccess ? TBE_OK : cuda_status(e);
@@ -574,6 +616,7 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
   const bool fused = o.long_mode != TBE_LONG_TWO_KERNEL;
   cudaError_t e;
   LaunchTally tally(o);
+  RangeGuard ranges;
   record(o, TBE_BWD_EV_START, s);
   if (o.prepared) {
     // the stage events of the transpose mark the start of the update

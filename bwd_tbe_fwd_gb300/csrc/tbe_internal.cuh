@@ -40,7 +40,8 @@ struct Problem {
   int wdtype = 0, itype = 0;
   bool weighted = false;
   int pooling = 0;          // tbe_pooling
-  bool scaled = false;      // the backward carries a per-lookup factor: weighted or mean pooling
+  bool scaled = false;      // the backward's sort carries a per-lookup factor (psw, over L for mean pooling)
+  bool mean_inv = false;    // unweighted mean pooling: the update kernels scale by 1 / L of the bag
   std::vector<int> D;
   std::vector<int64_t> E;
   std::vector<uint8_t> long_bags;
@@ -66,6 +67,10 @@ bool hist_forward_eligible(const Problem& P, const tbe_options& o, int t);
 
 tbe_status make_problem(const tbe_problem* p, Problem* out);
 
+// TBE_OK for cudaSuccess; otherwise records e as this thread's last CUDA error (reported by
+// tbe_last_cuda_error) and returns TBE_ERR_CUDA.
+tbe_status cuda_status(cudaError_t e);
+
 // Counts kernel launches of the current call on this host thread (reported through
 // tbe_options.launch_counter).
 void note_launch(int n = 1);
@@ -77,6 +82,7 @@ struct BwdLayout {
   size_t sort_counts = 0, sort_totals = 0, rle_counts = 0, unique = 0, run_off = 0, run_len = 0;
   size_t short_list[kNumBuckets] = {0};
   size_t long_list = 0, chunks = 0, countdown = 0, ws_rows = 0, cls_counts = 0;
+  size_t inv_len = 0;  // unweighted mean pooling: 1 / L per bag (TB floats)
   size_t total = 0;
   uint32_t short_cap[kNumBuckets] = {0};
   uint32_t long_cap = 0, chunk_cap = 0, u_cap = 0, n_cap = 0;
@@ -123,6 +129,7 @@ struct BwdCtx {
   const float* psw;
   const float* grad_out;
   float lr, eps;
+  float* inv_len;                   // [TB] 1 / L of each bag (unweighted mean pooling), else NULL
   // workspace
   uint32_t* counters;
   uint32_t* keys[2];

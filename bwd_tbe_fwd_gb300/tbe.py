@@ -42,7 +42,7 @@ EXPORTED = (
     "tbe_forward_workspace_size", "tbe_forward", "tbe_backward_workspace_size",
     "tbe_backward_update", "tbe_backward_metadata", "tbe_status_string", "tbe_version",
     "tbe_last_cuda_error", "tbe_backward_update_noalloc", "tbe_backward_prepare", "tbe_psw_gradient",
-    "tbe_bounds_check_offsets",
+    "tbe_bounds_check_offsets", "tbe_selftest_wait_timeout",
 )
 TBE_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -61,7 +61,7 @@ class Options(ctypes.Structure):
     _fields_ = [("long_threshold", c_i32), ("chunk", c_i32), ("long_mode", c_i32), ("scheduler", c_i32),
                 ("histogram", c_i32), ("fused_bounds", c_i32), ("events", ctypes.POINTER(vp)),
                 ("num_events", c_i32), ("launch_counter", ctypes.POINTER(c_i64)), ("classify_mode", c_i32),
-                ("prepared", c_i32), ("merge", c_i32), ("gather", c_i32)]
+                ("prepared", c_i32), ("merge", c_i32), ("gather", c_i32), ("nvtx", c_i32)]
 
 
 class RunMetadata(ctypes.Structure):
@@ -412,3 +412,18 @@ def tbe_backward_update_noalloc(tbe: TableBatchedEmbedding, weights, state, indi
                 _ptr(indices), _ptr(offsets), _ptr(psw), _ptr(grad_out), opt, c_f32(lr), c_f32(eps), _ptr(stats),
                 _stream(stream, tbe.device))
     _check(lib, st, "tbe_backward_update_noalloc")
+
+
+def selftest_wait_timeout(stats: torch.Tensor, polls: int = 8, stream=None):
+    """Diagnostic: one CTA waits, through the library's bounded mbarrier wait, for a phase that
+    never completes; it gives up after `polls` polls and adds 1 to stats[TBE_STAT_WAIT_TIMEOUT]
+    (stats: device int64[TBE_NUM_STATS]).  Asynchronous on `stream` (default: the current one)."""
+    lib = load()
+    fn = lib.tbe_selftest_wait_timeout
+    fn.argtypes = [ctypes.c_uint32, vp, vp]
+    fn.restype = ctypes.c_int
+    if not (stats.is_cuda and stats.dtype == torch.int64 and stats.numel() >= TBE_NUM_STATS):
+        raise TBEError(f"stats must be a CUDA int64 tensor of at least {TBE_NUM_STATS} elements")
+    with torch.cuda.device(stats.device):
+        st = fn(polls, _ptr(stats), _stream(stream, stats.device))
+    _check(lib, st, "tbe_selftest_wait_timeout")

@@ -168,6 +168,9 @@ typedef struct {
                                  tbe_backward_prepare left it, instead of computing it */
   int32_t merge;              /* tbe_merge_mode */
   int32_t gather;             /* tbe_gather_mode */
+  int32_t nvtx;               /* 1: NVTX ranges (host side, one per stage: "tbe_forward.gather",
+                                 "tbe_backward.sort", ...) around each stage's launches, for
+                                 timeline tools; 0 (the default): none */
 } tbe_options;
 
 /* Indices into d_stats (int64).  Counts accumulate over calls. */
@@ -181,7 +184,7 @@ enum {
 };
 
 /* The defaults: threshold 256, chunk 256, AUTO long mode, PERSISTENT scheduler, histogram on,
- * fused bounds off, no events, ORDERED classifier, ATOMIC merge, REGISTER gather. */
+ * fused bounds off, no events, ORDERED classifier, ATOMIC merge, REGISTER gather, no NVTX. */
 void tbe_default_options(tbe_options* opt);
 
 /* Fills the host arrays of the canonical packed layout for the problem; the caller copies
@@ -295,12 +298,15 @@ tbe_status tbe_backward_metadata(const tbe_problem* prob, const tbe_options* opt
  * arguments minus the workspace and uses instead a TBE_STATIC_SCRATCH_BYTES array compiled into
  * the library; it allocates nothing itself.
  *   - Limit: problems whose tbe_backward_workspace_size() exceeds TBE_STATIC_SCRATCH_BYTES are
- *     rejected with TBE_ERR_WORKSPACE (an invalid problem or options: TBE_ERR_INVALID_ARG or the
- *     status tbe_backward_update would return).
- *   - Memory: the array occupies device memory on every GPU where the entry point is used,
- *     until the process exits.
+ *     rejected with TBE_ERR_WORKSPACE; an invalid problem, options or arguments get the status
+ *     tbe_backward_update would return (TBE_ERR_INVALID_ARG, TBE_ERR_UNSUPPORTED, TBE_ERR_RANGE).
+ *   - Memory: the array occupies device memory from the time the library is loaded on a GPU
+ *     until the process exits: with lazy module loading (CUDA's default) on every GPU where the
+ *     library is used, with CUDA_MODULE_LOADING=EAGER on every GPU whose context loads the
+ *     library, whether or not this entry point is called there.
  *   - Set-up: the first call on a device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *     current) and keeps it; make that first call before any stream capture.  After a
+ *     cudaDeviceReset the library must be loaded again before this entry point is used there.
  *   - Sharing: all calls on one device use the same array, which keeps the last call's
  *     contents; each call zeroes what must start at zero.  Calls whose GPU work overlaps (other
  *     streams, other host threads) race on it; the caller must order them.

@@ -1,4 +1,4 @@
-"""The C-ABI library on the host: it loads, exports every function include/tbe.h declares, and
+"""The C-ABI library on the host: it loads, exports every function include/*.h declares, and
 its host-only entry points (layout, options, argument validation) behave as documented.
 No call here launches GPU work."""
 import ctypes
@@ -10,7 +10,7 @@ import pytest
 from bwd_tbe_fwd_gb300 import build as tbe_build
 from bwd_tbe_fwd_gb300 import tbe
 
-HEADER = os.path.join(tbe_build.INCLUDE, "tbe.h")
+HEADERS = sorted(os.path.join(tbe_build.INCLUDE, f) for f in os.listdir(tbe_build.INCLUDE) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -20,16 +20,18 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(tbe_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(tbe_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_every_declared_function_is_exported(lib):
     names = declared_functions()
     assert len(names) >= 12
     for name in names:
-        assert hasattr(lib, name), f"{name} declared in tbe.h but not exported"
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
     assert set(names) == set(tbe.EXPORTED)
 
 
@@ -47,7 +49,8 @@ def test_version_status_and_defaults(lib):
     lib.tbe_default_options(ctypes.byref(o))
     assert (o.long_threshold, o.chunk, o.long_mode, o.scheduler, o.histogram, o.fused_bounds) == \
         (256, 256, tbe.TBE_LONG_AUTO, tbe.TBE_SCHED_PERSISTENT, 1, 0)
-    assert (o.classify_mode, o.prepared, o.merge, o.gather) == (tbe.TBE_CLASSIFY_ORDERED, 0, 0, tbe.TBE_GATHER_REGISTER)
+    assert (o.classify_mode, o.prepared, o.merge, o.gather, o.nvtx) == \
+        (tbe.TBE_CLASSIFY_ORDERED, 0, 0, tbe.TBE_GATHER_REGISTER, 0)
 
 
 def test_table_layout(lib):

@@ -111,8 +111,9 @@ def test_prepared_transpose_beside_the_forward(name):
 @pytest.mark.parametrize("name", ["c5", "c2", "c1", "c3"])
 def test_mean_pooling(name):
     """Mean pooling ("Table-Batched Embeddings in Triton", "Try this"): the forward divides each
-    bag's sum by its length (empty bags stay 0), the backward scales each lookup by psw / L; the
-    per-lookup factors in the metadata are the oracle's, bit for bit."""
+    bag's sum by its length (empty bags stay 0), the backward scales each lookup by psw / L (1 / L,
+    taken from the offsets by the update kernels, when unweighted); the per-lookup factors the sort
+    carries for weighted tables are the oracle's, bit for bit."""
     c = Case(SMALL[name], pooling="mean")
     c.forward()
     c.backward()
@@ -359,3 +360,11 @@ def test_very_long_bags_hold_the_tolerance(lengths, D, gather):
     hot = np.bincount(idx[:lengths[0]].astype(np.int64)).max()
     assert hot > 40_000, hot
     c.forward(options=TBEOptions(gather={"register": TBE_GATHER_REGISTER, "tma": TBE_GATHER_TMA}[gather]))
+
+
+def test_nvtx_ranges_option_changes_nothing():
+    """With NVTX ranges on (one host-side range per stage), forward and backward give the same
+    results, metadata included."""
+    c = Case(SMALL["c5"], options=TBEOptions(nvtx=1))
+    c.forward(options=TBEOptions(nvtx=1))
+    c.backward(options=TBEOptions(nvtx=1))

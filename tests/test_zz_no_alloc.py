@@ -76,8 +76,19 @@ def test_noalloc_rejects_problems_beyond_the_scratch_size():
     fn.argtypes = [ctypes.POINTER(tbe_mod.Problem), ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_void_p] * 6 + \
         [ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
     fn.restype = ctypes.c_int
-    fake = ctypes.c_void_p(4096)
-    tables = tbe_mod.Tables(fake, fake, fake)
-    st = fn(ctypes.byref(prob), None, ctypes.byref(tables), fake, fake, fake, fake, None, fake,
+    lib.tbe_backward_workspace_size.argtypes = [ctypes.POINTER(tbe_mod.Problem), ctypes.c_void_p]
+    lib.tbe_backward_workspace_size.restype = ctypes.c_size_t
+    assert lib.tbe_backward_workspace_size(ctypes.byref(prob), None) > tbe_mod.TBE_STATIC_SCRATCH_BYTES
+    # every data pointer NULL: the size check rejects the call first; were it ever to pass, the
+    # workspace entry point's argument checks would reject the NULL buffers before any launch
+    tables = tbe_mod.Tables(None, None, None)
+    st = fn(ctypes.byref(prob), None, ctypes.byref(tables), None, None, None, None, None, None,
             tbe_mod.TBE_OPT_ROWWISE_ADAGRAD, 0.01, 1e-8, None, None)
     assert st == tbe_mod.TBE_ERR_WORKSPACE
+    # an invalid problem gets the status the workspace entry point gives it
+    bad = tbe_mod.Problem(0, 100, 1000, D, E, tbe_mod.TBE_F16, tbe_mod.TBE_I64, 0, None)
+    st = fn(ctypes.byref(bad), None, ctypes.byref(tables), None, None, None, None, None, None,
+            tbe_mod.TBE_OPT_ROWWISE_ADAGRAD, 0.01, 1e-8, None, None)
+    assert st == lib.tbe_backward_update(ctypes.byref(bad), None, ctypes.byref(tables), None, None, None, None,
+                                         None, None, tbe_mod.TBE_OPT_ROWWISE_ADAGRAD, ctypes.c_float(0.01),
+                                         ctypes.c_float(1e-8), None, 0, None, None) != tbe_mod.TBE_OK
