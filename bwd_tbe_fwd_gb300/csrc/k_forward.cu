@@ -207,9 +207,15 @@ fwd_gather_kernel(FwdArgs a) {
     // row 0 of the table; this lane's vectors of a row (lanes past the row width re-read its last
     // vector in full batches: their sums are never stored); the item's first output row
     const Raw* table = reinterpret_cast<const Raw*>(static_cast<const WT*>(a.weights) + __ldg(a.woff + t));
-    int vk[MAXV];
+    // this lane's vectors of row 0 as byte addresses: row id's vector m is at lbase[m] + id * rbytes,
+    // one wide multiply-add
+    const char* lbase[MAXV];
 #pragma unroll
-    for (int m = 0; m < MAXV; ++m) vk[m] = min(vi + m * kWarp, nvec - 1);
+    for (int m = 0; m < MAXV; ++m) lbase[m] = reinterpret_cast<const char*>(table + min(vi + m * kWarp, nvec - 1));
+    const uint32_t rbytes = static_cast<uint32_t>(nvec) * VB;
+    auto at = [&](int m, int32_t id) {
+      return reinterpret_cast<const Raw*>(lbase[m] + static_cast<uint64_t>(static_cast<uint32_t>(id)) * rbytes);
+    };
     float* orow = a.out + b0 * a.total_D + col0 + vi * NE;
     const int qmax = min(UNROLL, lpr);  // a batch (qmax * rps rows) covers at most 32 positions
 
@@ -281,7 +287,26 @@ fwd_gather_kernel(FwdArgs a) {
           if (my_id >= 0) my_w = rel < kWarp ? pa : pb;
         }
         const bool chunk_ok = __all_sync(FULL, lane >= n || my_id >= 0);  // no skipped id
-        for (int j = 0; j < n; j += rps * qmax) {
+        int j = 0;
+        if constexpr (!DOT && !PSW) {  // (with weights the extra loop spills registers)
+          if (chunk_ok && qmax == UNROLL) {
+            // whole batches of valid rows first: unpredicated loads, no per-batch checks
+            for (; j + rps * UNROLL <= n; j += rps * UNROLL) {
+              Raw v[UNROLL][MAXV];
+#pragma unroll
+              for (int q = 0; q < UNROLL; ++q) {
+                const int32_t id = __shfl_sync(FULL, my_id, j + q * rps + slot);
+#pragma unroll
+                for (int m = 0; m < MAXV; ++m) v[q][m] = ldg_raw(at(m, id));
+              }
+#pragma unroll
+              for (int q = 0; q < UNROLL; ++q)
+#pragma unroll
+                for (int m = 0; m < MAXV; ++m) accumulate<WT, VB, false>(acc[m], v[q][m], 1.0f);
+            }
+          }
+        }
+        for (; j < n; j += rps * qmax) {  // the bag's last rows, batches with a skipped id, dot mode
           Raw v[UNROLL][MAXV];
           int nq = UNROLL;  // load steps of this batch that hold a row (warp-uniform)
           const bool full = chunk_ok && qmax == UNROLL && j + rps * UNROLL <= n;
@@ -291,9 +316,8 @@ fwd_gather_kernel(FwdArgs a) {
             for (int q = 0; q < UNROLL; ++q) {
               const int r = j + q * rps + slot;
               const int32_t id = __shfl_sync(FULL, my_id, r);
-              const Raw* row = table + static_cast<int64_t>(id) * nvec;
 #pragma unroll
-              for (int m = 0; m < MAXV; ++m) v[q][m] = ldg_raw(row + vk[m]);
+              for (int m = 0; m < MAXV; ++m) v[q][m] = ldg_raw(at(m, id));
             }
           } else {
             // the bag's last rows (or a batch with a skipped id): only the load steps that hold a
@@ -307,10 +331,9 @@ fwd_gather_kernel(FwdArgs a) {
                 const int r = j + q * rps + slot;  // < 64; lanes past n hold -1
                 const int32_t id = __shfl_sync(FULL, my_id, r & (kWarp - 1));
                 const bool ok = r < n && id >= 0;
-                const Raw* row = table + static_cast<int64_t>(ok ? id : 0) * nvec;
 #pragma unroll
                 for (int m = 0; m < MAXV; ++m)
-                  if (ok && vi + m * kWarp < nvec) v[q][m] = ldg_raw(row + vk[m]);
+                  if (ok && vi + m * kWarp < nvec) v[q][m] = ldg_raw(at(m, id));
               }
             }
           }
