@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(BwdCtx c) {
   __shared__ uint32_t s_base[kNumBuckets + 1];
   __shared__ uint32_t s_chunks, s_chunk_base;
   const uint32_t U = min(c.counters[TBE_CNT_RUNS], c.u_cap);
+  const uint32_t N = c.counters[TBE_CNT_N];
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; r0 < U; r0 += stride) {
     const int64_t r = r0 + threadIdx.x;
@@ -37,9 +38,10 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(BwdCtx c) {
     if (r < U) {
       key = c.unique[r];
       start = c.run_off[r];
-      len = c.run_off[r + 1] - start;
+      const uint32_t end = c.run_off[r + 1];
+      len = end - start;
       c.run_len[r] = len;
-      if (key < c.total_rows) {
+      if (key < c.total_rows && TBE_CHECK(start <= end && end <= N, c.stats)) {
         t = table_of_row(c.roff, c.T, key);
         D = __ldg(c.doff + t + 1) - __ldg(c.doff + t);
         if (len >= static_cast<uint32_t>(c.threshold)) {
@@ -63,8 +65,9 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(BwdCtx c) {
     if (list >= 0) {
       const uint32_t slot = s_base[list] + my_off;
       if (list < kNumBuckets) {
-        if (slot < c.short_cap[list]) c.short_list[list][slot] = make_uint4(start, len, key, static_cast<uint32_t>(t));
-      } else if (slot < c.long_cap) {
+        if (TBE_GUARD(slot < c.short_cap[list], c.stats))
+          c.short_list[list][slot] = make_uint4(start, len, key, static_cast<uint32_t>(t));
+      } else if (TBE_GUARD(slot < c.long_cap, c.stats)) {
         c.long_list[slot] = static_cast<uint32_t>(r);
         c.countdown[slot] = nch;
         float4* row = reinterpret_cast<float4*>(static_cast<Acc*>(c.ws_rows) + static_cast<int64_t>(slot) * c.max_D);
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(BwdCtx c) {
         for (uint32_t k = 0; k < nch; ++k) {
           const uint32_t s0 = start + k * static_cast<uint32_t>(c.chunk);
           const uint32_t e0 = min(s0 + static_cast<uint32_t>(c.chunk), run_end);
-          if (cb + k < c.chunk_cap) c.chunks[cb + k] = make_uint4(s0, e0, key, slot);
+          if (TBE_GUARD(cb + k < c.chunk_cap, c.stats)) c.chunks[cb + k] = make_uint4(s0, e0, key, slot);
         }
       }
     }
@@ -105,8 +108,9 @@ struct RunRoute {
   int t, D;
 };
 
-// The route of the run with linear key `key` covering sorted positions [start, end).
-__device__ __forceinline__ RunRoute route_of(const BwdCtx& c, uint32_t key, uint32_t start, uint32_t end) {
+// The route of the run with linear key `key` covering sorted positions [start, end) of the N.
+__device__ __forceinline__ RunRoute route_of(const BwdCtx& c, uint32_t key, uint32_t start, uint32_t end,
+                                             uint32_t N) {
   RunRoute x;
   x.key = key;
   x.start = start;
@@ -115,7 +119,7 @@ __device__ __forceinline__ RunRoute route_of(const BwdCtx& c, uint32_t key, uint
   x.nch = 0;
   x.t = 0;
   x.D = 0;
-  if (x.key < c.total_rows) {
+  if (x.key < c.total_rows && TBE_CHECK(start <= end && end <= N, c.stats)) {
     x.t = table_of_row(c.roff, c.T, x.key);
     x.D = __ldg(c.doff + x.t + 1) - __ldg(c.doff + x.t);
     if (x.len >= static_cast<uint32_t>(c.threshold)) {
@@ -128,8 +132,8 @@ __device__ __forceinline__ RunRoute route_of(const BwdCtx& c, uint32_t key, uint
   return x;
 }
 
-__device__ __forceinline__ RunRoute route_run(const BwdCtx& c, uint32_t r) {
-  return route_of(c, c.unique[r], c.run_off[r], c.run_off[r + 1]);
+__device__ __forceinline__ RunRoute route_run(const BwdCtx& c, uint32_t r, uint32_t N) {
+  return route_of(c, c.unique[r], c.run_off[r], c.run_off[r + 1], N);
 }
 
 __global__ void __launch_bounds__(kThreads) classify_count_kernel(BwdCtx c) {
@@ -137,11 +141,12 @@ __global__ void __launch_bounds__(kThreads) classify_count_kernel(BwdCtx c) {
   if (threadIdx.x < kLists) s_cnt[threadIdx.x] = 0;
   __syncthreads();
   const uint32_t U = min(c.counters[TBE_CNT_RUNS], c.u_cap);
+  const uint32_t N = c.counters[TBE_CNT_N];
   uint32_t r0, r1;
   cls_segment(U, blockIdx.x, gridDim.x, &r0, &r1);
 #pragma unroll 4
   for (uint32_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
-    const RunRoute x = route_run(c, r);
+    const RunRoute x = route_run(c, r, N);
     if (x.list >= 0) atomicAdd(&s_cnt[x.list], 1u);
     if (x.nch) atomicAdd(&s_cnt[kChunkList], x.nch);
   }
@@ -184,6 +189,7 @@ __global__ void __launch_bounds__(kThreads) classify_write_kernel(BwdCtx c) {
   const unsigned lt = lanemask_lt();
   if (threadIdx.x < kLists) s_base[threadIdx.x] = c.cls_counts[threadIdx.x * gridDim.x + blockIdx.x];
   const uint32_t U = min(c.counters[TBE_CNT_RUNS], c.u_cap);
+  const uint32_t N = c.counters[TBE_CNT_N];
   uint32_t r0, r1;
   cls_segment(U, blockIdx.x, gridDim.x, &r0, &r1);
   // this thread's run of the next tile (key, start, end), loaded while the current tile is
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(kThreads) classify_write_kernel(BwdCtx c) {
     x.list = -1;
     x.nch = 0;
     if (r < r1) {
-      x = route_of(c, key, start, end);
+      x = route_of(c, key, start, end, N);
       c.run_len[r] = x.len;
     }
     // rank among the warp's lanes of the same list; the chunk list by an inclusive scan
@@ -230,8 +236,9 @@ __global__ void __launch_bounds__(kThreads) classify_write_kernel(BwdCtx c) {
     if (x.list >= 0) {
       const uint32_t slot = s_base[x.list] + before + rank;
       if (x.list < kNumBuckets) {
-        if (slot < c.short_cap[x.list]) c.short_list[x.list][slot] = make_uint4(x.start, x.len, x.key, static_cast<uint32_t>(x.t));
-      } else if (slot < c.long_cap) {
+        if (TBE_GUARD(slot < c.short_cap[x.list], c.stats))
+          c.short_list[x.list][slot] = make_uint4(x.start, x.len, x.key, static_cast<uint32_t>(x.t));
+      } else if (TBE_GUARD(slot < c.long_cap, c.stats)) {
         c.long_list[slot] = r;
         c.countdown[slot] = x.nch;
         float4* row = reinterpret_cast<float4*>(static_cast<Acc*>(c.ws_rows) + static_cast<int64_t>(slot) * c.max_D);
@@ -242,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) classify_write_kernel(BwdCtx c) {
         for (uint32_t k = 0; k < x.nch; ++k) {
           const uint32_t s0 = x.start + k * static_cast<uint32_t>(c.chunk);
           const uint32_t e0 = min(s0 + static_cast<uint32_t>(c.chunk), run_end);
-          if (cb + k < c.chunk_cap) c.chunks[cb + k] = make_uint4(s0, e0, x.key, slot);
+          if (TBE_GUARD(cb + k < c.chunk_cap, c.stats)) c.chunks[cb + k] = make_uint4(s0, e0, x.key, slot);
         }
       }
     }

@@ -80,7 +80,8 @@ __device__ __forceinline__ void long_chunk_body(const BwdCtx& c, int64_t ci, con
   const size_t row_bytes = static_cast<size_t>(c.max_D) * sizeof(Acc);
     const uint4 rec = __ldg(c.chunks + ci);  // {first lookup, end, key, slot}
     const uint32_t s = rec.x, e = rec.y, key = rec.z, slot = rec.w;
-    if (slot >= c.long_cap) return;
+    if (!TBE_GUARD(slot < c.long_cap, c.stats)) return;
+    if (!TBE_CHECK(s <= e && e <= c.counters[TBE_CNT_N] && key < c.total_rows, c.stats)) return;
     const int t = table_of_row(c.roff, c.T, key);
     const int col0 = __ldg(c.doff + t);
     const int D = __ldg(c.doff + t + 1) - col0;

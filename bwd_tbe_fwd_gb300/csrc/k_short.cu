@@ -59,7 +59,13 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
     if (base >= count) break;  // warp-uniform
     const int64_t i = base + g;
     uint4 rec = make_uint4(0, 0, 0, 0);  // {first lookup, length, key, table}
-    if (i < count) rec = __ldg(list + i);
+    if (i < count) {
+      rec = __ldg(list + i);
+      if (!TBE_CHECK(rec.w < static_cast<uint32_t>(c.T) && rec.z < c.total_rows &&
+                         rec.x <= c.counters[TBE_CNT_N] && rec.y <= c.counters[TBE_CNT_N] - rec.x,
+                     c.stats))
+        rec = make_uint4(0, 0, 0, 0);  // skipped: no row read or written
+    }
     const uint32_t off = rec.x, len = rec.y, key = rec.z;
     const int t = static_cast<int>(rec.w);
     const int col0 = __ldg(c.doff + t);

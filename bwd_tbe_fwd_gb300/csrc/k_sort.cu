@@ -339,8 +339,9 @@ __global__ void __launch_bounds__(kThreads, 2) radix_downsweep_kernel(
 
   const int lane = lane_id(), w = threadIdx.x / kWarp;
   const unsigned lt = lanemask_lt();
+  const int64_t N = counters[TBE_CNT_N];
   int64_t b0, b1;
-  segment_of(counters[TBE_CNT_N], blockIdx.x, G, &b0, &b1);
+  segment_of(N, blockIdx.x, G, &b0, &b1);
   {
     // output base of each digit for this CTA: exclusive prefix over the digit totals plus the
     // CTA's prefix within the digit
@@ -480,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 2) radix_downsweep_kernel(
       const uint2 kv = s_kv[j];
       const uint32_t d = (kv.x >> shift) & (R - 1);
       const uint32_t g = s_run[d] + (static_cast<uint32_t>(j) - s_dstart[d]);
+      if (!TBE_CHECK(g < N, stats)) continue;
       keys_out[g] = kv.x;
       vals_out[g] = kv.y;
       if (PSW) psw_out[g] = s_psw[j];
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(kThreads) rle_write_kernel(const uint32_t* key
                                                             uint32_t* counters,
                                                             const uint32_t* rle_counts, int G,
                                                             uint32_t* unique, uint32_t* run_off,
-                                                            uint32_t u_cap) {
+                                                            uint32_t u_cap, unsigned long long* stats) {
   __shared__ uint32_t sh[kWarpsPerBlock];
   const int64_t N = counters[TBE_CNT_N];
   uint32_t before = 0;
@@ -590,7 +592,7 @@ __global__ void __launch_bounds__(kThreads) rle_write_kernel(const uint32_t* key
 #pragma unroll
     for (int i = 0; i < kRleItems; ++i) {
       if (mask & (1u << i)) {
-        if (r < u_cap) {
+        if (TBE_GUARD(r < u_cap, stats)) {
           unique[r] = k[i];
           run_off[r] = static_cast<uint32_t>(p0 + i);
         }
@@ -707,7 +709,7 @@ cudaError_t launch_rle(const Problem& P, const BwdCtx& c, const BwdLayout& L, cu
   rle_count_kernel<<<L.rle_grid, kThreads, 0, s>>>(keys, c.counters, c.rle_counts, L.rle_grid);
   note_launch();
   rle_write_kernel<<<L.rle_grid, kThreads, 0, s>>>(keys, c.counters, c.rle_counts, L.rle_grid,
-                                                   c.unique, c.run_off, c.u_cap);
+                                                   c.unique, c.run_off, c.u_cap, c.stats);
   note_launch();
   return cudaGetLastError();
 }

@@ -221,6 +221,23 @@ __device__ __forceinline__ void stat_add(unsigned long long* stats, int k, unsig
   if (stats != nullptr && v != 0) atomicAdd(stats + k, v);
 }
 
+// Debug build (-DTBE_CHECKED=1): device-side range checks on indices the kernels derive from
+// data (sorted positions, run bounds, list slots), each failure counted in
+// stats[TBE_STAT_CHECK_FAILED] and the access skipped -- an error counter, never a trap.
+//   TBE_CHECK(ok, stats)  a check only the debug build has (true, not evaluated, otherwise)
+//   TBE_GUARD(ok, stats)  a guard every build keeps; the debug build also counts its failures
+#ifndef TBE_CHECKED
+#define TBE_CHECKED 0
+#endif
+__device__ __forceinline__ bool check_count(bool ok, unsigned long long* stats) {
+#if TBE_CHECKED
+  if (!ok) stat_add(stats, TBE_STAT_CHECK_FAILED, 1);
+#endif
+  return ok;
+}
+#define TBE_CHECK(ok, stats) (!TBE_CHECKED || ::tbe::check_count((ok), (stats)))
+#define TBE_GUARD(ok, stats) (::tbe::check_count((ok), (stats)))
+
 // Table of a linear row id: the t with row_offsets[t] <= key < row_offsets[t+1].
 __device__ __forceinline__ int table_of_row(const int64_t* roff, int T, int64_t key) {
   int lo = 0, hi = T;  // invariant: roff[lo] <= key < roff[hi]

@@ -32,7 +32,7 @@ TBE_BWD_NUM_EVENTS = 9
 FWD_STAGES = ("gather", "histogram")
 BWD_STAGES = ("expand", "sort", "rle", "classify", "short", "long", "apply", "bwd_histogram")
 TBE_NUM_STATS = 8
-STAT_NAMES = ("bad_indices", "bad_offsets", "unrepaired", "wait_timeout")
+STAT_NAMES = ("bad_indices", "bad_offsets", "unrepaired", "wait_timeout", "check_failed")
 TBE_CNT_N, TBE_CNT_RUNS, TBE_CNT_LONG, TBE_CNT_CHUNKS, TBE_CNT_SHORT0 = 0, 1, 2, 3, 4
 TBE_NUM_BUCKETS = 11
 TBE_NUM_COUNTERS = 32
@@ -357,10 +357,11 @@ class TableBatchedEmbedding:
             esz = torch.tensor([], dtype=dtype).element_size()
             return self.ws_backward[off:off + n * esz].view(dtype)
 
-        counters = view(m.counters, TBE_NUM_COUNTERS, torch.int32).clone().cpu().numpy().view("uint32")
+        counters_device = view(m.counters, TBE_NUM_COUNTERS, torch.int32)
+        counters = counters_device.clone().cpu().numpy().view("uint32")
         N, U, nlong = int(counters[TBE_CNT_N]), int(counters[TBE_CNT_RUNS]), int(counters[TBE_CNT_LONG])
         out = dict(
-            counters=counters, N=N, U=U, num_long=nlong, num_chunks=int(counters[TBE_CNT_CHUNKS]),
+            counters=counters, counters_device=counters_device, N=N, U=U, num_long=nlong, num_chunks=int(counters[TBE_CNT_CHUNKS]),
             short_per_bucket=counters[TBE_CNT_SHORT0:TBE_CNT_SHORT0 + TBE_NUM_BUCKETS].copy(),
             sorted_keys=view(m.sorted_keys, N, torch.int32), sorted_bags=view(m.sorted_bags, N, torch.int32),
             unique_keys=view(m.unique_keys, U, torch.int32), run_offsets=view(m.run_offsets, U + 1, torch.int32),

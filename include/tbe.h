@@ -180,6 +180,10 @@ enum {
   TBE_STAT_UNREPAIRED = 2,    /* out-of-range ids or decreasing offsets met by a kernel that does
                                  not repair them; such lookups are skipped */
   TBE_STAT_WAIT_TIMEOUT = 3,  /* a bounded device-side wait gave up */
+  TBE_STAT_CHECK_FAILED = 4,  /* a library built with TBE_CHECKED=1 found an internal index or
+                                 range out of bounds (a run past the sorted lookups, a list slot
+                                 past its capacity, ...) and skipped the access; always 0 in the
+                                 default build, which compiles these checks out */
   TBE_NUM_STATS = 8
 };
 

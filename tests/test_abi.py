@@ -143,3 +143,14 @@ def test_misaligned_buffers_are_rejected_on_the_host(lib):
     p32, keep32 = _problem([8], [10], itype=tbe.TBE_I32)
     assert lib.tbe_forward(ctypes.byref(p32), ctypes.byref(o), ctypes.byref(t_ok), ok, ctypes.c_void_p(258), ok,
                            None, ok, None, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
+
+
+def test_checked_flavour_builds_with_the_same_exports():
+    """The TBE_CHECKED debug library (device-side range checks counted in
+    TBE_STAT_CHECK_FAILED) compiles from the same sources and exports the same C-ABI."""
+    path = tbe_build.build(checked=True)
+    assert path == tbe_build.CHECKED_LIB_PATH and path != tbe_build.LIB_PATH
+    checked = tbe.load(path)
+    for name in declared_functions():
+        assert hasattr(checked, name), f"{name} missing from the checked library"
+    assert tbe.STAT_NAMES[4] == "check_failed"
