@@ -58,6 +58,9 @@ def parse_args():
     ap.add_argument("--hoist", choices=["on", "off"], default="off",
                     help="run the backward's transpose (tbe_backward_prepare) on a second stream beside "
                          "the forward gather")
+    ap.add_argument("--reuse-counts", choices=["on", "off"], default="on",
+                    help="the backward of the counts x table tables takes the per-bag counts the forward "
+                         "of the same step saved (tbe_options.forward_ws) instead of reading the ids again")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tables", type=int, default=0,
@@ -133,8 +136,10 @@ def batch_stats(cfg, batch):
                 hottest=int(cnt.max()) if len(cnt) else 0)
 
 
-def byte_model(cfg, st, threshold=256, chunk=256, passes=None, bounds_ids=True):
-    """Algorithmic bytes of each stage for one step (what the method must move)."""
+def byte_model(cfg, st, threshold=256, chunk=256, passes=None, bounds_ids=True, reuse_counts=False):
+    """Algorithmic bytes of each stage for one step (what the method must move).  reuse_counts:
+    the counts x table forward saves each bag's counts (128 bytes) and the backward reads them in
+    place of the ids (ids past a bag's 256th, which it still reads, are left out of the model)."""
     wb = {"f32": 4, "f16": 2, "bf16": 2}[cfg.wdtype]
     ib = 4 if cfg.itype == "i32" else 8
     D = cfg.D.astype(np.int64)
@@ -145,12 +150,14 @@ def byte_model(cfg, st, threshold=256, chunk=256, passes=None, bounds_ids=True):
                      for t in cfg.tables])
     per_lookup = st["per_table"] * (D * wb + ib + pw)
     fwd = int(np.sum(per_lookup[~hist]) + int((~hist).sum()) * cfg.B * ib + cfg.B * int(D[~hist].sum()) * 4)
+    counts_bytes = int(hist.sum()) * cfg.B * 128 if reuse_counts else 0
     hist_bytes = int(np.sum(st["per_table"][hist] * ib) + int(hist.sum()) * cfg.B * ib
-                     + cfg.B * int(D[hist].sum()) * 4 + int(np.sum(cfg.E[hist] * D[hist] * wb)))
+                     + cfg.B * int(D[hist].sum()) * 4 + int(np.sum(cfg.E[hist] * D[hist] * wb)) + counts_bytes)
     hist_flops = int(np.sum(2 * cfg.B * cfg.E[hist] * D[hist]))
     # backward of those tables: counts^T x grad_out (ids and offsets again, the gradient slice,
     # the table and its state read and written once)
-    bwd_hist = int(np.sum(st["per_table"][hist] * ib) + int(hist.sum()) * cfg.B * ib
+    ids_again = counts_bytes if reuse_counts else int(np.sum(st["per_table"][hist] * ib))
+    bwd_hist = int(ids_again + int(hist.sum()) * cfg.B * ib
                    + cfg.B * int(D[hist].sum()) * 4 + int(np.sum(cfg.E[hist] * (2 * D[hist] * wb + 8))))
     bwd_hist_flops = hist_flops
     # gradient with respect to psw (weighted workloads): the rows again, the ids, one fp32 out per
@@ -411,7 +418,7 @@ class Workload:
         self.main = torch.cuda.current_stream(dev)
         self.side = torch.cuda.Stream(device=dev, priority=-1)  # its CTAs go first when SMs free up
         self.model = byte_model(cfg, self.st, self.opts.c.long_threshold, self.opts.c.chunk,
-                                bounds_ids=args.bounds != "fused")
+                                bounds_ids=args.bounds != "fused", reuse_counts=args.reuse_counts == "on")
 
     def step(self, fev=None, bev=None, bounds_ev=None, pev=None, gev=None, ins=None):
         args, tbe, cfg = self.args, self.tbe, self.cfg
@@ -438,7 +445,8 @@ class Workload:
                 gev[1].record()
         self.opts.with_events(bev)
         tbe.backward_update(self.weights, self.state, idx, off, self.grad, psw=psw, optimizer=cfg.optimizer,
-                            lr=cfg.lr, eps=cfg.eps, stats=self.stats, prepared=args.hoist == "on")
+                            lr=cfg.lr, eps=cfg.eps, stats=self.stats, prepared=args.hoist == "on",
+                            reuse_forward=args.reuse_counts == "on")
         self.opts.with_events(None)
 
     def timed(self, K, W, world=1, clocks=None):
@@ -665,6 +673,7 @@ def run_ours(args):
                          + (" (ids repaired inside tbe_forward)" if args.bounds == "fused" else "")),
                 "long_mode": args.long_mode, "scheduler": args.scheduler, "merge": args.merge, "gather": args.gather, "classify": args.classify,
                 "transpose": "hoisted beside the forward (second stream)" if args.hoist == "on" else "in the backward",
+                "counts_reuse": args.reuse_counts == "on",
                 "pooling": args.pooling, "psw_grad": bool(wl.psw_grad),
                 "parallelism": f"replicas x{world}",
                 "l2": "inputs larger than L2 (weights alone exceed 129 MB); no flush between steps",

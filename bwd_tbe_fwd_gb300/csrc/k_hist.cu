@@ -9,16 +9,18 @@
 //
 // GB300 design: a persistent CTA of 256 threads owns TMEM columns for one 128 x D fp32
 // accumulator and keeps the table in shared memory as the B operand.  Per tile of 128 bags:
-//   1. the tile's 129 offsets go to shared memory; all 256 threads stream the tile's contiguous
-//      id range with 16 coalesced loads in flight each, find every id's bag by binary search over
-//      the offsets, and for ids among the first 256 of their bag count them with 32-bit
-//      shared-memory atomics on packed 16-bit pairs; the counts are then written as the fp16 A
-//      tile (counts <= 256 are exact in fp16) in the canonical K-major layout without swizzle
-//      (8 x 16-byte core matrices);
+//   1. the tile's 129 offsets go to shared memory; each warp streams the contiguous positions of
+//      its 16 bags with four 16-byte id loads in flight per lane, walking the bag boundaries
+//      forward, and for ids among the first 256 of their bag counts them with 32-bit
+//      shared-memory atomics on packed 16-bit pairs (given a place to save them, the tile's
+//      counts also go to global memory for the backward); the counts are then written as the
+//      fp16 A tile (counts <= 256 are exact in fp16) in the canonical K-major layout without
+//      swizzle (8 x 16-byte core matrices);
 //   2. one thread issues four tcgen05.mma.cta_group::1.kind::f16 (M=128, N=D rounded up to 16,
 //      K=16 each) and commits them to an mbarrier; the CTA waits on it (bounded);
-//   3. warps 0-3 read their 32 accumulator lanes each (one bag per thread) with tcgen05.ld
-//      32x32b.x32, add the rows of ids past the 256th, and store the pooled row.
+//   3. all 8 warps read the accumulator (one bag per thread: warps w and w + 4 share TMEM lanes
+//      32 (w % 4) .. + 31 and split the 32-column chunks) with tcgen05.ld 32x32b.x32, add the rows
+//      of ids past the 256th, and store the pooled rows through shared memory as 128-byte pieces.
 // Counts x table is exact up to fp32 rounding, so the result equals the gather's sum.
 #include <atomic>
 
@@ -28,11 +30,16 @@ namespace tbe {
 namespace {
 
 constexpr int kThreads = 256;       // 8 warps count; warps 0-3 (one bag per thread) read TMEM
-constexpr int kIdsPerThread = 16;   // ids in flight per thread while counting
 constexpr int kM = 128;
 constexpr int kK = 64;              // E padded to 64
 constexpr int kMaxN = 128;          // D <= 128
 constexpr int kHistIds = 256;       // ids per bag counted by the histogram
+// id loads in flight per lane while counting: 16-byte loads in the forward, single ids in the
+// backward (measured faster each way)
+constexpr bool kFwdVecIds = true;
+constexpr int kFwdLoads = 4;
+constexpr bool kBwdVecIds = false;
+constexpr int kBwdLoads = 16;
 constexpr int kTileBytes = kM * kK * 2;  // A tile: 128 x 64 fp16 = 16 KB (B tile: 128 x 64 as well)
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -53,6 +60,7 @@ struct HistArgs {
   int E, D, N;           // N = D rounded up to a multiple of 16
   int col0, total_D;
   int fused_bounds;      // repair out-of-range ids in flight (row 0, written back) instead of skipping
+  uint32_t* save_pairs;  // NULL, or [B][32]: each bag's count pairs, saved for the backward
   unsigned long long* stats;
 };
 
@@ -121,6 +129,82 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Offsets of a tile's bags made non-decreasing (a bag never ends before it starts): each entry
+// becomes the running maximum of the ones before it.  Warp 0 scans the n + 1 <= 160 entries,
+// five per lane; the caller synchronizes before and after.
+__device__ __forceinline__ void monotone_offsets(int64_t* s_off, int n, int lane) {
+  constexpr int kPer = 5;
+  const int i0 = lane * kPer;
+  int64_t v[kPer], m = INT64_MIN;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    if (i0 + j <= n) m = max(m, s_off[i0 + j]);
+    v[j] = m;
+  }
+  int64_t incl = m;  // inclusive prefix maximum over the lanes
+  for (int d = 1; d < kWarp; d <<= 1) {
+    const int64_t o = __shfl_up_sync(FULL, incl, d);
+    if (lane >= d) incl = max(incl, o);
+  }
+  int64_t before = __shfl_up_sync(FULL, incl, 1);
+  if (lane == 0) before = INT64_MIN;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j)
+    if (i0 + j <= n) s_off[i0 + j] = max(v[j], before);
+}
+
+// Visits every lookup of the tile's bags once: warp w takes the bags [w * per, (w + 1) * per) of
+// the tile, one contiguous range of positions, and streams it with U loads in flight per lane
+// (16-byte loads of 16 / sizeof(IT) ids with VEC, else one id each); visit(r, bag, bag_start, id) gets the position relative to the
+// tile's first lookup p0, the bag within the tile and that bag's first position.  The loads start
+// at the 16-byte boundary at or below the range's first id (ids before it are loaded, not
+// visited); one that would pass the range's end, or an ids array not 16-byte aligned, takes
+// scalar loads.  A lane's positions only grow, so it walks its bag boundaries forward.
+template <typename IT, bool VEC, int U, int kWarps, typename F>
+__device__ __forceinline__ void for_each_lookup(const IT* ids, int64_t p0, bool vec_ok, const int* s_rel, int nb,
+                                                int warp, int lane, F&& visit) {
+  constexpr int V = VEC ? 16 / static_cast<int>(sizeof(IT)) : 1;
+  vec_ok = vec_ok && VEC;
+  const int per = (nb + kWarps - 1) / kWarps;
+  const int bw0 = min(nb, warp * per), bw1 = min(nb, bw0 + per);
+  const int r_beg = s_rel[bw0], r_end = s_rel[bw1];
+  if (r_beg >= r_end) return;  // (so bw0 < bw1)
+  int lo = bw0, cur = r_beg, nxt = s_rel[bw0 + 1];
+  const int r_first = r_beg - static_cast<int>((p0 + r_beg) & (V - 1));  // 16-byte aligned
+  for (int r0 = r_first; r0 < r_end; r0 += kWarp * V * U) {
+    IT id[U][V];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int rv = r0 + (u * kWarp + lane) * V;
+      if (vec_ok && rv + V <= r_end) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(ids + rv));
+        const IT* e = reinterpret_cast<const IT*>(&x);
+#pragma unroll
+        for (int j = 0; j < V; ++j) id[u][j] = e[j];
+      } else {
+#pragma unroll
+        for (int j = 0; j < V; ++j) id[u][j] = (rv + j >= r_beg && rv + j < r_end) ? __ldg(ids + rv + j) : IT(0);
+      }
+    }
+    bool past = false;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const int r = r0 + (u * kWarp + lane) * V + j;
+        past = past || r >= r_end;
+        if (past || r < r_beg) continue;
+        while (r >= nxt) {  // into the next bag (empty bags are stepped over)
+          ++lo;
+          cur = nxt;
+          nxt = lo + 1 <= bw1 ? s_rel[lo + 1] : 0x7fffffff;
+        }
+        visit(r, lo, cur, id[u][j]);
+      }
+    }
+  }
+}
+
 template <typename IT>
 __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -136,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
   __shared__ int s_rel[kM + 1];
 
   const int tid = threadIdx.x, lane = lane_id(), warp = tid / kWarp;
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(a.indices) & 15) == 0;  // 16-byte id loads
   const int64_t tiles = (a.B + kM - 1) / kM;
 
   // TMEM for the accumulator (warp 0 allocates for the CTA), the MMA completion barrier
@@ -145,18 +230,19 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
     s_failed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // B tile: element (n, k) = W[k][n] for k < E and n < D, zero elsewhere
-  for (int q = tid; q < kMaxN * (kK / 8); q += kThreads) {
-    const int n = q / (kK / 8), kb = (q % (kK / 8)) * 8;
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int k0 = kb + 2 * j, k1 = k0 + 1;
-      const __half h0 = (k0 < a.E && n < a.D) ? a.table[static_cast<int64_t>(k0) * a.D + n] : __float2half(0.f);
-      const __half h1 = (k1 < a.E && n < a.D) ? a.table[static_cast<int64_t>(k1) * a.D + n] : __float2half(0.f);
-      w[j] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+  // B tile: element (n, k) = W[k][n] for k < E and n < D, zero elsewhere.  A warp fills one
+  // 128-byte block (8 columns n x 8 rows k of core matrix memory) per step, one 32-bit pair of
+  // rows (k, k + 1) of one column per lane: the block covers every bank once
+  for (int blk = warp; blk < (kMaxN / 8) * (kK / 8); blk += kThreads / kWarp) {
+    const int n = (blk % (kMaxN / 8)) * 8 + (lane >> 2);
+    const int k = (blk / (kMaxN / 8)) * 8 + (lane & 3) * 2;
+    uint32_t w = 0;
+    if (n < a.D) {
+      const uint32_t h0 = k < a.E ? __half_as_ushort(a.table[static_cast<int64_t>(k) * a.D + n]) : 0u;
+      const uint32_t h1 = k + 1 < a.E ? __half_as_ushort(a.table[static_cast<int64_t>(k + 1) * a.D + n]) : 0u;
+      w = h0 | (h1 << 16);
     }
-    *reinterpret_cast<uint4*>(b_tile + kmajor_offset(n, kb)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint32_t*>(b_tile + kmajor_offset(n, k)) = w;
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -177,50 +263,34 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
       s_off[i] = o;
     }
     __syncthreads();
-    for (int i = 1; i <= nb; ++i) {  // guard: never let a bag end before it starts
-      if (tid == 0 && s_off[i] < s_off[i - 1]) s_off[i] = s_off[i - 1];
-    }
+    if (warp == 0) monotone_offsets(s_off, nb, lane);  // guard: never let a bag end before it starts
     __syncthreads();
     {
       // positions relative to the tile's first lookup (32-bit), bag starts in shared memory
       const int64_t p0 = s_off[0];
-      const int rel_end = static_cast<int>(s_off[nb] - p0);
       for (int i = tid; i <= nb; i += kThreads) s_rel[i] = static_cast<int>(s_off[i] - p0);
       __syncthreads();
-      const IT* ids = static_cast<const IT*>(a.indices) + p0;
+      IT* ids = const_cast<IT*>(static_cast<const IT*>(a.indices)) + p0;
       uint32_t bad = 0;
-      int lo = 0, cur = 0, nxt = nb > 0 ? s_rel[1] : 0x7fffffff;  // this thread's bag and its bounds
-      for (int base = 0; base < rel_end; base += kThreads * kIdsPerThread) {
-        IT id[kIdsPerThread];
-#pragma unroll
-        for (int j = 0; j < kIdsPerThread; ++j) {
-          const int r = base + j * kThreads + tid;
-          id[j] = r < rel_end ? __ldg(ids + r) : IT(0);
+      for_each_lookup<IT, kFwdVecIds, kFwdLoads, kThreads / kWarp>(ids, p0, vec_ok, s_rel, nb, warp, lane,
+                                                           [&](int r, int lo, int cur, IT id) {
+        if (static_cast<uint64_t>(static_cast<int64_t>(id)) >= static_cast<uint64_t>(a.E)) {
+          ++bad;
+          if (!a.fused_bounds) return;  // skipped (the scalar path skips it too)
+          ids[r] = IT(0);  // repaired in flight: row 0, written back
+          id = IT(0);
         }
-#pragma unroll
-        for (int j = 0; j < kIdsPerThread; ++j) {
-          const int r = base + j * kThreads + tid;
-          if (r >= rel_end) continue;
-          while (r >= nxt) {  // positions only increase: walk forward to r's bag
-            ++lo;
-            cur = nxt;
-            nxt = lo + 1 <= nb ? s_rel[lo + 1] : 0x7fffffff;
-          }
-          if (static_cast<uint64_t>(static_cast<int64_t>(id[j])) >= static_cast<uint64_t>(a.E)) {
-            ++bad;
-            if (!a.fused_bounds) continue;  // skipped (the scalar path skips it too)
-            const_cast<IT*>(ids)[r] = IT(0);  // repaired in flight: row 0, written back
-            id[j] = IT(0);
-          }
-          if (r - cur >= kHistIds) continue;  // the scalar path adds it
-          const uint32_t k = static_cast<uint32_t>(id[j]);
-          // two 16-bit counts per word (counts <= 256 never carry into the neighbour)
-          atomicAdd(&pairs[lo * (kK / 2) + (k >> 1)], (k & 1u) << 16 | (~k & 1u));
-        }
-      }
+        if (r - cur >= kHistIds) return;  // the scalar path adds it
+        const uint32_t k = static_cast<uint32_t>(id);
+        // two 16-bit counts per word (counts <= 256 never carry into the neighbour)
+        atomicAdd(&pairs[lo * (kK / 2) + (k >> 1)], (k & 1u) << 16 | (~k & 1u));
+      });
       if (bad) stat_add(a.stats, a.fused_bounds ? TBE_STAT_BAD_INDICES : TBE_STAT_UNREPAIRED, bad);
     }
     __syncthreads();
+    if (a.save_pairs != nullptr)  // the tile's counts for a backward on the same batch
+      for (int i = tid; i < nb * (kK / 8); i += kThreads)
+        reinterpret_cast<uint4*>(a.save_pairs + b0 * (kK / 2))[i] = reinterpret_cast<const uint4*>(pairs)[i];
     // counts -> fp16 A tile (exact: counts <= 256), 8 counts (one 16-byte row of a core matrix)
     // per item
     for (int q = tid; q < kM * (kK / 8); q += kThreads) {
@@ -258,19 +328,25 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
     }
     phase ^= 1u;
     tc_fence_after();
-    // 3. warps 0-3 read their bag rows out of TMEM, add the ids past the 256th, store
-    if (warp < kM / kWarp) {
-      const int64_t b = b0 + tid;
-      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * kWarp) << 16);
+    // 4. readout: warp w reads TMEM lanes 32 (w % 4) .. + 31 (one bag per thread) in the 32-column
+    //    chunks c0 = 32 j with j % 2 == w / 4, adds the ids past the 256th, stages the chunk in
+    //    shared memory (the A tile and the count pairs are free once the MMA has completed; 16-byte
+    //    slots XOR-swizzled by the row) and stores it as 128-byte row pieces, four bags per warp
+    //    instruction
+    {
+      const int quad = warp & 3, half = warp >> 2;
+      const int bag = quad * kWarp + lane;
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * kWarp) << 16);
+      float4* stage = reinterpret_cast<float4*>(half == 0 ? a_tile : reinterpret_cast<uint8_t*>(pairs)) + quad * (kWarp * 8);
       int64_t ts = 0, te = 0;
-      if (tid < nb) {
-        te = s_off[tid + 1];
-        ts = min(te, s_off[tid] + kHistIds);
+      if (bag < nb) {
+        te = s_off[bag + 1];
+        ts = min(te, s_off[bag] + kHistIds);
       }
-      for (int c0 = 0; c0 < a.N; c0 += 32) {
+      for (int c0 = half * 32; c0 < a.N; c0 += 64) {
         float v[32];
         tmem_ld32(lane_addr + c0, v);  // warp-wide: every lane takes part
-        if (tid < nb) {
+        if (bag < nb) {
           for (int64_t p = ts; p < te; ++p) {  // the scalar path of ids past the 256th
             const int64_t id = ld_int<IT>(a.indices, p);
             if (id < 0 || id >= a.E) continue;
@@ -279,11 +355,20 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
             for (int i = 0; i < 32; ++i)
               if (c0 + i < a.D) v[i] += __half2float(row[i]);
           }
-          float* orow = a.out + b * a.total_D + a.col0 + c0;
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            if (c0 + i < a.D) __stcs(reinterpret_cast<float4*>(orow + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
         }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          stage[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < kWarp / 4; ++it) {
+          const int r = it * 4 + (lane >> 3), j = lane & 7;  // row of the stage, 16-byte piece
+          const int rb = quad * kWarp + r;                     // its bag within the tile
+          if (rb < nb && c0 + 4 * j < a.D)
+            __stcs(reinterpret_cast<float4*>(a.out + (b0 + rb) * a.total_D + a.col0 + c0 + 4 * j),
+                   stage[r * 8 + (j ^ (r & 7))]);
+        }
+        __syncwarp();
       }
     }
     tc_fence_before();
@@ -311,8 +396,10 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
 // parts (hi + mid + lo carry all 24 significand bits and keep fp32's exponent range, so no
 // gradient overflows or flushes), and counts <= 256 are exact in bf16.  Per CTA and tile of 64
 // bags (K = 64; two CTAs per SM):
-//   1. count the first 256 ids of each bag as in the forward; ids past the 256th (rare) add
-//      their gradient row to the row's fp32 sum with atomics directly;
+//   1. count the first 256 ids of each bag as in the forward -- or, when the forward on the same
+//      batch saved its per-bag counts ([FBT] section 2, "Forward-state reuse"), load those and
+//      read no id among the first 256; ids past the 256th (rare) add their gradient row to the
+//      row's fp32 sum with atomics directly;
 //   2. B operand (N = E rounded up to 16, K-major): counts of row e in the tile's bags, bf16;
 //      A operands (M = 128 gradient columns, K-major): the three bf16 parts of grad_out[bag, d]
 //      -- a warp loads 8 bags x 32 columns coalesced and writes one 16-byte core-matrix row per
@@ -344,6 +431,7 @@ struct HistBwdArgs {
   int E, D, N, col0, total_D;
   int opt;
   float lr, eps;
+  const uint32_t* saved_pairs;  // NULL, or [B][32]: the counts the forward saved (ids not re-read)
   unsigned long long* stats;
 };
 
@@ -392,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2) hist_bwd_kernel(HistBwdArgs a) {
   __shared__ uint32_t s_rowcnt[kK];
 
   const int tid = threadIdx.x, lane = lane_id(), warp = tid / kWarp;
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(a.indices) & 15) == 0;  // 16-byte id loads
   const int64_t tiles = (a.B + kBK - 1) / kBK;
 
   if (warp == 0) tmem_alloc(&s_tmem, kBTmemCols);
@@ -413,54 +502,47 @@ __global__ void __launch_bounds__(kThreads, 2) hist_bwd_kernel(HistBwdArgs a) {
   for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++mine) {
     const int64_t b0 = tile * kBK;
     const int nb = static_cast<int>(min(static_cast<int64_t>(kBK), a.B - b0));
-    // 1. counts of the first 256 ids of each bag
-    for (int i = tid; i < kBK * kK / 2 / 4; i += kThreads) reinterpret_cast<uint4*>(pairs)[i] = make_uint4(0, 0, 0, 0);
+    // 1. counts of the first 256 ids of each bag: the ones the forward saved, or counted here
+    if (a.saved_pairs != nullptr) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.saved_pairs + b0 * (kK / 2));
+      for (int i = tid; i < kBK * kK / 2 / 4; i += kThreads)
+        reinterpret_cast<uint4*>(pairs)[i] = i < nb * (kK / 8) ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+    } else {
+      for (int i = tid; i < kBK * kK / 2 / 4; i += kThreads) reinterpret_cast<uint4*>(pairs)[i] = make_uint4(0, 0, 0, 0);
+    }
     for (int i = tid; i <= kBK; i += kThreads)
       s_off[i] = clamp64(ld_int<IT>(a.offsets, a.bag0 + b0 + min(i, nb)), 0, a.num_indices);
     __syncthreads();
-    for (int i = 1; i <= nb; ++i) {
-      if (tid == 0 && s_off[i] < s_off[i - 1]) s_off[i] = s_off[i - 1];
-    }
+    if (warp == 0) monotone_offsets(s_off, nb, lane);  // guard: never let a bag end before it starts
     __syncthreads();
     {
       const int64_t p0 = s_off[0];
-      const int rel_end = static_cast<int>(s_off[nb] - p0);
       for (int i = tid; i <= nb; i += kThreads) s_rel[i] = static_cast<int>(s_off[i] - p0);
       __syncthreads();
       const IT* ids = static_cast<const IT*>(a.indices) + p0;
       uint32_t bad = 0;
-      int lo = 0, cur = 0, nxt = nb > 0 ? s_rel[1] : 0x7fffffff;
-      for (int base = 0; base < rel_end; base += kThreads * kIdsPerThread) {
-        IT id[kIdsPerThread];
-#pragma unroll
-        for (int j = 0; j < kIdsPerThread; ++j) {
-          const int r = base + j * kThreads + tid;
-          id[j] = r < rel_end ? __ldg(ids + r) : IT(0);
+      auto visit = [&](int r, int lo, int cur, IT id) {
+        if (static_cast<uint64_t>(static_cast<int64_t>(id)) >= static_cast<uint64_t>(a.E)) {
+          ++bad;
+          return;
         }
-#pragma unroll
-        for (int j = 0; j < kIdsPerThread; ++j) {
-          const int r = base + j * kThreads + tid;
-          if (r >= rel_end) continue;
-          while (r >= nxt) {
-            ++lo;
-            cur = nxt;
-            nxt = lo + 1 <= nb ? s_rel[lo + 1] : 0x7fffffff;
-          }
-          if (static_cast<uint64_t>(static_cast<int64_t>(id[j])) >= static_cast<uint64_t>(a.E)) {
-            ++bad;
-            continue;
-          }
-          const uint32_t k = static_cast<uint32_t>(id[j]);
-          if (r - cur >= kHistIds) {
-            // past the 256th id of its bag: add the bag's gradient row to row k directly
-            const float4* g = reinterpret_cast<const float4*>(a.grad_out + (b0 + lo) * a.total_D + a.col0);
-            float4* dst = reinterpret_cast<float4*>(a.gsum + static_cast<int64_t>(k) * a.D);
-            for (int v = 0; v < a.D / 4; ++v) atomicAdd(dst + v, __ldg(g + v));
-            atomicAdd(&s_rowcnt[k], 1u);
-            continue;
-          }
-          atomicAdd(&pairs[lo * (kK / 2) + (k >> 1)], (k & 1u) << 16 | (~k & 1u));
+        const uint32_t k = static_cast<uint32_t>(id);
+        if (r - cur >= kHistIds) {
+          // past the 256th id of its bag: add the bag's gradient row to row k directly
+          const float4* g = reinterpret_cast<const float4*>(a.grad_out + (b0 + lo) * a.total_D + a.col0);
+          float4* dst = reinterpret_cast<float4*>(a.gsum + static_cast<int64_t>(k) * a.D);
+          for (int v = 0; v < a.D / 4; ++v) atomicAdd(dst + v, __ldg(g + v));
+          atomicAdd(&s_rowcnt[k], 1u);
+          return;
         }
+        atomicAdd(&pairs[lo * (kK / 2) + (k >> 1)], (k & 1u) << 16 | (~k & 1u));
+      };
+      if (a.saved_pairs != nullptr) {
+        // counts saved: only the ids past the 256th of each bag are read, a warp per bag
+        for (int bl = warp; bl < nb; bl += kThreads / kWarp)
+          for (int r = s_rel[bl] + kHistIds + lane; r < s_rel[bl + 1]; r += kWarp) visit(r, bl, s_rel[bl], __ldg(ids + r));
+      } else {
+        for_each_lookup<IT, kBwdVecIds, kBwdLoads, kThreads / kWarp>(ids, p0, vec_ok, s_rel, nb, warp, lane, visit);
       }
       if (bad) stat_add(a.stats, TBE_STAT_UNREPAIRED, bad);
     }
@@ -612,8 +694,8 @@ bool histogram_supported() { return true; }
 
 cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, const void* weights,
                                      const void* indices, const void* offsets, float* out, int table,
-                                     bool fused_bounds, unsigned long long* stats, const DeviceInfo& dev,
-                                     cudaStream_t s) {
+                                     bool fused_bounds, uint32_t* save_pairs, unsigned long long* stats,
+                                     const DeviceInfo& dev, cudaStream_t s) {
   (void)tab;
   int64_t woff = 0, col0 = 0;
   for (int t = 0; t < table; ++t) {
@@ -634,6 +716,7 @@ cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, co
   a.col0 = static_cast<int>(col0);
   a.total_D = P.total_D;
   a.fused_bounds = fused_bounds ? 1 : 0;
+  a.save_pairs = save_pairs;
   a.stats = stats;
   if (P.B == 0) return cudaSuccess;
   const size_t smem = 3 * kTileBytes + 1024;  // A, B, count pairs + alignment slack
@@ -662,7 +745,8 @@ cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, co
 size_t hist_backward_ws_bytes() { return kHistWsBytes; }
 
 cudaError_t launch_backward_histogram(const Problem& P, const BwdCtx& c, int table, void* hist_ws,
-                                      tbe_optimizer opt, const DeviceInfo& dev, cudaStream_t s) {
+                                      const uint32_t* saved_pairs, tbe_optimizer opt, const DeviceInfo& dev,
+                                      cudaStream_t s) {
   int64_t woff = 0, roff = 0, col0 = 0;
   for (int t = 0; t < table; ++t) {
     woff += P.E[t] * P.D[t];
@@ -690,6 +774,7 @@ cudaError_t launch_backward_histogram(const Problem& P, const BwdCtx& c, int tab
   a.opt = opt;
   a.lr = c.lr;
   a.eps = c.eps;
+  a.saved_pairs = saved_pairs;
   a.stats = c.stats;
   if (P.B == 0) return cudaSuccess;
   const size_t smem = 3 * kBATile + kBBTile + kBK * kK * 2 + 1024;

@@ -19,7 +19,8 @@
 //               reduce-then-scan: a per-CTA digit histogram over a contiguous segment, one
 //               exclusive scan of the [digit][CTA] counts, and a stable scatter in which each
 //               CTA walks its segment in 4096-key tiles, ranks keys with warp-level match
-//               (__match_any_sync) and per-warp digit counters in shared memory, reorders the
+//               (__match_any_sync; one ballot per digit bit in the first pass, whose digits
+//               are mostly distinct) and per-warp digit counters in shared memory, reorders the
 //               tile in shared memory and writes each digit's keys as one contiguous run.
 //               No CTA ever waits on another, so the sort needs no spin loops.
 //   RLE         two passes over the sorted keys: per-CTA head counts, then each CTA writes the
@@ -421,7 +422,22 @@ __global__ void __launch_bounds__(kThreads, 2) radix_downsweep_kernel(
     for (int i = 0; i < kSortItems; ++i) {
       const int e = w * (kSortItems * kWarp) + i * kWarp + lane;
       const uint32_t d = e < n ? ((k[i] >> shift) & (R - 1)) : static_cast<uint32_t>(R);
-      const unsigned peers = __match_any_sync(FULL, d);
+      // The lanes with the same digit.  The first pass reads the batch order, where a warp's 32
+      // digits are mostly distinct: there one ballot per digit bit is cheaper than the match,
+      // whose cost grows with the number of distinct values (it wins on the later passes, whose
+      // input is grouped by the lower digits).
+      unsigned peers;
+      if (!PSW && shift == 0) {
+        peers = __ballot_sync(FULL, d < R);
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+          const unsigned bb = __ballot_sync(FULL, (d >> b) & 1u);
+          peers &= ((d >> b) & 1u) ? bb : ~bb;
+        }
+        if (d >= R) peers = 1u << lane;  // past the tile: no counter, no rank
+      } else {
+        peers = __match_any_sync(FULL, d);
+      }
       const int leader = __ffs(peers) - 1;
       uint32_t base = 0;
       if (lane == leader && d < R) {

@@ -90,7 +90,16 @@ tbe_status check_options(const tbe_options& o) {
   if (o.num_events < 0 || (o.num_events > 0 && o.events == nullptr)) return TBE_ERR_INVALID_ARG;
   if (o.classify_mode != TBE_CLASSIFY_ORDERED && o.classify_mode != TBE_CLASSIFY_ATOMIC) return TBE_ERR_INVALID_ARG;
   if (o.prepared != 0 && o.prepared != 1) return TBE_ERR_INVALID_ARG;
+  if (!aligned(o.forward_ws, 16)) return TBE_ERR_INVALID_ARG;
   return TBE_OK;
+}
+
+// The counts x table tables whose per-bag counts the forward saves in its workspace (the first
+// kMaxHistTables eligible ones, as the backward takes them): their count and the bytes.
+int saved_count_tables(const Problem& P, const tbe_options& o) {
+  int n = 0;
+  for (int t = 0; t < P.T && n < kMaxHistTables; ++t) n += hist_forward_eligible(P, o, t) ? 1 : 0;
+  return n;
 }
 }  // namespace
 
@@ -463,16 +472,16 @@ tbe_status tbe_bounds_check_offsets(const tbe_problem* prob, const tbe_tables* t
 }
 
 size_t tbe_forward_workspace_size(const tbe_problem* prob, const tbe_options* opt) {
-  (void)prob;
-  (void)opt;
-  return 0;
+  Problem P;
+  if (make_problem(prob, &P) != TBE_OK) return 0;
+  const tbe_options o = resolve(opt);
+  if (check_options(o) != TBE_OK) return 0;
+  return static_cast<size_t>(saved_count_tables(P, o)) * static_cast<size_t>(P.B) * kHistPairsBytesPerBag;
 }
 
 tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tbe_tables* tables,
                        const void* weights, void* indices, const void* offsets, const float* psw,
                        float* out, void* ws, size_t ws_bytes, int64_t* d_stats, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   Problem P;
   tbe_status st = make_problem(prob, &P);
   if (st != TBE_OK) return st;
@@ -517,9 +526,17 @@ tbe_status tbe_forward(const tbe_problem* prob, const tbe_options* opt, const tb
     t0 = t1;
   }
   record_fwd(o, TBE_FWD_EV_GATHER, s);
-  for (int t : hist) {
+  // the per-bag counts of the first kMaxHistTables counts x table tables go to ws when it holds them
+  const size_t saved_bytes =
+      static_cast<size_t>(saved_count_tables(P, o)) * static_cast<size_t>(P.B) * kHistPairsBytesPerBag;
+  uint32_t* saved = (saved_bytes > 0 && ws != nullptr && ws_bytes >= saved_bytes && aligned(ws, 16))
+                        ? static_cast<uint32_t*>(ws) : nullptr;
+  for (size_t h = 0; h < hist.size(); ++h) {
+    const int t = hist[h];
+    uint32_t* save = saved != nullptr && h < static_cast<size_t>(kMaxHistTables)
+                         ? saved + h * static_cast<size_t>(P.B) * (kHistPairsBytesPerBag / 4) : nullptr;
     cudaError_t e = launch_forward_histogram(P, *tables, weights, indices, offsets, out, t, o.fused_bounds != 0,
-                                             stats, dev, s);
+                                             save, stats, dev, s);
     if (e == cudaSuccess)
       e = launch_forward_long_bags(P, *tables, weights, indices, offsets, psw, out, t * P.B, (t + 1) * P.B, dev, s);
     if (e != cudaSuccess) return cuda_status(e);
@@ -635,7 +652,10 @@ tbe_status tbe_backward_update(const tbe_problem* prob, const tbe_options* opt,
   if (c.nhist > 0) {
     if ((e = cudaMemsetAsync(c.hist_ws, 0, kHistWsBytes * c.nhist, s)) != cudaSuccess) return cuda_status(e);
     for (int h = 0; h < c.nhist; ++h) {
-      e = launch_backward_histogram(P, c, c.hist_t[h], c.hist_ws + kHistWsBytes * h, optimizer, dev, s);
+      const uint32_t* saved = o.forward_ws == nullptr ? nullptr
+                              : static_cast<const uint32_t*>(o.forward_ws) +
+                                    h * static_cast<size_t>(P.B) * (kHistPairsBytesPerBag / 4);
+      e = launch_backward_histogram(P, c, c.hist_t[h], c.hist_ws + kHistWsBytes * h, saved, optimizer, dev, s);
       if (e != cudaSuccess) return cuda_status(e);
     }
   }

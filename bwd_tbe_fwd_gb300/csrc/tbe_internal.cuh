@@ -173,12 +173,17 @@ cudaError_t launch_forward_long_bags(const Problem& P, const tbe_tables& tab, co
                                      int64_t unit_begin, int64_t unit_end, const DeviceInfo& dev, cudaStream_t s);
 
 bool histogram_supported();
+// saved_pairs / save_pairs: NULL, or the table's per-bag counts ([B][32] words, two 16-bit
+// counts each) that the forward saves and a backward on the same batch reads instead of the ids
 cudaError_t launch_backward_histogram(const Problem& P, const BwdCtx& c, int table, void* hist_ws,
-                                      tbe_optimizer opt, const DeviceInfo& dev, cudaStream_t s);
+                                      const uint32_t* saved_pairs, tbe_optimizer opt, const DeviceInfo& dev,
+                                      cudaStream_t s);
 cudaError_t launch_forward_histogram(const Problem& P, const tbe_tables& tab, const void* weights,
                                      const void* indices, const void* offsets, float* out, int table,
-                                     bool fused_bounds, unsigned long long* stats, const DeviceInfo& dev,
-                                     cudaStream_t s);
+                                     bool fused_bounds, uint32_t* save_pairs, unsigned long long* stats,
+                                     const DeviceInfo& dev, cudaStream_t s);
+// Bytes of the per-bag counts of one counts x table table, saved by the forward.
+constexpr size_t kHistPairsBytesPerBag = 32 * sizeof(uint32_t);
 
 cudaError_t launch_psw_gradient(const Problem& P, const tbe_tables& tab, const void* weights,
                                 const void* indices, const void* offsets, const float* grad_out,

@@ -61,7 +61,8 @@ class Options(ctypes.Structure):
     _fields_ = [("long_threshold", c_i32), ("chunk", c_i32), ("long_mode", c_i32), ("scheduler", c_i32),
                 ("histogram", c_i32), ("fused_bounds", c_i32), ("events", ctypes.POINTER(vp)),
                 ("num_events", c_i32), ("launch_counter", ctypes.POINTER(c_i64)), ("classify_mode", c_i32),
-                ("prepared", c_i32), ("merge", c_i32), ("gather", c_i32), ("nvtx", c_i32)]
+                ("prepared", c_i32), ("merge", c_i32), ("gather", c_i32), ("nvtx", c_i32),
+                ("forward_ws", vp)]
 
 
 class RunMetadata(ctypes.Structure):
@@ -323,7 +324,10 @@ class TableBatchedEmbedding:
 
     def backward_update(self, weights, state, indices, offsets, grad_out, psw=None, optimizer="adagrad",
                         lr=0.01, eps=1e-8, stats=None, stream=None, options: TBEOptions | None = None,
-                        prepared: bool = False):
+                        prepared: bool = False, reuse_forward: bool = False):
+        """reuse_forward: the last forward() of this object ran on the same batch (indices and
+        offsets unchanged since): its counts x table tables' per-bag counts, saved in the forward
+        workspace, replace reading their ids again (tbe_options.forward_ws)."""
         self._idx(indices, offsets)
         self._dev(weights, "weights", self.weight_dtype, self.num_weights)
         self._dev(state, "state", torch.float32, self.total_rows)
@@ -334,9 +338,11 @@ class TableBatchedEmbedding:
         o = (options or self.options).c
         if o.long_threshold != self.options.c.long_threshold or o.chunk != self.options.c.chunk:
             raise ValueError("threshold/chunk differ from the options the workspace was sized for")
-        if bool(o.prepared) != prepared:
+        if bool(o.prepared) != prepared or reuse_forward:
             o = Options.from_buffer_copy(o)
             o.prepared = 1 if prepared else 0
+            if reuse_forward:
+                o.forward_ws = self.ws_forward.data_ptr()
         with torch.cuda.device(self.device):
             st = self.lib.tbe_backward_update(
                 ctypes.byref(self.prob), ctypes.byref(o), ctypes.byref(self.tables), _ptr(weights), _ptr(state),

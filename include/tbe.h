@@ -171,6 +171,16 @@ typedef struct {
   int32_t nvtx;               /* 1: NVTX ranges (host side, one per stage: "tbe_forward.gather",
                                  "tbe_backward.sort", ...) around each stage's launches, for
                                  timeline tools; 0 (the default): none */
+  const void* forward_ws;     /* tbe_backward_update only.  NULL (the default), or the workspace
+                                 (16-byte aligned) of the tbe_forward call on the same batch --
+                                 the same problem and options, indices and offsets, ids not
+                                 changed in between -- which saved there the per-bag counts of
+                                 the counts x table tables ([FBT] section 2, "Forward-state
+                                 reuse"): the backward of those tables then takes their counts
+                                 from it instead of reading the ids again (it still reads the ids
+                                 past a bag's 256th, and does not count out-of-range ids among
+                                 the first 256 a second time).  The caller answers for the
+                                 match, as for `prepared`. */
 } tbe_options;
 
 /* Indices into d_stats (int64).  Counts accumulate over calls. */
@@ -213,7 +223,10 @@ tbe_status tbe_bounds_check(const tbe_problem* prob, const tbe_tables* tables, v
 tbe_status tbe_bounds_check_offsets(const tbe_problem* prob, const tbe_tables* tables, void* offsets,
                                     void* ws, size_t ws_bytes, int64_t* d_stats, void* stream);
 
-/* Pooled forward.  With opt->fused_bounds the kernels (gather and counts x table) repair
+/* Pooled forward.  ws: tbe_forward_workspace_size() bytes -- 128 per bag of each counts x table
+ * table (at most 8), 0 when there is none -- where the counts x table kernel saves each bag's
+ * counts for a backward that reuses them (tbe_options.forward_ws); with a NULL or smaller ws
+ * nothing is saved.  With opt->fused_bounds the kernels (gather and counts x table) repair
  * out-of-range ids as they read them (writing 0 back into indices, so the backward sees the
  * repaired id, counted as TBE_STAT_BAD_INDICES); without it the ids must be valid (out-of-range
  * ones are skipped and counted as TBE_STAT_UNREPAIRED).

@@ -191,7 +191,8 @@ class Case:
                                  f"({int(bad.sum())} of {n} out of tolerance)")
         return g
 
-    def backward(self, optimizer=None, steps=1, options=None, check_meta=True, prepared=False):
+    def backward(self, optimizer=None, steps=1, options=None, check_meta=True, prepared=False,
+                 reuse_forward=False):
         cfg = self.cfg
         assert steps == 1 or cfg.wdtype == "f32", "multi-step parity needs fp32 tables"
         opt = optimizer or cfg.optimizer
@@ -215,7 +216,8 @@ class Case:
                 self.tbe.forward(w_d, self.idx_d, self.off_d, psw=self.psw_d)
                 main.wait_stream(side)
             self.tbe.backward_update(w_d, state_d, self.idx_d, self.off_d, grad_d, psw=self.psw_d, optimizer=opt,
-                                     lr=cfg.lr, eps=cfg.eps, stats=self.stats, options=options, prepared=prepared)
+                                     lr=cfg.lr, eps=cfg.eps, stats=self.stats, options=options, prepared=prepared,
+                                     reuse_forward=reuse_forward)
             torch.cuda.synchronize()
             res = oracle.backward(self.tables, cfg.B, w_h, state_h, self.idx_h, self.off_h, grad_h, psw=self.psw_h,
                                   optimizer=opt, lr=cfg.lr, eps=cfg.eps, wdtype=cfg.wdtype, pooling=self.pooling)

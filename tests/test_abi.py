@@ -49,6 +49,7 @@ def test_version_status_and_defaults(lib):
     lib.tbe_default_options(ctypes.byref(o))
     assert (o.long_threshold, o.chunk, o.long_mode, o.scheduler, o.histogram, o.fused_bounds) == \
         (256, 256, tbe.TBE_LONG_AUTO, tbe.TBE_SCHED_PERSISTENT, 1, 0)
+    assert o.forward_ws is None
     assert (o.classify_mode, o.prepared, o.merge, o.gather, o.nvtx) == \
         (tbe.TBE_CLASSIFY_ORDERED, 0, 0, tbe.TBE_GATHER_REGISTER, 0)
 

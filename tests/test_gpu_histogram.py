@@ -128,3 +128,56 @@ def test_histogram_backward_counts_out_of_range_ids():
     # after repair the update equals the oracle's
     c.run_bounds()
     c.backward()
+
+
+def saved_counts(c, table_index=0):
+    """The per-bag counts the forward saved in its workspace for counts-path table `table_index`:
+    [B, 64] uint16 (two 16-bit counts per 32-bit word, the lower id in the lower half)."""
+    B = c.cfg.B
+    n = B * 128
+    raw = c.tbe.ws_forward[table_index * n:(table_index + 1) * n].view(torch.int16).cpu().numpy().view(np.uint16)
+    return raw.reshape(B, 64)
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_forward_saves_each_bags_counts(name):
+    """[FBT] section 2, "Forward-state reuse": the counts x table forward leaves, per bag, the
+    number of times each row appears among the bag's first 256 ids -- bit-exact against a count
+    on the host."""
+    cfg = CASES[name]
+    c = Case(cfg)
+    assert c.tbe.ws_forward.numel() >= cfg.B * 128
+    c.tbe.ws_forward.fill_(0xAB)
+    c.forward()
+    got = saved_counts(c)
+    E = cfg.tables[0].E
+    expect = np.zeros((cfg.B, 64), dtype=np.uint16)
+    for b in range(cfg.B):
+        ids = c.idx_h[c.off_h[b]:c.off_h[b + 1]][:256].astype(np.int64)
+        expect[b, :E] = np.bincount(ids, minlength=E)
+    assert np.array_equal(got, expect)
+
+
+@pytest.mark.parametrize("optimizer", ["adagrad", "sgd"])
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_histogram_backward_reusing_forward_counts(name, optimizer):
+    """The backward that takes table 0's counts from the forward of the same batch (reading no id
+    among a bag's first 256) matches the oracle as the recounting one does."""
+    c = Case(CASES[name])
+    c.forward()
+    c.backward(optimizer=optimizer, reuse_forward=True)
+
+
+def test_histogram_forward_with_ids_not_16_byte_aligned():
+    """Ids whose array starts 8 bytes past a 16-byte boundary take the scalar loads."""
+    cfg = CASES["ragged_tile_E37_D96"]
+    c = Case(cfg)
+    buf = torch.empty(c.idx_d.numel() + 1, dtype=c.idx_d.dtype, device="cuda")
+    ids = buf[1:]
+    ids.copy_(c.idx_d)
+    assert ids.data_ptr() % 16 == 8
+    out = c.tbe.forward(c.w0.cuda(), ids, c.off_d)
+    torch.cuda.synchronize()
+    _, exact, absterms = oracle.forward(c.tables, cfg.B, weights_to_oracle(c.w0, cfg.wdtype), c.idx_h, c.off_h,
+                                        wdtype=cfg.wdtype)
+    check_forward(out.cpu().numpy(), exact, absterms, cfg.wdtype)
