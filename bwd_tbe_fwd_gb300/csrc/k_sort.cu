@@ -236,16 +236,18 @@ __global__ void __launch_bounds__(kThreads) radix_upsweep_kernel(const uint32_t*
   const int64_t nvec = (b1 - b0) / 4;  // b0 is a multiple of the tile: 16-byte aligned
   const uint4* kv = reinterpret_cast<const uint4*>(keys + b0);
   int64_t i = threadIdx.x;
-  for (; i + blockDim.x < nvec; i += 2 * blockDim.x) {
-    const uint4 k0 = kv[i], k1 = kv[i + blockDim.x];
-    atomicAdd(&hist[w][(k0.x >> shift) & (R - 1)], 1u);
-    atomicAdd(&hist[w][(k0.y >> shift) & (R - 1)], 1u);
-    atomicAdd(&hist[w][(k0.z >> shift) & (R - 1)], 1u);
-    atomicAdd(&hist[w][(k0.w >> shift) & (R - 1)], 1u);
-    atomicAdd(&hist[w][(k1.x >> shift) & (R - 1)], 1u);
-    atomicAdd(&hist[w][(k1.y >> shift) & (R - 1)], 1u);
-    atomicAdd(&hist[w][(k1.z >> shift) & (R - 1)], 1u);
-    atomicAdd(&hist[w][(k1.w >> shift) & (R - 1)], 1u);
+  constexpr int UP = 4;  // 16-byte loads in flight per thread (2 or 8 measured slower)
+  for (; i + (UP - 1) * static_cast<int64_t>(blockDim.x) < nvec; i += UP * blockDim.x) {
+    uint4 k[UP];
+#pragma unroll
+    for (int u = 0; u < UP; ++u) k[u] = kv[i + u * blockDim.x];
+#pragma unroll
+    for (int u = 0; u < UP; ++u) {
+      atomicAdd(&hist[w][(k[u].x >> shift) & (R - 1)], 1u);
+      atomicAdd(&hist[w][(k[u].y >> shift) & (R - 1)], 1u);
+      atomicAdd(&hist[w][(k[u].z >> shift) & (R - 1)], 1u);
+      atomicAdd(&hist[w][(k[u].w >> shift) & (R - 1)], 1u);
+    }
   }
   for (; i < nvec; i += blockDim.x) {
     const uint4 k0 = kv[i];
