@@ -62,6 +62,9 @@ def parse_args():
                     help="the backward of the counts x table tables takes the per-bag counts the forward "
                          "of the same step saved (tbe_options.forward_ws) instead of reading the ids again")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the side measurement of the other run classifier (a few steps of the "
+                         "headline workload with --classify flipped)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tables", type=int, default=0,
                     help="keep only the first T tables of the workload (small cases for profiling)")
@@ -639,6 +642,20 @@ def run_ours(args):
                        "buffered: step k+1's copy overlaps step k), bounds+forward+backward, the step's "
                        "int64 counters device->host; wall clock over all steps"}
 
+    # the other classifier on the same workload: [FBT] section 4, Problem 4 names one atomic per
+    # block per list (ATOMIC); ORDERED writes the lists in key order (the default)
+    side = None
+    if rank == 0 and world == 1 and not args.no_side:
+        from bwd_tbe_fwd_gb300.tbe import TBE_CLASSIFY_ATOMIC, TBE_CLASSIFY_ORDERED
+        keep = wl.opts.c.classify_mode
+        wl.opts.c.classify_mode = TBE_CLASSIFY_ATOMIC if keep == TBE_CLASSIFY_ORDERED else TBE_CLASSIFY_ORDERED
+        ks = min(K, 10)
+        ts = wl.timed(ks, 3)
+        wl.opts.c.classify_mode = keep
+        side = {"classify": "atomic" if keep == TBE_CLASSIFY_ORDERED else "ordered", "steps": ks,
+                "ms_per_step": round(ts["ms_total"] / ks, 4),
+                "stages_ms": {k: round(float(ts["stage_ms"][k]), 4) for k in ("classify", "short", "long")}}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, wl.batch, args.cpu_sample_bags)
@@ -682,6 +699,7 @@ def run_ours(args):
             "roofline": roof,
             "stages": stages,
             "per_config": per_config,
+            "classify_alternative": side,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clk,

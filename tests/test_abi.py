@@ -155,3 +155,44 @@ def test_checked_flavour_builds_with_the_same_exports():
     for name in declared_functions():
         assert hasattr(checked, name), f"{name} missing from the checked library"
     assert tbe.STAT_NAMES[4] == "check_failed"
+
+
+def test_forward_workspace_holds_the_saved_counts(lib):
+    """tbe_forward_workspace_size(): 128 bytes per bag for each counts x table table (fp16,
+    E <= 64, 64 <= D <= 128, long bags, unweighted sum pooling), at most 8 of them; 0 when no
+    table qualifies or the path is off."""
+    D = [128] * 10 + [64, 96]
+    E = [64] * 10 + [1000, 50]
+    flags = [1] * 10 + [1, 0]  # table 10 is too tall, table 11 has no long-bags flag
+    long_bags = (ctypes.c_uint8 * len(D))(*flags)
+    p, keep = _problem(D, E, B=100, n=1000)
+    p.long_bags = ctypes.cast(long_bags, ctypes.POINTER(ctypes.c_uint8))
+    o = tbe.Options()
+    lib.tbe_default_options(ctypes.byref(o))
+    assert lib.tbe_forward_workspace_size(ctypes.byref(p), ctypes.byref(o)) == 8 * 100 * 128
+    o.histogram = 0
+    assert lib.tbe_forward_workspace_size(ctypes.byref(p), ctypes.byref(o)) == 0
+    lib.tbe_default_options(ctypes.byref(o))
+    p.weighted = 1
+    assert lib.tbe_forward_workspace_size(ctypes.byref(p), ctypes.byref(o)) == 0
+    p.weighted = 0
+    p.long_bags = None
+    assert lib.tbe_forward_workspace_size(ctypes.byref(p), ctypes.byref(o)) == 0
+
+
+def test_misaligned_forward_ws_is_rejected_on_the_host(lib):
+    """tbe_options.forward_ws must be 16-byte aligned: the options are rejected (workspace queries
+    answer 0, entry points INVALID_ARG) before any launch.  Data pointers are NULL, so that
+    nothing could reach a kernel even if a check were missing."""
+    p, keep = _problem([8], [10])
+    t = tbe.Tables(None, None, None)
+    o = tbe.Options()
+    lib.tbe_default_options(ctypes.byref(o))
+    o.forward_ws = 256 + 8
+    assert lib.tbe_backward_workspace_size(ctypes.byref(p), ctypes.byref(o)) == 0
+    assert lib.tbe_forward_workspace_size(ctypes.byref(p), ctypes.byref(o)) == 0
+    assert lib.tbe_backward_update(ctypes.byref(p), ctypes.byref(o), ctypes.byref(t), None, None, None, None,
+                                   None, None, tbe.TBE_OPT_ROWWISE_ADAGRAD, 0.1, 1e-8, None, 0, None,
+                                   None) == tbe.TBE_ERR_INVALID_ARG
+    o.forward_ws = 256
+    assert lib.tbe_forward_workspace_size(ctypes.byref(p), ctypes.byref(o)) == 0  # no counts-path table
