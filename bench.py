@@ -334,8 +334,9 @@ def source_digest(files) -> str:
 _CSRC = "bwd_tbe_fwd_gb300/csrc/"
 KERNEL_SOURCES = {
     "gather": [_CSRC + "k_forward.cu", _CSRC + "tbe_internal.cuh"],
-    "short": [_CSRC + "k_short.cu", _CSRC + "k_update_common.cuh", _CSRC + "tbe_internal.cuh"],
-    "long": [_CSRC + "k_long.cu", _CSRC + "k_update_common.cuh", _CSRC + "tbe_internal.cuh"],
+    # the update kernels walk the run lists in the classifier's order, which shapes their traffic
+    "short": [_CSRC + "k_short.cu", _CSRC + "k_update_common.cuh", _CSRC + "k_classify.cu", _CSRC + "tbe_internal.cuh"],
+    "long": [_CSRC + "k_long.cu", _CSRC + "k_update_common.cuh", _CSRC + "k_classify.cu", _CSRC + "tbe_internal.cuh"],
     "sort": [_CSRC + "k_sort.cu", _CSRC + "tbe_internal.cuh"],
     "histogram": [_CSRC + "k_hist.cu", _CSRC + "tbe_internal.cuh"],
     "bwd_histogram": [_CSRC + "k_hist.cu", _CSRC + "tbe_internal.cuh"],
