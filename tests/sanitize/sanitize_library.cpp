@@ -1,7 +1,7 @@
 // The CUDA library's host code (the problem planner, argument validation, workspace layout, the
 // no-alloc entry point) built with AddressSanitizer and UndefinedBehaviorSanitizer and driven
-// through its C interface on paths that return before any device work: the table layout and the
-// rejection of invalid problems, options and buffers.  Any invalid memory access or undefined
+// through its C interface on paths that return before any device work: the table layout, the
+// forward workspace rule and the rejection of invalid problems, options and buffers.  Any invalid memory access or undefined
 // behaviour aborts the program (-fno-sanitize-recover); it prints "sanitize ok" at the end.
 #include <cstdint>
 #include <cstdio>
@@ -75,6 +75,21 @@ void library_validation() {
   expect(tbe_forward(&p, &bad, &tabs, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr) !=
              TBE_OK,
          "bad options rejected");
+  // the forward workspace: 128 bytes per bag of each counts x table table (at most 8), none otherwise
+  const int32_t hD[10] = {128, 128, 128, 128, 128, 128, 128, 128, 128, 64};
+  const int64_t hE[10] = {64, 64, 64, 64, 64, 64, 64, 64, 64, 1000};
+  const uint8_t hL[10] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1};
+  tbe_problem h = p;
+  h.T = 10;
+  h.D = hD;
+  h.E = hE;
+  h.long_bags = hL;
+  expect(tbe_forward_workspace_size(&h, &o) == size_t(8) * 4 * 128, "forward workspace: eight counts tables");
+  expect(tbe_forward_workspace_size(&p, &o) == 0, "forward workspace: no counts table");
+  tbe_options mis = o;
+  mis.forward_ws = reinterpret_cast<const void*>(uintptr_t(4096 + 8));
+  expect(tbe_forward_workspace_size(&h, &mis) == 0, "misaligned forward_ws rejected");
+  expect(tbe_backward_workspace_size(&h, &mis) == 0, "misaligned forward_ws rejected by the backward");
   for (int s = 0; s <= 6; ++s) expect(tbe_status_string(static_cast<tbe_status>(s)) != nullptr, "status strings");
   expect(tbe_version() == TBE_VERSION, "version");
 }
