@@ -181,3 +181,11 @@ def test_histogram_forward_with_ids_not_16_byte_aligned():
     _, exact, absterms = oracle.forward(c.tables, cfg.B, weights_to_oracle(c.w0, cfg.wdtype), c.idx_h, c.off_h,
                                         wdtype=cfg.wdtype)
     check_forward(out.cpu().numpy(), exact, absterms, cfg.wdtype)
+
+
+def test_histogram_backward_prepared_beside_the_forward_and_reusing_counts():
+    """The transpose of the sort-path tables prepared on a second stream beside the forward, and
+    the counts-path table's counts taken from that forward: the update matches the oracle and the
+    sort-path metadata is bit-exact."""
+    c = Case(CASES["c4_like"])
+    c.backward(prepared=True, reuse_forward=True)
