@@ -189,3 +189,18 @@ def test_histogram_backward_prepared_beside_the_forward_and_reusing_counts():
     sort-path metadata is bit-exact."""
     c = Case(CASES["c4_like"])
     c.backward(prepared=True, reuse_forward=True)
+
+
+@pytest.mark.parametrize("reuse", [False, True], ids=["recount", "reuse"])
+def test_more_than_eight_counts_tables(reuse):
+    """Twelve tables qualify for the counts x table path: the forward serves all twelve on it,
+    the backward the first eight (the rest go through the sort), and the forward saves the counts
+    of those eight only."""
+    spec = TableSpec(48, 64, LengthSpec("poisson", 90.0), IdSpec("uniform"), histogram=True)
+    tables = (spec,) * 12 + (TableSpec(3000, 96, LengthSpec("poisson", 8.0), IdSpec("zipf", s=1.1)),)
+    cfg = dataclasses.replace(get_config("c4"), name="hist12", B=160, tables=tables, bad_id_frac=0.0)
+    c = Case(cfg)
+    assert c.counts_path_tables() == list(range(8))
+    assert c.tbe.ws_forward.numel() >= 8 * cfg.B * 128
+    c.forward()
+    c.backward(reuse_forward=reuse)

@@ -368,3 +368,19 @@ def test_nvtx_ranges_option_changes_nothing():
     c = Case(SMALL["c5"], options=TBEOptions(nvtx=1))
     c.forward(options=TBEOptions(nvtx=1))
     c.backward(options=TBEOptions(nvtx=1))
+
+
+def test_hundreds_of_tables():
+    """300 tables of 1 to 400 rows and mixed widths (one row in some tables): gather items, the
+    table search of linear keys and the per-bucket launches over many small tables."""
+    import dataclasses
+    import numpy as np
+    from synth.configs import IdSpec, LengthSpec, TableSpec
+    rng = np.random.default_rng(7)
+    widths = [4, 8, 16, 24, 32, 64, 128]
+    tables = tuple(TableSpec(1 if i % 50 == 0 else int(rng.integers(1, 400)), int(rng.choice(widths)),
+                             LengthSpec("poisson", 3.0), IdSpec("zipf", s=1.1)) for i in range(300))
+    cfg = dataclasses.replace(get_config("c5"), name="t300", B=40, tables=tables, bad_id_frac=0.0)
+    c = Case(cfg, threshold=16, chunk=8)
+    c.forward()
+    c.backward()
