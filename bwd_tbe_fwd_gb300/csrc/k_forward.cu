@@ -678,9 +678,10 @@ constexpr int kLongBag = 16384;
 constexpr int kSegment = 1024;
 constexpr int kLongThreads = 128;
 
-template <typename WT, typename IT, bool PSW>
+template <typename WT, typename IT, bool PSW, int VB>
 __global__ void __launch_bounds__(kLongThreads, 8) fwd_long_bags_kernel(FwdArgs a) {
-  using IO = VecIO<WT, 16>;
+  using IO = VecIO<WT, VB>;  // rows read as 16-byte vectors, or 8-byte ones for widths that need it
+  using Raw = typename IO::Raw;
   constexpr int NE = IO::N;
   constexpr int UNROLL = PSW ? 4 : 8;
   const unsigned FULL = 0xffffffffu;
@@ -705,14 +706,14 @@ __global__ void __launch_bounds__(kLongThreads, 8) fwd_long_bags_kernel(FwdArgs 
       const int t = static_cast<int>(ub / a.B);
       const int64_t b = ub - static_cast<int64_t>(t) * a.B;
       const int col0 = __ldg(a.doff + t);
-      const int nvec = (__ldg(a.doff + t + 1) - col0) * static_cast<int>(sizeof(WT)) / 16;
+      const int nvec = (__ldg(a.doff + t + 1) - col0) * static_cast<int>(sizeof(WT)) / VB;
       const int E = static_cast<int>(__ldg(a.roff + t + 1) - __ldg(a.roff + t));
-      const uint4* table = reinterpret_cast<const uint4*>(static_cast<const WT*>(a.weights) + __ldg(a.woff + t));
+      const Raw* table = reinterpret_cast<const Raw*>(static_cast<const WT*>(a.weights) + __ldg(a.woff + t));
       const int lpr = nvec >= kWarp ? kWarp : (nvec <= 1 ? 1 : 1 << (32 - __clz(nvec - 1)));
       const int rps = kWarp / lpr, slot = lane / lpr, vi = lane % lpr;
       const float inv = a.mean ? 1.0f / static_cast<float>(be - bs) : 1.0f;
       float* orow = a.out + b * a.total_D + col0;
-      // one pass over the bag per 32 vectors of the row (one pass for rows of up to 512 bytes)
+      // one pass over the bag per 32 vectors of the row (one pass for rows of up to 32 * VB bytes)
       for (int c = vi; c - vi < nvec; c += kWarp) {
         float tot[NE], seg[NE];
 #pragma unroll
@@ -720,7 +721,7 @@ __global__ void __launch_bounds__(kLongThreads, 8) fwd_long_bags_kernel(FwdArgs 
         for (int g0 = bs; g0 < be; g0 += kSegment) {
           const int g1 = be - g0 > kSegment ? g0 + kSegment : be;
           for (int p = g0; p < g1; p += rps * UNROLL) {
-            uint4 v[UNROLL];
+            Raw v[UNROLL];
             float w[UNROLL];
 #pragma unroll
             for (int q = 0; q < UNROLL; ++q) {
@@ -732,8 +733,8 @@ __global__ void __launch_bounds__(kLongThreads, 8) fwd_long_bags_kernel(FwdArgs 
                 if (id < 0 || id >= E) id = -1;  // skipped (and counted) by the gather
                 else if (PSW) w[q] = __ldg(a.psw + pos);
               }
-              v[q] = make_uint4(0, 0, 0, 0);
-              if (id >= 0 && c < nvec) v[q] = __ldg(table + id * nvec + c);
+              v[q] = Raw{};
+              if (id >= 0 && c < nvec) v[q] = ldg_raw(table + id * nvec + c);
             }
 #pragma unroll
             for (int q = 0; q < UNROLL; ++q) {
@@ -975,8 +976,7 @@ cudaError_t launch_forward_gather(const Problem& P, const tbe_tables& tab, const
 cudaError_t launch_forward_long_bags(const Problem& P, const tbe_tables& tab, const void* weights,
                                      const void* indices, const void* offsets, const float* psw, float* out,
                                      int64_t unit_begin, int64_t unit_end, const DeviceInfo& dev, cudaStream_t s) {
-  if (unit_end <= unit_begin || P.wbytes != 2 || P.vec_bytes != 16 || P.max_D * P.wbytes > 16 * 4 * kWarp)
-    return cudaSuccess;
+  if (unit_end <= unit_begin || P.wbytes != 2) return cudaSuccess;
   if (P.num_indices <= kLongBag) return cudaSuccess;  // no bag can be long
   FwdArgs a{};
   a.weights = weights;
@@ -999,16 +999,22 @@ cudaError_t launch_forward_long_bags(const Problem& P, const tbe_tables& tab, co
   if (blocks > cap) blocks = cap;
   const bool w = psw != nullptr;
   const bool i32 = P.itype == TBE_I32;
+  auto go = [&](auto wt, auto vb) {
+    using WT = decltype(wt);
+    constexpr int VB = decltype(vb)::value;
+    if (i32) w ? fwd_long_bags_kernel<WT, int32_t, true, VB><<<blocks, kLongThreads, 0, s>>>(a)
+             : fwd_long_bags_kernel<WT, int32_t, false, VB><<<blocks, kLongThreads, 0, s>>>(a);
+    else w ? fwd_long_bags_kernel<WT, int64_t, true, VB><<<blocks, kLongThreads, 0, s>>>(a)
+           : fwd_long_bags_kernel<WT, int64_t, false, VB><<<blocks, kLongThreads, 0, s>>>(a);
+  };
+  using V16 = std::integral_constant<int, 16>;
+  using V8 = std::integral_constant<int, 8>;
   if (P.wdtype == TBE_F16) {
-    if (i32) w ? fwd_long_bags_kernel<__half, int32_t, true><<<blocks, kLongThreads, 0, s>>>(a)
-             : fwd_long_bags_kernel<__half, int32_t, false><<<blocks, kLongThreads, 0, s>>>(a);
-    else w ? fwd_long_bags_kernel<__half, int64_t, true><<<blocks, kLongThreads, 0, s>>>(a)
-           : fwd_long_bags_kernel<__half, int64_t, false><<<blocks, kLongThreads, 0, s>>>(a);
+    if (P.vec_bytes == 16) go(__half{}, V16{});
+    else go(__half{}, V8{});
   } else {
-    if (i32) w ? fwd_long_bags_kernel<__nv_bfloat16, int32_t, true><<<blocks, kLongThreads, 0, s>>>(a)
-             : fwd_long_bags_kernel<__nv_bfloat16, int32_t, false><<<blocks, kLongThreads, 0, s>>>(a);
-    else w ? fwd_long_bags_kernel<__nv_bfloat16, int64_t, true><<<blocks, kLongThreads, 0, s>>>(a)
-           : fwd_long_bags_kernel<__nv_bfloat16, int64_t, false><<<blocks, kLongThreads, 0, s>>>(a);
+    if (P.vec_bytes == 16) go(__nv_bfloat16{}, V16{});
+    else go(__nv_bfloat16{}, V8{});
   }
   note_launch();
   return cudaGetLastError();

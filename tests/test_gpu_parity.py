@@ -332,14 +332,15 @@ def test_graph_capture_no_host_sync():
 
 
 @pytest.mark.parametrize("gather", ["register", "tma"])
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [100, 128, 256])
 @pytest.mark.parametrize("lengths", [(600_000, 3, 7), (1_050_000,)])
 def test_very_long_bags_hold_the_tolerance(lengths, D, gather):
     """Bags of 6*10^5 and 1.05*10^6 lookups of Zipf-hot fp16 rows (the stress workload's id law
     over a table of 61 rows, so the hottest rows are each added 4*10^4 - 10^5 times into one bag)
     beside short ones: every pooled element within the fp16 bound of the oracle's exact sum.  At
     D = 256 every lane of the register gather sums one column over the whole bag (at D = 128 two
-    row slots share it), which is where a single fp32 running sum drifts furthest."""
+    row slots share it), which is where a single fp32 running sum drifts furthest; D = 100 rows
+    (200 bytes) are read as 8-byte vectors, by the register gather whichever gather is asked for."""
     import dataclasses
     from synth.configs import LengthSpec
     from bwd_tbe_fwd_gb300.tbe import TBE_GATHER_REGISTER, TBE_GATHER_TMA
