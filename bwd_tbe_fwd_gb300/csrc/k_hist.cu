@@ -230,20 +230,6 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
     s_failed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // B tile: element (n, k) = W[k][n] for k < E and n < D, zero elsewhere.  A warp fills one
-  // 128-byte block (8 columns n x 8 rows k of core matrix memory) per step, one 32-bit pair of
-  // rows (k, k + 1) of one column per lane: the block covers every bank once
-  for (int blk = warp; blk < (kMaxN / 8) * (kK / 8); blk += kThreads / kWarp) {
-    const int n = (blk % (kMaxN / 8)) * 8 + (lane >> 2);
-    const int k = (blk / (kMaxN / 8)) * 8 + (lane & 3) * 2;
-    uint32_t w = 0;
-    if (n < a.D) {
-      const uint32_t h0 = k < a.E ? __half_as_ushort(a.table[static_cast<int64_t>(k) * a.D + n]) : 0u;
-      const uint32_t h1 = k + 1 < a.E ? __half_as_ushort(a.table[static_cast<int64_t>(k + 1) * a.D + n]) : 0u;
-      w = h0 | (h1 << 16);
-    }
-    *reinterpret_cast<uint32_t*>(b_tile + kmajor_offset(n, k)) = w;
-  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -252,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
   const uint32_t idesc = instr_desc(kM, a.N);
   const uint64_t a_desc0 = smem_desc(smem_u32(a_tile)), b_desc0 = smem_desc(smem_u32(b_tile));
   uint32_t phase = 0;
+  bool b_built = false;
 
   for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int64_t b0 = tile * kM;
@@ -291,6 +278,25 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
     if (a.save_pairs != nullptr)  // the tile's counts for a backward on the same batch
       for (int i = tid; i < nb * (kK / 8); i += kThreads)
         reinterpret_cast<uint4*>(a.save_pairs + b0 * (kK / 2))[i] = reinterpret_cast<const uint4*>(pairs)[i];
+    if (!b_built) {
+      // B tile (once per CTA, after its first tile's ids are counted, so that the id stream starts
+      // at once and the CTAs' reads of the table from L2 spread out): element (n, k) = W[k][n] for
+      // k < E and n < D, zero elsewhere.  A warp fills one 128-byte block (8 columns n x 8 rows k
+      // of core matrix memory) per step, one 32-bit pair of rows (k, k + 1) of one column per
+      // lane: the block covers every bank once
+      for (int blk = warp; blk < (kMaxN / 8) * (kK / 8); blk += kThreads / kWarp) {
+        const int n = (blk % (kMaxN / 8)) * 8 + (lane >> 2);
+        const int k = (blk / (kMaxN / 8)) * 8 + (lane & 3) * 2;
+        uint32_t w = 0;
+        if (n < a.D) {
+          const uint32_t h0 = k < a.E ? __half_as_ushort(a.table[static_cast<int64_t>(k) * a.D + n]) : 0u;
+          const uint32_t h1 = k + 1 < a.E ? __half_as_ushort(a.table[static_cast<int64_t>(k + 1) * a.D + n]) : 0u;
+          w = h0 | (h1 << 16);
+        }
+        *reinterpret_cast<uint32_t*>(b_tile + kmajor_offset(n, k)) = w;
+      }
+      b_built = true;
+    }
     // counts -> fp16 A tile (exact: counts <= 256), 8 counts (one 16-byte row of a core matrix)
     // per item
     for (int q = tid; q < kM * (kK / 8); q += kThreads) {
