@@ -8,7 +8,8 @@
 // scalar path.  The pages evaluate counts x table with a Triton dot over 16 bags per program.
 //
 // GB300 design: a persistent CTA of 256 threads owns TMEM columns for one 128 x D fp32
-// accumulator and keeps the table in shared memory as the B operand.  Per tile of 128 bags:
+// accumulator and keeps the table in shared memory as the B operand (written once, after the
+// CTA's first tile's ids are counted).  Per tile of 128 bags:
 //   1. the tile's 129 offsets go to shared memory; each warp streams the contiguous positions of
 //      its 16 bags with four 16-byte id loads in flight per lane, walking the bag boundaries
 //      forward, and for ids among the first 256 of their bag counts them with 32-bit
@@ -230,7 +231,6 @@ __global__ void __launch_bounds__(kThreads, 4) hist_tc_kernel(HistArgs a) {
     s_failed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -572,29 +572,47 @@ __global__ void __launch_bounds__(kThreads, 2) hist_bwd_kernel(HistBwdArgs a) {
       *reinterpret_cast<uint4*>(b_tile + kmajor_offset_bwd(e, kb)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     // 2b. A operands: element (column d, bag k) of each bf16 part of the gradient
-    for (int task = warp; task < (kBM / kWarp) * (kBK / 8); task += kThreads / kWarp) {
-      const int d = (task % (kBM / kWarp)) * kWarp + lane;
-      const int kb = (task / (kBM / kWarp)) * 8;
-      float g[8];
+    //     A warp loads the gradient values of all its core-matrix rows (four per warp: 32 per
+    //     lane in flight) before splitting and writing any of them.
+    {
+      constexpr int NT = (kBM / kWarp) * (kBK / 8);  // 16-byte core-matrix rows per part
+      constexpr int NW = kThreads / kWarp;
+      constexpr int TPASS = (NT + NW - 1) / NW;
+      for (int t0 = warp; t0 < NT; t0 += TPASS * NW) {
+        float g[TPASS][8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int k = kb + j;
-        g[j] = (d < a.D && k < nb) ? __ldg(a.grad_out + (b0 + k) * a.total_D + a.col0 + d) : 0.f;
-      }
-      uint32_t hw[4], mw[4], lw[4];
+        for (int p = 0; p < TPASS; ++p) {
+          const int task = t0 + p * NW;
+          const int d = (task % (kBM / kWarp)) * kWarp + lane;
+          const int kb = (task / (kBM / kWarp)) * 8;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t h0, m0, l0, h1, m1, l1;
-        split3(g[2 * j], h0, m0, l0);
-        split3(g[2 * j + 1], h1, m1, l1);
-        hw[j] = h0 | (h1 << 16);
-        mw[j] = m0 | (m1 << 16);
-        lw[j] = l0 | (l1 << 16);
+          for (int j = 0; j < 8; ++j) {
+            const int k = kb + j;
+            g[p][j] = (task < NT && d < a.D && k < nb) ? __ldg(a.grad_out + (b0 + k) * a.total_D + a.col0 + d) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int p = 0; p < TPASS; ++p) {
+          const int task = t0 + p * NW;
+          if (task >= NT) break;
+          const int d = (task % (kBM / kWarp)) * kWarp + lane;
+          const int kb = (task / (kBM / kWarp)) * 8;
+          uint32_t hw[4], mw[4], lw[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t h0, m0, l0, h1, m1, l1;
+            split3(g[p][2 * j], h0, m0, l0);
+            split3(g[p][2 * j + 1], h1, m1, l1);
+            hw[j] = h0 | (h1 << 16);
+            mw[j] = m0 | (m1 << 16);
+            lw[j] = l0 | (l1 << 16);
+          }
+          const uint32_t off = kmajor_offset_bwd(d, kb);
+          *reinterpret_cast<uint4*>(a_tiles + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(a_tiles + kBATile + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+          *reinterpret_cast<uint4*>(a_tiles + 2 * kBATile + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
       }
-      const uint32_t off = kmajor_offset_bwd(d, kb);
-      *reinterpret_cast<uint4*>(a_tiles + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(a_tiles + kBATile + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
-      *reinterpret_cast<uint4*>(a_tiles + 2 * kBATile + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
