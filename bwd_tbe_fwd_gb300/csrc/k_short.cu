@@ -7,9 +7,10 @@
 //
 // GB300 design: one group of min(32, D/4) lanes per run (a warp holds 32/group runs of a narrow
 // bucket); each lane owns float4 slices of the row; the run's weight row and state are fetched
-// before its gradient rows; the group walks the run's sorted bags, broadcasting them by shuffle,
-// with 4 gradient rows in flight; the optimizer runs in registers and the row is written with
-// plain stores.
+// before its gradient rows (and, for unweighted tables, the next claimed run's record meanwhile);
+// the group walks the run's sorted bags, broadcasting them by shuffle, in batches of up to 4
+// gradient rows that never run past the run; the optimizer runs in registers and the row is
+// written with plain stores.
 #include "k_update_common.cuh"
 
 namespace tbe {
@@ -26,7 +27,6 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
                                                             const float* __restrict__ sorted_psw) {
   using Acc = typename WTraits<WT>::Acc;
   constexpr int GPW = kWarp / LPR;  // runs per warp
-  constexpr int UNROLL = 4;  // gradient rows in flight per run
   const int lane = lane_id();
   const int g = lane / LPR, li = lane % LPR;
   const unsigned gmask = LPR == kWarp ? FULL : (((1u << LPR) - 1u) << (g * LPR));
@@ -117,11 +117,12 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
         if (FAC == FAC_INV_LEN && my_b != kNoBag) my_w = __ldg(c.inv_len + static_cast<int64_t>(t) * c.B + my_b);
       }
       const int steps = static_cast<int>(min(static_cast<uint32_t>(LPR), maxlen - j0));
-      for (int q0 = 0; q0 < steps; q0 += UNROLL) {
-        float4 v[UNROLL][VPL];
-        float w[UNROLL];
+      auto rows = [&](auto uc, int q0) {
+        constexpr int U = decltype(uc)::value;
+        float4 v[U][VPL];
+        float w[U];
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
+        for (int u = 0; u < U; ++u) {
           const int src = g * LPR + ((q0 + u) & (LPR - 1));
           const uint32_t b = __shfl_sync(FULL, my_b, src);
           const bool ok = b != kNoBag && q0 + u < steps;
@@ -135,9 +136,9 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
         // the factors after the row loads: with FAC_INV_LEN each one is a load that depends on
         // the bag, which must not hold the row loads back
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) w[u] = PSW ? __shfl_sync(FULL, my_w, g * LPR + ((q0 + u) & (LPR - 1))) : 1.f;
+        for (int u = 0; u < U; ++u) w[u] = PSW ? __shfl_sync(FULL, my_w, g * LPR + ((q0 + u) & (LPR - 1))) : 1.f;
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u)
+        for (int u = 0; u < U; ++u)
 #pragma unroll
           for (int jj = 0; jj < VPL; ++jj) {
             const Acc wu = static_cast<Acc>(w[u]);
@@ -146,6 +147,17 @@ __global__ void __launch_bounds__(kThreads) short_run_kernel(BwdCtx c, int bucke
             acc[jj][2] += PSW ? static_cast<Acc>(v[u][jj].z) * wu : static_cast<Acc>(v[u][jj].z);
             acc[jj][3] += PSW ? static_cast<Acc>(v[u][jj].w) * wu : static_cast<Acc>(v[u][jj].w);
           }
+      };
+      // Rows in flight: most runs are a few lookups long, so a batch must not carry steps past the
+      // run.  Unweighted tables take batches of 4 while 4 remain, then 2, then 1; with per-lookup
+      // factors batches of 2 (the factor loads' registers) measured faster.
+      int q0 = 0;
+      if constexpr (PSW) {
+        for (; q0 < steps; q0 += 2) rows(std::integral_constant<int, 2>{}, q0);
+      } else {
+        for (; q0 + 4 <= steps; q0 += 4) rows(std::integral_constant<int, 4>{}, q0);
+        for (; q0 + 2 <= steps; q0 += 2) rows(std::integral_constant<int, 2>{}, q0);
+        if (q0 < steps) rows(std::integral_constant<int, 1>{}, q0);
       }
     }
     if (len > 0) apply_row_prefetched<WT, OPT, Acc, VPL>(wrow, c.state + key, s_old, wv, acc, li, LPR, nv, D,
