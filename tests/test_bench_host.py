@@ -46,6 +46,20 @@ def test_byte_model_counts_and_histogram_split():
         assert m[k] >= 0
 
 
+def test_byte_model_with_the_forward_counts_reused():
+    """With the forward's counts reused, the counts-path forward also writes 128 bytes per bag
+    and the backward reads those instead of the table's ids; nothing else changes."""
+    cfg = get_config("c4").shrink(B=512, E_div=100)
+    st = bench.batch_stats(cfg, make_batch(cfg))
+    m0 = bench.byte_model(cfg, st)
+    m1 = bench.byte_model(cfg, st, reuse_counts=True)
+    ids0 = int(st["per_table"][0]) * 8
+    assert m1["histogram"] - m0["histogram"] == cfg.B * 128
+    assert m0["bwd_histogram"] - m1["bwd_histogram"] == ids0 - cfg.B * 128
+    for k in ("gather", "expand", "sort", "rle", "classify", "short", "long", "lookups_histogram"):
+        assert m0[k] == m1[k], k
+
+
 def test_reference_arm_prints_one_line():
     env = dict(os.environ, PYTHONPATH=ROOT)
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "c1",
