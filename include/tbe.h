@@ -171,8 +171,10 @@ typedef struct {
   int32_t nvtx;               /* 1: NVTX ranges (host side, one per stage: "tbe_forward.gather",
                                  "tbe_backward.sort", ...) around each stage's launches, for
                                  timeline tools; 0 (the default): none */
-  const void* forward_ws;     /* tbe_backward_update only.  NULL (the default), or the workspace
-                                 (16-byte aligned) of the tbe_forward call on the same batch --
+  const void* forward_ws;     /* Read by tbe_backward_update and tbe_backward_update_noalloc;
+                                 every entry point rejects one that is not 16-byte aligned
+                                 (TBE_ERR_INVALID_ARG).  NULL (the default), or the workspace
+                                 of the tbe_forward call on the same batch --
                                  the same problem and options, indices and offsets, ids not
                                  changed in between -- which saved there the per-bag counts of
                                  the counts x table tables ([FBT] section 2, "Forward-state
